@@ -1,0 +1,1441 @@
+// Host side of libdllm: models, decoding states, the denoise-step pipeline and
+// the C ABI of include/dllm.h.
+//
+// One denoise step (Algorithm 1, steps 5-10 of the Fast-dLLM notes) is a chain
+// of kernels on the state's stream, each launched with programmatic dependent
+// launch so the next weight stream starts while the previous kernel drains:
+//   embed -> per layer [QKV+RoPE+K/V write, attention, O-proj+residual+norm,
+//   gate/up+SwiGLU, down+residual+norm] -> LM head + softmax statistics ->
+//   merge + select/commit.
+// The only device->host traffic of a step is the committed count per sequence.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/dllm.h"
+#include "launch.h"
+#include "small_kernels.cuh"
+
+using namespace dllm;
+
+// ====================================================================== errors
+namespace {
+
+thread_local char g_err[2048] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+#define CK(call)                                                                                   \
+  do {                                                                                             \
+    cudaError_t e_ = (call);                                                                       \
+    if (e_ != cudaSuccess) {                                                                       \
+      set_error("%s:%d %s: %s", __FILE__, __LINE__, #call, cudaGetErrorString(e_));                \
+      return DLLM_ECUDA;                                                                           \
+    }                                                                                              \
+  } while (0)
+
+#define CKS(expr)                         \
+  do {                                    \
+    dllm_status s_ = (expr);              \
+    if (s_ != DLLM_OK) return s_;         \
+  } while (0)
+
+// Host-side fault injection for tests: DLLM_FAULT=alloc makes device
+// allocations fail, DLLM_FAULT=io makes weight-file reads fail.
+bool fault(const char* what) {
+  const char* f = std::getenv("DLLM_FAULT");
+  return f && std::strcmp(f, what) == 0;
+}
+
+dllm_status dev_alloc(void** p, size_t bytes) {
+  *p = nullptr;
+  if (fault("alloc")) {
+    set_error("device allocation of %zu bytes refused (DLLM_FAULT=alloc)", bytes);
+    return DLLM_ENOMEM;
+  }
+  if (bytes == 0) bytes = 256;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    set_error("cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+    return e == cudaErrorMemoryAllocation ? DLLM_ENOMEM : DLLM_ECUDA;
+  }
+  return DLLM_OK;
+}
+
+// ====================================================================== tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows][inner] matrix, box [box_rows][64], 128-byte swizzle.
+dllm_status map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return DLLM_ECUDA;
+  }
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled(2d, inner=%llu rows=%llu box_rows=%u) failed: %d",
+              (unsigned long long)inner, (unsigned long long)rows, box_rows, (int)r);
+    return DLLM_ECUDA;
+  }
+  return DLLM_OK;
+}
+
+// 3-D bf16 map over [planes][T][hd] (K or V planes of the cache), box [1][64][64].
+dllm_status map_kv(CUtensorMap* m, const void* base, uint64_t hd, uint64_t T, uint64_t planes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return DLLM_ECUDA;
+  }
+  cuuint64_t dims[3] = {hd, T, planes};
+  cuuint64_t strides[2] = {hd * 2, T * hd * 2};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled(3d kv) failed: %d", (int)r);
+    return DLLM_ECUDA;
+  }
+  return DLLM_OK;
+}
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+int pick_bn(int n) {
+  if (n <= 32) return 32;
+  if (n <= 64) return 64;
+  if (n <= 128) return 128;
+  return 256;
+}
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
+}
+
+struct AttnPlan {
+  int wq, q_tiles, splits, kps;
+};
+
+AttnPlan plan_attention(int b, int H, int R, int T, int sms) {
+  AttnPlan a;
+  a.wq = R <= 32 ? 2 : 4;
+  const int QT = 16 * a.wq;
+  a.q_tiles = ceil_div(R, QT);
+  const long long items = (long long)b * H * a.q_tiles;
+  const int max_splits = std::max(1, ceil_div(T, 64));
+  int splits = 1;
+  const long long target = 3LL * sms;
+  if (items < target) splits = std::min<long long>(max_splits, (target + items - 1) / items);
+  a.kps = round_up(ceil_div(T, splits), 64);
+  a.splits = ceil_div(T, a.kps);
+  return a;
+}
+
+}  // namespace
+
+// ====================================================================== model
+struct LayerW {
+  uint16_t *attn_norm, *wqkv, *wo, *ffn_norm, *wgu, *wd;
+  CUtensorMap tm_qkv, tm_o, tm_gu, tm_d;
+};
+
+struct dllm_model {
+  dllm_config cfg;
+  int F_pad;
+  int sms;
+  void* arena = nullptr;
+  size_t arena_bytes = 0;
+  uint16_t *embed = nullptr, *final_norm = nullptr, *lm = nullptr;
+  std::vector<LayerW> layers;
+  CUtensorMap tm_lm;
+};
+
+namespace {
+
+dllm_status check_config(const dllm_config* c) {
+  if (!c) {
+    set_error("config is NULL");
+    return DLLM_EINVAL;
+  }
+  if (c->n_layers < 1 || c->d_model < 128 || c->d_model % 128 != 0 || c->n_heads < 1 ||
+      (c->head_dim != 64 && c->head_dim != 128) || c->n_heads * c->head_dim != c->d_model || c->d_ffn < 1 ||
+      c->vocab < 2 || c->d_model > 8192 || !(c->rope_theta > 0) || !(c->norm_eps >= 0)) {
+    set_error("unsupported config: layers=%d d=%d heads=%d head_dim=%d ffn=%d vocab=%d (need d %% 128 == 0, "
+              "head_dim 64|128, heads*head_dim == d, d <= 8192)",
+              c->n_layers, c->d_model, c->n_heads, c->head_dim, c->d_ffn, c->vocab);
+    return DLLM_EINVAL;
+  }
+  return DLLM_OK;
+}
+
+}  // namespace
+
+extern "C" dllm_status dllm_model_create(const dllm_config* cfg, dllm_model** out) {
+  if (!out) {
+    set_error("out is NULL");
+    return DLLM_EINVAL;
+  }
+  *out = nullptr;
+  CKS(check_config(cfg));
+  dllm_model* m = new dllm_model();
+  m->cfg = *cfg;
+  m->F_pad = round_up(cfg->d_ffn, 64);
+  m->sms = device_sms();
+  const size_t d = cfg->d_model, F = m->F_pad, V = cfg->vocab, L = cfg->n_layers;
+  auto al = [](size_t bytes) { return (bytes + 1023) / 1024 * 1024; };
+  const size_t per_layer = al(d * 2) * 2 + al(3 * d * d * 2) + al(d * d * 2) + al(2 * F * d * 2) + al(d * F * 2);
+  m->arena_bytes = al((V + 1) * d * 2) + al(d * 2) + al(V * d * 2) + L * per_layer;
+  dllm_status st = dev_alloc(&m->arena, m->arena_bytes);
+  if (st != DLLM_OK) {
+    delete m;
+    return st;
+  }
+  cudaError_t e = cudaMemset(m->arena, 0, m->arena_bytes);
+  if (e != cudaSuccess) {
+    cudaFree(m->arena);
+    delete m;
+    set_error("cudaMemset of the weight arena failed: %s", cudaGetErrorString(e));
+    return DLLM_ECUDA;
+  }
+  uint8_t* p = static_cast<uint8_t*>(m->arena);
+  auto take = [&](size_t bytes) {
+    uint16_t* r = reinterpret_cast<uint16_t*>(p);
+    p += al(bytes);
+    return r;
+  };
+  m->embed = take((V + 1) * d * 2);
+  m->final_norm = take(d * 2);
+  m->lm = take(V * d * 2);
+  m->layers.resize(L);
+  for (size_t l = 0; l < L; ++l) {
+    LayerW& w = m->layers[l];
+    w.attn_norm = take(d * 2);
+    w.ffn_norm = take(d * 2);
+    w.wqkv = take(3 * d * d * 2);
+    w.wo = take(d * d * 2);
+    w.wgu = take(2 * F * d * 2);
+    w.wd = take(d * F * 2);
+    if ((st = map_2d(&w.tm_qkv, w.wqkv, d, 3 * d, 128)) != DLLM_OK ||
+        (st = map_2d(&w.tm_o, w.wo, d, d, 128)) != DLLM_OK ||
+        (st = map_2d(&w.tm_gu, w.wgu, d, 2 * F, 128)) != DLLM_OK ||
+        (st = map_2d(&w.tm_d, w.wd, F, d, 128)) != DLLM_OK) {
+      cudaFree(m->arena);
+      delete m;
+      return st;
+    }
+  }
+  if ((st = map_2d(&m->tm_lm, m->lm, d, V, 128)) != DLLM_OK) {
+    cudaFree(m->arena);
+    delete m;
+    return st;
+  }
+  *out = m;
+  return DLLM_OK;
+}
+
+extern "C" void dllm_free_model(dllm_model* m) {
+  if (!m) return;
+  if (m->arena) cudaFree(m->arena);
+  delete m;
+}
+
+extern "C" dllm_status dllm_model_config(const dllm_model* m, dllm_config* cfg) {
+  if (!m || !cfg) {
+    set_error("NULL argument");
+    return DLLM_EINVAL;
+  }
+  *cfg = m->cfg;
+  return DLLM_OK;
+}
+
+namespace {
+
+int64_t tensor_count(const dllm_config& c, int t) {
+  const int64_t d = c.d_model, F = c.d_ffn, V = c.vocab;
+  switch (t) {
+    case DLLM_T_EMBED: return (V + 1) * d;
+    case DLLM_T_ATTN_NORM:
+    case DLLM_T_FFN_NORM:
+    case DLLM_T_FINAL_NORM: return d;
+    case DLLM_T_WQ:
+    case DLLM_T_WK:
+    case DLLM_T_WV:
+    case DLLM_T_WO: return d * d;
+    case DLLM_T_WG:
+    case DLLM_T_WU:
+    case DLLM_T_WD: return F * d;
+    case DLLM_T_LM_HEAD: return V * d;
+    default: return -1;
+  }
+}
+
+}  // namespace
+
+extern "C" dllm_status dllm_model_set_tensor(dllm_model* m, int32_t tensor, int32_t layer, const uint16_t* src,
+                                             int64_t count, int32_t src_on_device) {
+  if (!m || !src) {
+    set_error("NULL argument");
+    return DLLM_EINVAL;
+  }
+  const dllm_config& c = m->cfg;
+  const int64_t want = tensor_count(c, tensor);
+  if (want < 0) {
+    set_error("unknown tensor id %d", tensor);
+    return DLLM_EINVAL;
+  }
+  const bool per_layer = tensor >= DLLM_T_ATTN_NORM && tensor <= DLLM_T_WD;
+  if (per_layer && (layer < 0 || layer >= c.n_layers)) {
+    set_error("layer %d out of range [0, %d)", layer, c.n_layers);
+    return DLLM_EINVAL;
+  }
+  if (count != want) {
+    set_error("tensor %d expects %lld values, got %lld", tensor, (long long)want, (long long)count);
+    return DLLM_EINVAL;
+  }
+  const cudaMemcpyKind kind = src_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+  const size_t d = c.d_model, F = c.d_ffn, Fp = m->F_pad;
+  LayerW* w = per_layer ? &m->layers[layer] : nullptr;
+  switch (tensor) {
+    case DLLM_T_EMBED: CK(cudaMemcpy(m->embed, src, count * 2, kind)); break;
+    case DLLM_T_FINAL_NORM: CK(cudaMemcpy(m->final_norm, src, count * 2, kind)); break;
+    case DLLM_T_LM_HEAD: CK(cudaMemcpy(m->lm, src, count * 2, kind)); break;
+    case DLLM_T_ATTN_NORM: CK(cudaMemcpy(w->attn_norm, src, count * 2, kind)); break;
+    case DLLM_T_FFN_NORM: CK(cudaMemcpy(w->ffn_norm, src, count * 2, kind)); break;
+    case DLLM_T_WQ:
+    case DLLM_T_WK:
+    case DLLM_T_WV:
+      CK(cudaMemcpy(w->wqkv + (size_t)(tensor - DLLM_T_WQ) * d * d, src, count * 2, kind));
+      break;
+    case DLLM_T_WO: CK(cudaMemcpy(w->wo, src, count * 2, kind)); break;
+    case DLLM_T_WG:
+    case DLLM_T_WU: {
+      // gate/up interleaved in 64-row groups: rows [128i, 128i+64) gate, [128i+64, 128i+128) up
+      const size_t off = tensor == DLLM_T_WU ? 64 : 0;
+      for (size_t f0 = 0; f0 < F; f0 += 64) {
+        const size_t rows = std::min<size_t>(64, F - f0);
+        CK(cudaMemcpy(w->wgu + ((f0 / 64) * 128 + off) * d, src + f0 * d, rows * d * 2, kind));
+      }
+      break;
+    }
+    case DLLM_T_WD:
+      CK(cudaMemcpy2D(w->wd, Fp * 2, src, F * 2, F * 2, d, kind));
+      break;
+    default: set_error("unknown tensor"); return DLLM_EINVAL;
+  }
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_load(const char* path, dllm_model** out) {
+  if (!path || !out) {
+    set_error("NULL argument");
+    return DLLM_EINVAL;
+  }
+  *out = nullptr;
+  if (fault("io")) {
+    set_error("weight file read refused (DLLM_FAULT=io)");
+    return DLLM_EIO;
+  }
+  FILE* fh = std::fopen(path, "rb");
+  if (!fh) {
+    set_error("cannot open %s", path);
+    return DLLM_EIO;
+  }
+  char magic[8];
+  int32_t hdr[6];
+  float flt[2];
+  if (std::fread(magic, 1, 8, fh) != 8 || std::memcmp(magic, "DLLMW001", 8) != 0 ||
+      std::fread(hdr, 4, 6, fh) != 6 || std::fread(flt, 4, 2, fh) != 2) {
+    std::fclose(fh);
+    set_error("%s: bad header", path);
+    return DLLM_EIO;
+  }
+  dllm_config c{hdr[0], hdr[1], hdr[2], hdr[3], hdr[4], hdr[5], flt[0], flt[1]};
+  dllm_model* m = nullptr;
+  dllm_status st = dllm_model_create(&c, &m);
+  if (st != DLLM_OK) {
+    std::fclose(fh);
+    return st;
+  }
+  std::vector<int> order;
+  std::vector<int> layers;
+  order.push_back(DLLM_T_EMBED);
+  layers.push_back(0);
+  const int per[] = {DLLM_T_ATTN_NORM, DLLM_T_WQ, DLLM_T_WK, DLLM_T_WV, DLLM_T_WO,
+                     DLLM_T_FFN_NORM, DLLM_T_WG, DLLM_T_WU, DLLM_T_WD};
+  for (int l = 0; l < c.n_layers; ++l)
+    for (int t : per) {
+      order.push_back(t);
+      layers.push_back(l);
+    }
+  order.push_back(DLLM_T_FINAL_NORM);
+  layers.push_back(0);
+  order.push_back(DLLM_T_LM_HEAD);
+  layers.push_back(0);
+  std::vector<uint16_t> buf;
+  for (size_t i = 0; i < order.size(); ++i) {
+    const int64_t n = tensor_count(c, order[i]);
+    buf.resize(n);
+    if ((int64_t)std::fread(buf.data(), 2, n, fh) != n) {
+      std::fclose(fh);
+      dllm_free_model(m);
+      set_error("%s: file ends inside tensor %d (layer %d)", path, order[i], layers[i]);
+      return DLLM_EIO;
+    }
+    st = dllm_model_set_tensor(m, order[i], layers[i], buf.data(), n, 0);
+    if (st != DLLM_OK) {
+      std::fclose(fh);
+      dllm_free_model(m);
+      return st;
+    }
+  }
+  std::fclose(fh);
+  *out = m;
+  return DLLM_OK;
+}
+
+// ====================================================================== state
+enum KClass { KC_EMBED = 0, KC_QKV, KC_ATTN, KC_O, KC_GU, KC_D, KC_LM, KC_MERGE, KC_N };
+
+struct dllm_state {
+  dllm_model* m = nullptr;
+  int b = 0, P = 0, gen = 0, B = 0, T = 0, n_blocks = 0;
+  cudaStream_t st = nullptr;
+  bool own_stream = false;
+  void* arena = nullptr;
+  int32_t* x = nullptr;
+  uint16_t* kv = nullptr;
+  float* h = nullptr;
+  uint16_t* xn = nullptr;
+  float* ss = nullptr;
+  uint16_t* q = nullptr;
+  uint16_t* ao = nullptr;
+  uint16_t* act = nullptr;
+  uint16_t* xf = nullptr;
+  float* ssf = nullptr;
+  float *st_m = nullptr, *st_s = nullptr;
+  int* st_a = nullptr;
+  float* conf = nullptr;
+  int32_t* arg = nullptr;
+  int32_t* count_err = nullptr;   // [b] counts, then the error word
+  float* gemm_ws = nullptr;
+  int* gemm_cnt = nullptr;
+  float* attn_o = nullptr;
+  float* attn_ml = nullptr;
+  int* attn_cnt = nullptr;
+  float2* rope = nullptr;
+  int32_t* host_ce = nullptr;     // pinned copy of count_err
+  CUtensorMap tm_kv;
+  std::map<std::tuple<const void*, int, int, int>, CUtensorMap> act_maps;
+  std::vector<int32_t> prompts;   // host copy of the prompt part
+  std::vector<int32_t> remaining; // [b][n_blocks] MASK count per block
+  // last step
+  int last_row0 = 0, last_R = 0, last_blk = 0;
+  // trace
+  bool trace = false;
+  float* trace_buf = nullptr;
+  // per-kernel timing
+  bool timing = false;
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> pending;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_next = 0;
+  double kt_ms[KC_N] = {0};
+  long long kt_n[KC_N] = {0};
+  double kt_bytes[KC_N] = {0};
+  double pend_bytes[64] = {0};
+  cudaEvent_t ev_a = nullptr, ev_b = nullptr;
+};
+
+namespace {
+
+dllm_status state_free_device(dllm_state* s) {
+  if (s->arena) cudaFree(s->arena);
+  if (s->gemm_ws) cudaFree(s->gemm_ws);
+  if (s->trace_buf) cudaFree(s->trace_buf);
+  if (s->host_ce) cudaFreeHost(s->host_ce);
+  for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
+  if (s->ev_a) cudaEventDestroy(s->ev_a);
+  if (s->ev_b) cudaEventDestroy(s->ev_b);
+  if (s->own_stream && s->st) cudaStreamDestroy(s->st);
+  s->arena = nullptr;
+  s->gemm_ws = nullptr;
+  return DLLM_OK;
+}
+
+dllm_status upload_canvas(dllm_state* s) {
+  std::vector<int32_t> canvas((size_t)s->b * s->T, s->m->cfg.vocab);
+  for (int i = 0; i < s->b; ++i)
+    std::memcpy(&canvas[(size_t)i * s->T], &s->prompts[(size_t)i * s->P], sizeof(int32_t) * s->P);
+  CK(cudaMemcpyAsync(s->x, canvas.data(), canvas.size() * 4, cudaMemcpyHostToDevice, s->st));
+  CK(cudaStreamSynchronize(s->st));
+  return DLLM_OK;
+}
+
+void reset_counters(dllm_state* s) {
+  s->remaining.assign((size_t)s->b * s->n_blocks, s->B);
+}
+
+dllm_status check_prompts(const dllm_model* m, const int32_t* prompts, int b, int P) {
+  for (long long i = 0; i < (long long)b * P; ++i)
+    if (prompts[i] < 0 || prompts[i] >= m->cfg.vocab) {
+      set_error("prompt token %d at index %lld is outside [0, %d)", prompts[i], i, m->cfg.vocab);
+      return DLLM_EINVAL;
+    }
+  return DLLM_OK;
+}
+
+}  // namespace
+
+extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, int32_t b, int32_t P,
+                                         int32_t gen_len, int32_t block, void* stream, dllm_state** out) {
+  if (!m || !out) {
+    set_error("NULL argument");
+    return DLLM_EINVAL;
+  }
+  *out = nullptr;
+  if (b < 1 || P < 0 || gen_len < 0 || block < 1 || block > kMaxBlock || (gen_len > 0 && gen_len % block != 0) ||
+      (long long)P + gen_len < 1 || (long long)P + gen_len > (1 << 20)) {
+    set_error("bad shape: b=%d P=%d gen_len=%d block=%d (need b>=1, 1<=block<=%d, gen_len %% block == 0)", b, P,
+              gen_len, block, kMaxBlock);
+    return DLLM_EINVAL;
+  }
+  if (prompts) CKS(check_prompts(m, prompts, b, P));
+  const dllm_config& c = m->cfg;
+  dllm_state* s = new dllm_state();
+  s->m = m;
+  s->b = b;
+  s->P = P;
+  s->gen = gen_len;
+  s->B = block;
+  s->T = P + gen_len;
+  s->n_blocks = gen_len / block;
+  s->prompts.assign((size_t)b * P, 0);
+  if (prompts) std::memcpy(s->prompts.data(), prompts, sizeof(int32_t) * b * P);
+  reset_counters(s);
+
+  const size_t d = c.d_model, F = m->F_pad, V = c.vocab, L = c.n_layers, H = c.n_heads, hd = c.head_dim;
+  const size_t T = s->T, n_max = (size_t)b * T, n_lm = (size_t)b * block;
+  const size_t v_tiles = (V + 127) / 128, d_tiles = d / 128;
+  // fix-up counters: the largest tile grid of any GEMM of this state
+  auto nt = [&](size_t n) { return (n + pick_bn((int)n) - 1) / pick_bn((int)n); };
+  size_t cnt_n = std::max({(3 * d / 128) * nt(n_max), (2 * F / 128) * nt(n_max), (d / 128) * nt(n_max),
+                           v_tiles * nt(n_lm)});
+  // attention workspace: the largest plan among the row counts this state can use
+  size_t attn_floats = 0, attn_cnt = 0;
+  {
+    std::vector<int> Rs = {block, (int)T};
+    for (int j = 0; j < s->n_blocks; ++j) Rs.push_back((int)T - (P + j * block));
+    for (int R : Rs) {
+      if (R < 1) continue;
+      AttnPlan a = plan_attention(b, (int)H, R, (int)T, m->sms);
+      const size_t works = (size_t)b * H * a.q_tiles;
+      attn_floats = std::max(attn_floats, works * a.splits * 16 * a.wq * (hd + 2));
+      attn_cnt = std::max(attn_cnt, works);
+    }
+  }
+  auto al = [](size_t bytes) { return (bytes + 1023) / 1024 * 1024; };
+  size_t total = 0;
+  const size_t o_x = total; total += al(n_max * 4);
+  const size_t o_kv = total; total += al(L * 2 * b * H * T * hd * 2);
+  const size_t o_h = total; total += al(n_max * d * 4);
+  const size_t o_xn = total; total += al(n_max * d * 2);
+  const size_t o_ss = total; total += al(n_max * d_tiles * 4);
+  const size_t o_q = total; total += al(n_max * d * 2);
+  const size_t o_ao = total; total += al(n_max * d * 2);
+  const size_t o_act = total; total += al(n_max * F * 2);
+  const size_t o_xf = total; total += al(n_lm * d * 2);
+  const size_t o_ssf = total; total += al(n_lm * d_tiles * 4);
+  const size_t o_stm = total; total += al(v_tiles * n_lm * 4);
+  const size_t o_sts = total; total += al(v_tiles * n_lm * 4);
+  const size_t o_sta = total; total += al(v_tiles * n_lm * 4);
+  const size_t o_conf = total; total += al(n_lm * 4);
+  const size_t o_arg = total; total += al(n_lm * 4);
+  const size_t o_ce = total; total += al((b + 1) * 4);
+  const size_t o_gc = total; total += al(cnt_n * 4);
+  const size_t o_ao2 = total; total += al(attn_floats * 4);
+  const size_t o_ac = total; total += al(attn_cnt * 4);
+  const size_t o_rope = total; total += al(T * (hd / 2) * 8);
+
+  dllm_status st = dev_alloc(&s->arena, total);
+  if (st != DLLM_OK) {
+    delete s;
+    return st;
+  }
+  st = dev_alloc((void**)&s->gemm_ws, (size_t)m->sms * 2 * 256 * 128 * 4);
+  if (st != DLLM_OK) {
+    state_free_device(s);
+    delete s;
+    return st;
+  }
+  uint8_t* a = static_cast<uint8_t*>(s->arena);
+  s->x = reinterpret_cast<int32_t*>(a + o_x);
+  s->kv = reinterpret_cast<uint16_t*>(a + o_kv);
+  s->h = reinterpret_cast<float*>(a + o_h);
+  s->xn = reinterpret_cast<uint16_t*>(a + o_xn);
+  s->ss = reinterpret_cast<float*>(a + o_ss);
+  s->q = reinterpret_cast<uint16_t*>(a + o_q);
+  s->ao = reinterpret_cast<uint16_t*>(a + o_ao);
+  s->act = reinterpret_cast<uint16_t*>(a + o_act);
+  s->xf = reinterpret_cast<uint16_t*>(a + o_xf);
+  s->ssf = reinterpret_cast<float*>(a + o_ssf);
+  s->st_m = reinterpret_cast<float*>(a + o_stm);
+  s->st_s = reinterpret_cast<float*>(a + o_sts);
+  s->st_a = reinterpret_cast<int*>(a + o_sta);
+  s->conf = reinterpret_cast<float*>(a + o_conf);
+  s->arg = reinterpret_cast<int32_t*>(a + o_arg);
+  s->count_err = reinterpret_cast<int32_t*>(a + o_ce);
+  s->gemm_cnt = reinterpret_cast<int*>(a + o_gc);
+  s->attn_o = reinterpret_cast<float*>(a + o_ao2);
+  s->attn_ml = s->attn_o;   // carved per launch from the same block (see run_attention)
+  s->attn_cnt = reinterpret_cast<int*>(a + o_ac);
+  s->rope = reinterpret_cast<float2*>(a + o_rope);
+
+  auto fail = [&](dllm_status e) {
+    state_free_device(s);
+    delete s;
+    return e;
+  };
+  if (stream) {
+    s->st = static_cast<cudaStream_t>(stream);
+  } else {
+    if (cudaStreamCreateWithFlags(&s->st, cudaStreamNonBlocking) != cudaSuccess) {
+      set_error("cudaStreamCreate failed");
+      return fail(DLLM_ECUDA);
+    }
+    s->own_stream = true;
+  }
+  if (cudaMallocHost((void**)&s->host_ce, (b + 1) * 4) != cudaSuccess) {
+    cudaGetLastError();
+    set_error("cudaMallocHost failed");
+    return fail(DLLM_ENOMEM);
+  }
+  if (cudaEventCreate(&s->ev_a) != cudaSuccess || cudaEventCreate(&s->ev_b) != cudaSuccess) {
+    set_error("cudaEventCreate failed");
+    return fail(DLLM_ECUDA);
+  }
+  if (cudaMemsetAsync(s->arena, 0, total, s->st) != cudaSuccess) {
+    set_error("cudaMemset failed");
+    return fail(DLLM_ECUDA);
+  }
+  // RoPE table: angle = pos * theta^(-2j/hd), rotate-half pairs (j, j + hd/2)
+  {
+    std::vector<float2> cs(T * (hd / 2));
+    for (size_t pos = 0; pos < T; ++pos)
+      for (size_t j = 0; j < hd / 2; ++j) {
+        const double inv = std::pow((double)c.rope_theta, -2.0 * (double)j / (double)hd);
+        const double ang = (double)pos * inv;
+        cs[pos * (hd / 2) + j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    if (cudaMemcpyAsync(s->rope, cs.data(), cs.size() * 8, cudaMemcpyHostToDevice, s->st) != cudaSuccess) {
+      set_error("rope upload failed");
+      return fail(DLLM_ECUDA);
+    }
+    if (cudaStreamSynchronize(s->st) != cudaSuccess) {
+      set_error("stream sync failed");
+      return fail(DLLM_ECUDA);
+    }
+  }
+  if ((st = map_kv(&s->tm_kv, s->kv, hd, T, L * 2 * b * H)) != DLLM_OK) return fail(st);
+  if ((st = upload_canvas(s)) != DLLM_OK) return fail(st);
+  *out = s;
+  return DLLM_OK;
+}
+
+extern "C" void dllm_free_state(dllm_state* s) {
+  if (!s) return;
+  if (s->st) cudaStreamSynchronize(s->st);
+  state_free_device(s);
+  delete s;
+}
+
+extern "C" dllm_status dllm_state_reset(dllm_state* s, const int32_t* prompts) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  if (prompts) {
+    CKS(check_prompts(s->m, prompts, s->b, s->P));
+    std::memcpy(s->prompts.data(), prompts, sizeof(int32_t) * s->b * s->P);
+  }
+  reset_counters(s);
+  CK(cudaMemsetAsync(s->kv, 0, (size_t)s->m->cfg.n_layers * 2 * s->b * s->m->cfg.d_model * s->T * 2, s->st));
+  return upload_canvas(s);
+}
+
+namespace {
+
+__global__ void set_prompts_kernel(int32_t* x, const int32_t* prompts, int b, int P, int T, int mask) {
+  const long long n = (long long)b * T;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int seq = (int)(i / T), pos = (int)(i % T);
+    x[i] = pos < P ? prompts[(long long)seq * P + pos] : mask;
+  }
+}
+
+}  // namespace
+
+extern "C" dllm_status dllm_state_set_prompts_device(dllm_state* s, const int32_t* prompts_dev) {
+  if (!s || (!prompts_dev && s->P > 0)) {
+    set_error("NULL argument");
+    return DLLM_EINVAL;
+  }
+  reset_counters(s);
+  const long long n = (long long)s->b * s->T;
+  const int grid = (int)std::min<long long>((n + 255) / 256, 4096);
+  set_prompts_kernel<<<grid, 256, 0, s->st>>>(s->x, prompts_dev, s->b, s->P, s->T, s->m->cfg.vocab);
+  CK(cudaGetLastError());
+  return DLLM_OK;
+}
+
+// ====================================================================== pipeline
+namespace {
+
+cudaEvent_t next_event(dllm_state* s) {
+  if (s->ev_next == s->ev_pool.size()) {
+    cudaEvent_t e;
+    cudaEventCreate(&e);
+    s->ev_pool.push_back(e);
+  }
+  return s->ev_pool[s->ev_next++];
+}
+
+struct Timed {
+  dllm_state* s;
+  int cls;
+  double bytes;
+  cudaEvent_t e1 = nullptr;
+  Timed(dllm_state* s_, int c, double b) : s(s_), cls(c), bytes(b) {
+    if (s->timing) {
+      cudaEvent_t e0 = next_event(s);
+      e1 = next_event(s);
+      cudaEventRecord(e0, s->st);
+      s->pending.push_back({cls, {e0, e1}});
+      if (s->pending.size() <= 64) s->pend_bytes[s->pending.size() - 1] = bytes;
+    }
+  }
+  ~Timed() {
+    if (s->timing) cudaEventRecord(e1, s->st);
+  }
+};
+
+void collect_timing(dllm_state* s) {
+  for (size_t i = 0; i < s->pending.size(); ++i) {
+    float ms = 0.0f;
+    cudaEventElapsedTime(&ms, s->pending[i].second.first, s->pending[i].second.second);
+    const int c = s->pending[i].first;
+    s->kt_ms[c] += ms;
+    s->kt_n[c] += 1;
+  }
+  s->pending.clear();
+  s->ev_next = 0;
+}
+
+const CUtensorMap* act_map(dllm_state* s, const void* base, int K, int N, int BN, dllm_status* st) {
+  auto key = std::make_tuple(base, K, N, BN);
+  auto it = s->act_maps.find(key);
+  if (it != s->act_maps.end()) return &it->second;
+  CUtensorMap m;
+  *st = map_2d(&m, base, (uint64_t)K, (uint64_t)N, (uint32_t)BN);
+  if (*st != DLLM_OK) return nullptr;
+  return &(s->act_maps[key] = m);
+}
+
+dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int K, const uint16_t* X, int N,
+                     GemmParams p, int cls, double bytes) {
+  const int BN = pick_bn(N);
+  dllm_status st = DLLM_OK;
+  const CUtensorMap* tmB = act_map(s, X, K, N, BN, &st);
+  if (!tmB) return st;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = ceil_div(M, 128);
+  p.n_tiles = ceil_div(N, BN);
+  p.kc = ceil_div(K, 64);
+  p.total = (long long)p.m_tiles * p.n_tiles * p.kc;
+  p.ws = s->gemm_ws;
+  p.counters = s->gemm_cnt;
+  p.err = s->count_err + s->b;
+  const int grid = (int)std::min<long long>(s->m->sms, p.total);
+  if (s->timing) s->kt_bytes[cls] += bytes;
+  Timed t(s, cls, bytes);
+  CK(launch_gemm(kind, BN, tmA, *tmB, p, grid, s->st, true));
+  return DLLM_OK;
+}
+
+dllm_status run_attention(dllm_state* s, int layer, int R, double bytes) {
+  const dllm_config& c = s->m->cfg;
+  AttnPlan a = plan_attention(s->b, c.n_heads, R, s->T, s->m->sms);
+  const int QT = 16 * a.wq;
+  const long long works = (long long)s->b * c.n_heads * a.q_tiles;
+  AttnParams p;
+  p.q = s->q;
+  p.o = s->ao;
+  p.R = R;
+  p.b = s->b;
+  p.H = c.n_heads;
+  p.T = s->T;
+  p.z_k0 = (layer * 2 + 0) * s->b * c.n_heads;
+  p.z_v0 = (layer * 2 + 1) * s->b * c.n_heads;
+  p.q_tiles = a.q_tiles;
+  p.splits = a.splits;
+  p.kps = a.kps;
+  p.scale_log2 = kLog2e / std::sqrt((float)c.head_dim);
+  p.ws_o = s->attn_o;
+  p.ws_ml = s->attn_o + works * a.splits * QT * c.head_dim;
+  p.counters = s->attn_cnt;
+  p.err = s->count_err + s->b;
+  if (s->timing) s->kt_bytes[KC_ATTN] += bytes;
+  Timed t(s, KC_ATTN, bytes);
+  CK(launch_attention(c.head_dim, a.wq, s->tm_kv, s->tm_kv, p, dim3(a.splits, a.q_tiles * c.n_heads, s->b), s->st,
+                      true));
+  return DLLM_OK;
+}
+
+// Forward over rows [row0, row0 + R) of every sequence.  refresh: write K/V
+// only (stop after the last layer's QKV).  Otherwise finish with the LM head
+// on the block rows [blk, blk + B) and select/commit with `rule`.
+dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, const SelectRule& rule) {
+  const dllm_model* m = s->m;
+  const dllm_config& c = m->cfg;
+  const int d = c.d_model, L = c.n_layers, F = m->F_pad, V = c.vocab;
+  const int n = s->b * R, n_lm = s->b * s->B;
+  const double wb = 2.0;  // bf16
+  s->last_row0 = row0;
+  s->last_R = R;
+  s->last_blk = blk;
+  {
+    EmbedParams e{s->x, m->embed, m->layers[0].attn_norm, s->h, s->xn, s->ss, d, R, row0, s->T};
+    Timed t(s, KC_EMBED, (double)n * d * (2 + 4 + 2));
+    if (s->timing) s->kt_bytes[KC_EMBED] += (double)n * d * 8;
+    CK(launch_ex(embed_kernel, dim3(n), dim3(d / 8), 0, s->st, true, e));
+  }
+  if (s->trace) CK(cudaMemcpyAsync(s->trace_buf, s->h, (size_t)n * d * 4, cudaMemcpyDeviceToDevice, s->st));
+  const double kv_bytes = (double)s->b * s->T * d * 2 * 2;
+  for (int l = 0; l < L; ++l) {
+    const LayerW& w = m->layers[l];
+    const bool last = l == L - 1;
+    GemmParams p = {};
+    p.ss_in = s->ss;
+    p.ss_in_tiles = d / 128;
+    p.inv_d = 1.0f / d;
+    p.eps = c.norm_eps;
+    p.R = R;
+    p.row0 = row0;
+    p.q_out = s->q;
+    p.kv = s->kv;
+    p.rope_cs = s->rope;
+    p.d_model = d;
+    p.head_dim = c.head_dim;
+    p.n_heads = c.n_heads;
+    p.T_pad = s->T;
+    p.b_seqs = s->b;
+    p.layer = l;
+    CKS(run_gemm(s, GEMM_QKV, w.tm_qkv, 3 * d, d, s->xn, n, p, KC_QKV,
+                 3.0 * d * d * wb + (double)n * d * wb * 4));
+    if (refresh && last) break;
+    CKS(run_attention(s, l, R, kv_bytes + (double)n * d * wb * 2));
+    GemmParams o = {};
+    o.R = R;
+    o.row0 = row0;
+    o.d_model = d;
+    o.h = s->h;
+    o.g_next = w.ffn_norm;
+    o.xn_out = s->xn;
+    o.ss_out = s->ss;
+    CKS(run_gemm(s, GEMM_RESID, w.tm_o, d, d, s->ao, n, o, KC_O,
+                 (double)d * d * wb + (double)n * d * (wb + 8 + wb)));
+    GemmParams gu = {};
+    gu.ss_in = s->ss;
+    gu.ss_in_tiles = d / 128;
+    gu.inv_d = 1.0f / d;
+    gu.eps = c.norm_eps;
+    gu.act = s->act;
+    gu.act_ld = F;
+    CKS(run_gemm(s, GEMM_SWIGLU, w.tm_gu, 2 * F, d, s->xn, n, gu, KC_GU,
+                 2.0 * F * d * wb + (double)n * (d + F) * wb));
+    GemmParams dn = {};
+    dn.R = R;
+    dn.row0 = row0;
+    dn.d_model = d;
+    dn.h = s->h;
+    if (last) {
+      dn.g_next = m->final_norm;
+      dn.xn_out = s->xf;
+      dn.ss_out = s->ssf;
+      dn.remap = 1;
+      dn.blk_start = blk;
+      dn.blk_len = s->B;
+    } else {
+      dn.g_next = m->layers[l + 1].attn_norm;
+      dn.xn_out = s->xn;
+      dn.ss_out = s->ss;
+    }
+    CKS(run_gemm(s, GEMM_RESID, w.tm_d, d, F, s->act, n, dn, KC_D,
+                 (double)d * F * wb + (double)n * (F * wb + 8.0 * d + wb * d)));
+    if (s->trace)
+      CK(cudaMemcpyAsync(s->trace_buf + (size_t)(l + 1) * n * d, s->h, (size_t)n * d * 4, cudaMemcpyDeviceToDevice,
+                         s->st));
+  }
+  if (refresh) return DLLM_OK;
+  GemmParams lm = {};
+  lm.ss_in = s->ssf;
+  lm.ss_in_tiles = d / 128;
+  lm.inv_d = 1.0f / d;
+  lm.eps = c.norm_eps;
+  lm.st_m = s->st_m;
+  lm.st_s = s->st_s;
+  lm.st_a = s->st_a;
+  CKS(run_gemm(s, GEMM_LMHEAD, m->tm_lm, V, d, s->xf, n_lm, lm, KC_LM, (double)V * d * wb + (double)n_lm * d * wb));
+  MergeParams mp;
+  mp.st_m = s->st_m;
+  mp.st_s = s->st_s;
+  mp.st_a = s->st_a;
+  mp.v_tiles = ceil_div(V, 128);
+  mp.n_rows = n_lm;
+  mp.B = s->B;
+  mp.T = s->T;
+  mp.blk_start = blk;
+  mp.mask_id = V;
+  mp.x = s->x;
+  mp.conf = s->conf;
+  mp.arg = s->arg;
+  mp.count = s->count_err;
+  mp.rule = rule;
+  {
+    Timed t(s, KC_MERGE, (double)mp.v_tiles * n_lm * 12);
+    if (s->timing) s->kt_bytes[KC_MERGE] += (double)mp.v_tiles * n_lm * 12;
+    CK(launch_ex(merge_select_kernel, dim3(s->b), dim3(256), 0, s->st, true, mp));
+  }
+  return DLLM_OK;
+}
+
+dllm_status finish_sync(dllm_state* s) {
+  CK(cudaMemcpyAsync(s->host_ce, s->count_err, (s->b + 1) * 4, cudaMemcpyDeviceToHost, s->st));
+  CK(cudaStreamSynchronize(s->st));
+  if (s->timing) collect_timing(s);
+  if (s->host_ce[s->b] != 0) {
+    set_error("a kernel gave up a bounded wait (site %d); outputs are invalid", s->host_ce[s->b]);
+    return DLLM_ETIMEOUT;
+  }
+  return DLLM_OK;
+}
+
+dllm_status to_rule(const dllm_select* sel, SelectRule* r) {
+  if (!sel) {
+    set_error("selection rule is NULL");
+    return DLLM_EINVAL;
+  }
+  r->policy = sel->policy;
+  r->tau = sel->tau;
+  r->k = sel->k;
+  r->factor = sel->factor;
+  if (sel->policy < 0 || sel->policy > 3 || (sel->policy == 0 && std::isnan(sel->tau)) ||
+      (sel->policy == 1 && sel->k < 1) || (sel->policy == 2 && !(sel->factor > 0))) {
+    set_error("bad selection rule: policy=%d tau=%f k=%d factor=%f", sel->policy, sel->tau, sel->k, sel->factor);
+    return DLLM_EINVAL;
+  }
+  return DLLM_OK;
+}
+
+dllm_status do_refresh(dllm_state* s, cudaEvent_t e0 = nullptr, cudaEvent_t e1 = nullptr) {
+  if (s->T < 1) return DLLM_OK;
+  SelectRule none{0, 2.0f, 1, 1.0f};
+  if (e0) CK(cudaEventRecord(e0, s->st));
+  CK(cudaMemsetAsync(s->count_err + s->b, 0, 4, s->st));
+  CKS(run_forward(s, 0, s->T, true, 0, none));
+  if (e1) CK(cudaEventRecord(e1, s->st));
+  return finish_sync(s);
+}
+
+dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int32_t* committed, int* total,
+                    cudaEvent_t e0 = nullptr, cudaEvent_t e1 = nullptr) {
+  if (j < 0 || j >= s->n_blocks) {
+    set_error("block_idx %d outside [0, %d)", j, s->n_blocks);
+    return DLLM_EINVAL;
+  }
+  if (mode < 0 || mode > 2) {
+    set_error("bad cache mode %d", mode);
+    return DLLM_EINVAL;
+  }
+  const int blk = s->P + j * s->B;
+  int row0, R;
+  if (mode == DLLM_CACHE_DUAL) {
+    row0 = blk;
+    R = s->B;
+  } else if (mode == DLLM_CACHE_PREFIX) {
+    row0 = blk;
+    R = s->T - blk;
+  } else {
+    row0 = 0;
+    R = s->T;
+  }
+  if (e0) CK(cudaEventRecord(e0, s->st));
+  CK(cudaMemsetAsync(s->count_err, 0, (s->b + 1) * 4, s->st));
+  CKS(run_forward(s, row0, R, false, blk, rule));
+  if (e1) CK(cudaEventRecord(e1, s->st));
+  CKS(finish_sync(s));
+  int sum = 0;
+  for (int i = 0; i < s->b; ++i) {
+    const int cnt = s->host_ce[i];
+    int& rem = s->remaining[(size_t)i * s->n_blocks + j];
+    if (cnt > rem || (rem > 0 && cnt == 0)) {
+      set_error("sequence %d committed %d with %d MASK left in block %d", i, cnt, rem, j);
+      return DLLM_ESTATE;
+    }
+    rem -= cnt;
+    sum += cnt;
+    if (committed) committed[i] = cnt;
+  }
+  *total = sum;
+  return DLLM_OK;
+}
+
+}  // namespace
+
+extern "C" dllm_status dllm_prefill_refresh(dllm_state* s) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  return do_refresh(s);
+}
+
+extern "C" dllm_status dllm_denoise_step_ex(dllm_state* s, int32_t block_idx, const dllm_select* sel,
+                                           int32_t cache_mode, int32_t* committed) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  SelectRule r;
+  CKS(to_rule(sel, &r));
+  int total = 0;
+  return do_step(s, block_idx, r, cache_mode, committed, &total);
+}
+
+extern "C" int32_t dllm_denoise_step(dllm_state* s, int32_t block_idx, float tau, int32_t cache_mode,
+                                     int32_t* committed) {
+  if (!s) {
+    set_error("NULL state");
+    return -DLLM_EINVAL;
+  }
+  dllm_select sel{DLLM_SEL_THRESHOLD, tau, 1, 1.0f};
+  SelectRule r;
+  dllm_status st = to_rule(&sel, &r);
+  if (st != DLLM_OK) return -(int32_t)st;
+  int total = 0;
+  st = do_step(s, block_idx, r, cache_mode, committed, &total);
+  return st == DLLM_OK ? total : -(int32_t)st;
+}
+
+extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t cache_mode, int32_t refresh_interval,
+                                dllm_stats* stats) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  SelectRule r;
+  CKS(to_rule(sel, &r));
+  if (cache_mode < 0 || cache_mode > 2 || refresh_interval < 0) {
+    set_error("bad cache mode %d or refresh interval %d", cache_mode, refresh_interval);
+    return DLLM_EINVAL;
+  }
+  const auto t0 = std::chrono::steady_clock::now();
+  double refresh_ms = 0, step_ms = 0;
+  int steps = 0, refreshes = 0, max_spb = 0;
+  long long committed = 0, active = 0;
+  const bool cached = cache_mode != DLLM_CACHE_NONE;
+  std::vector<int32_t> cnt(s->b);
+  auto timed_refresh = [&]() -> dllm_status {
+    CKS(do_refresh(s, s->ev_a, s->ev_b));
+    float ms = 0;
+    CK(cudaEventElapsedTime(&ms, s->ev_a, s->ev_b));
+    refresh_ms += ms;
+    ++refreshes;
+    return DLLM_OK;
+  };
+  if (cached && s->n_blocks > 0) CKS(timed_refresh());
+  for (int j = 0; j < s->n_blocks; ++j) {
+    int spb = 0;
+    for (;;) {
+      int any = 0, act = 0;
+      for (int i = 0; i < s->b; ++i) {
+        const int rem = s->remaining[(size_t)i * s->n_blocks + j];
+        any |= rem > 0;
+        act += rem > 0;
+      }
+      if (!any) break;
+      if (cached && refresh_interval > 0 && spb > 0 && spb % refresh_interval == 0) CKS(timed_refresh());
+      int total = 0;
+      CKS(do_step(s, j, r, cache_mode, cnt.data(), &total, s->ev_a, s->ev_b));
+      float ms = 0;
+      CK(cudaEventElapsedTime(&ms, s->ev_a, s->ev_b));
+      step_ms += ms;
+      ++steps;
+      ++spb;
+      committed += total;
+      active += act;
+    }
+    max_spb = std::max(max_spb, spb);
+    if (cached && j + 1 < s->n_blocks) CKS(timed_refresh());
+  }
+  if (stats) {
+    stats->wall_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    stats->refresh_ms = refresh_ms;
+    stats->step_ms = step_ms;
+    stats->steps = steps;
+    stats->refreshes = refreshes;
+    stats->blocks = s->n_blocks;
+    stats->max_steps_per_block = max_spb;
+    stats->committed = committed;
+    stats->tau_bar = active > 0 ? (double)committed / (double)active : 0.0;
+  }
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_generate(dllm_model* m, const int32_t* prompts, int32_t b, int32_t P, int32_t gen_len,
+                                     int32_t block, float tau, int32_t cache_mode, int32_t* out_tokens,
+                                     dllm_stats* stats) {
+  if (!m || (!prompts && P > 0) || !out_tokens) {
+    set_error("NULL argument");
+    return DLLM_EINVAL;
+  }
+  const auto t0 = std::chrono::steady_clock::now();
+  dllm_state* s = nullptr;
+  std::vector<int32_t> empty;
+  CKS(dllm_state_create(m, prompts ? prompts : empty.data(), b, P, gen_len, block, nullptr, &s));
+  dllm_select sel{DLLM_SEL_THRESHOLD, tau, 1, 1.0f};
+  dllm_status st = dllm_run(s, &sel, cache_mode, 0, stats);
+  if (st == DLLM_OK && gen_len > 0) {
+    cudaError_t e = cudaMemcpy2DAsync(out_tokens, (size_t)gen_len * 4, s->x + P, (size_t)s->T * 4,
+                                      (size_t)gen_len * 4, b, cudaMemcpyDeviceToHost, s->st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s->st);
+    if (e != cudaSuccess) {
+      set_error("copying the answer back failed: %s", cudaGetErrorString(e));
+      st = DLLM_ECUDA;
+    }
+  }
+  dllm_free_state(s);
+  if (stats && st == DLLM_OK)
+    stats->wall_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  return st;
+}
+
+extern "C" dllm_status dllm_read_state(const dllm_state* s, int32_t* tokens, float* conf, int32_t* arg) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  CK(cudaStreamSynchronize(s->st));
+  if (tokens) CK(cudaMemcpy(tokens, s->x, (size_t)s->b * s->T * 4, cudaMemcpyDeviceToHost));
+  if (conf) CK(cudaMemcpy(conf, s->conf, (size_t)s->b * s->B * 4, cudaMemcpyDeviceToHost));
+  if (arg) CK(cudaMemcpy(arg, s->arg, (size_t)s->b * s->B * 4, cudaMemcpyDeviceToHost));
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_read_hidden(const dllm_state* s, float* h) {
+  if (!s || !h) {
+    set_error("NULL argument");
+    return DLLM_EINVAL;
+  }
+  const int d = s->m->cfg.d_model;
+  CK(cudaStreamSynchronize(s->st));
+  const int off = s->last_blk - s->last_row0;
+  if (off < 0 || off + s->B > s->last_R) {
+    set_error("no denoise step has run");
+    return DLLM_ESTATE;
+  }
+  for (int i = 0; i < s->b; ++i)
+    CK(cudaMemcpy(h + (size_t)i * s->B * d, s->h + ((size_t)i * s->last_R + off) * d, (size_t)s->B * d * 4,
+                  cudaMemcpyDeviceToHost));
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_read_kv(const dllm_state* s, int32_t layer, float* k, float* v) {
+  if (!s || layer < 0 || layer >= s->m->cfg.n_layers) {
+    set_error("bad argument");
+    return DLLM_EINVAL;
+  }
+  const dllm_config& c = s->m->cfg;
+  const size_t plane = (size_t)s->b * c.n_heads * s->T * c.head_dim;
+  std::vector<uint16_t> buf(plane);
+  CK(cudaStreamSynchronize(s->st));
+  for (int kvi = 0; kvi < 2; ++kvi) {
+    float* dst = kvi == 0 ? k : v;
+    if (!dst) continue;
+    CK(cudaMemcpy(buf.data(), s->kv + ((size_t)layer * 2 + kvi) * plane, plane * 2, cudaMemcpyDeviceToHost));
+    for (size_t i = 0; i < plane; ++i) {
+      uint32_t u = (uint32_t)buf[i] << 16;
+      std::memcpy(&dst[i], &u, 4);
+    }
+  }
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_trace(dllm_state* s, int32_t enable) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  if (enable && !s->trace_buf) {
+    const size_t n = (size_t)(s->m->cfg.n_layers + 1) * s->b * s->T * s->m->cfg.d_model * 4;
+    CKS(dev_alloc((void**)&s->trace_buf, n));
+  }
+  s->trace = enable != 0;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_read_trace(const dllm_state* s, float* out, int64_t capacity, int32_t* rows_per_seq,
+                                       int32_t* first_pos) {
+  if (!s || !s->trace_buf) {
+    set_error("tracing was never enabled");
+    return DLLM_ESTATE;
+  }
+  const size_t n = (size_t)s->b * s->last_R * s->m->cfg.d_model;
+  const size_t need = (size_t)(s->m->cfg.n_layers + 1) * n;
+  if (rows_per_seq) *rows_per_seq = s->last_R;
+  if (first_pos) *first_pos = s->last_row0;
+  if (!out) return DLLM_OK;
+  if ((size_t)capacity < need) {
+    set_error("trace needs %zu floats, capacity %lld", need, (long long)capacity);
+    return DLLM_EINVAL;
+  }
+  CK(cudaStreamSynchronize(s->st));
+  CK(cudaMemcpy(out, s->trace_buf, need * 4, cudaMemcpyDeviceToHost));
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_kernel_timing(dllm_state* s, int32_t enable) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  s->timing = enable != 0;
+  for (int i = 0; i < KC_N; ++i) {
+    s->kt_ms[i] = 0;
+    s->kt_n[i] = 0;
+    s->kt_bytes[i] = 0;
+  }
+  s->pending.clear();
+  s->ev_next = 0;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_kernel_times(const dllm_state* s, double* ms, int64_t* launches, double* bytes,
+                                         int32_t n) {
+  if (!s || n < 0) {
+    set_error("bad argument");
+    return DLLM_EINVAL;
+  }
+  for (int i = 0; i < n && i < KC_N; ++i) {
+    if (ms) ms[i] = s->kt_ms[i];
+    if (launches) launches[i] = s->kt_n[i];
+    if (bytes) bytes[i] = s->kt_bytes[i];
+  }
+  return DLLM_OK;
+}
+
+// ====================================================================== kernel-level ops
+namespace {
+
+struct OpWorkspace {
+  float* ws = nullptr;
+  int* cnt = nullptr;
+  size_t cnt_n = 0;
+  float* attn = nullptr;
+  size_t attn_floats = 0;
+  int* attn_cnt = nullptr;
+  size_t attn_cnt_n = 0;
+  int* err = nullptr;
+};
+
+std::mutex g_op_mu;
+std::map<int, OpWorkspace> g_op_ws;
+
+dllm_status op_workspace(OpWorkspace** out, size_t cnt_n, size_t attn_floats, size_t attn_cnt_n) {
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  OpWorkspace& w = g_op_ws[dev];
+  if (!w.ws) {
+    CKS(dev_alloc((void**)&w.ws, (size_t)device_sms() * 2 * 256 * 128 * 4));
+    CKS(dev_alloc((void**)&w.err, 256));
+    CK(cudaMemset(w.err, 0, 256));
+  }
+  if (w.cnt_n < cnt_n) {
+    if (w.cnt) cudaFree(w.cnt);
+    w.cnt = nullptr;
+    CKS(dev_alloc((void**)&w.cnt, cnt_n * 4));
+    CK(cudaMemset(w.cnt, 0, cnt_n * 4));
+    w.cnt_n = cnt_n;
+  }
+  if (w.attn_floats < attn_floats) {
+    if (w.attn) cudaFree(w.attn);
+    w.attn = nullptr;
+    CKS(dev_alloc((void**)&w.attn, attn_floats * 4));
+    w.attn_floats = attn_floats;
+  }
+  if (w.attn_cnt_n < attn_cnt_n) {
+    if (w.attn_cnt) cudaFree(w.attn_cnt);
+    w.attn_cnt = nullptr;
+    CKS(dev_alloc((void**)&w.attn_cnt, attn_cnt_n * 4));
+    CK(cudaMemset(w.attn_cnt, 0, attn_cnt_n * 4));
+    w.attn_cnt_n = attn_cnt_n;
+  }
+  *out = &w;
+  return DLLM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" dllm_status dllm_op_gemm(const uint16_t* W, const uint16_t* X, float* Y, int32_t M, int32_t N, int32_t K,
+                                    void* stream) {
+  if (!W || !X || !Y || M < 1 || N < 1 || K < 8 || K % 8 != 0 || !aligned16(W) || !aligned16(X)) {
+    set_error("bad gemm arguments: M=%d N=%d K=%d (K %% 8 == 0, 16-byte aligned operands)", M, N, K);
+    return DLLM_EINVAL;
+  }
+  std::lock_guard<std::mutex> lk(g_op_mu);
+  const int BN = pick_bn(N);
+  GemmParams p = {};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = ceil_div(M, 128);
+  p.n_tiles = ceil_div(N, BN);
+  p.kc = ceil_div(K, 64);
+  p.total = (long long)p.m_tiles * p.n_tiles * p.kc;
+  OpWorkspace* w = nullptr;
+  CKS(op_workspace(&w, (size_t)p.m_tiles * p.n_tiles, 0, 0));
+  p.ws = w->ws;
+  p.counters = w->cnt;
+  p.err = w->err;
+  p.y = Y;
+  p.ldy = M;
+  CUtensorMap ta, tb;
+  CKS(map_2d(&ta, W, K, M, 128));
+  CKS(map_2d(&tb, X, K, N, BN));
+  const int grid = (int)std::min<long long>(device_sms(), p.total);
+  CK(launch_gemm(GEMM_PLAIN, BN, ta, tb, p, grid, static_cast<cudaStream_t>(stream), false));
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                         uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R, int32_t T,
+                                         void* stream) {
+  if (!q || !k_cache || !v_cache || !out || b < 1 || H < 1 || (hd != 64 && hd != 128) || R < 1 || T < 1 ||
+      !aligned16(k_cache) || !aligned16(v_cache)) {
+    set_error("bad attention arguments: b=%d H=%d hd=%d R=%d T=%d", b, H, hd, R, T);
+    return DLLM_EINVAL;
+  }
+  std::lock_guard<std::mutex> lk(g_op_mu);
+  const int sms = device_sms();
+  AttnPlan a = plan_attention(b, H, R, T, sms);
+  const int QT = 16 * a.wq;
+  const size_t works = (size_t)b * H * a.q_tiles;
+  OpWorkspace* w = nullptr;
+  CKS(op_workspace(&w, 1, works * a.splits * QT * (hd + 2), works));
+  CUtensorMap tk, tv;
+  CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H));
+  CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H));
+  AttnParams p;
+  p.q = q;
+  p.o = out;
+  p.R = R;
+  p.b = b;
+  p.H = H;
+  p.T = T;
+  p.z_k0 = 0;
+  p.z_v0 = 0;
+  p.q_tiles = a.q_tiles;
+  p.splits = a.splits;
+  p.kps = a.kps;
+  p.scale_log2 = kLog2e / std::sqrt((float)hd);
+  p.ws_o = w->attn;
+  p.ws_ml = w->attn + works * a.splits * QT * hd;
+  p.counters = w->attn_cnt;
+  p.err = w->err;
+  CK(launch_attention(hd, a.wq, tk, tv, p, dim3(a.splits, a.q_tiles * H, b), static_cast<cudaStream_t>(stream),
+                      false));
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_op_select_commit(const float* conf, const int32_t* arg, int32_t* x, int32_t b, int32_t T,
+                                             int32_t blk_start, int32_t B, int32_t mask_id, const dllm_select* sel,
+                                             int32_t* count, void* stream) {
+  if (!conf || !arg || !x || !count || b < 1 || B < 1 || B > kMaxBlock || blk_start < 0 || blk_start + B > T) {
+    set_error("bad select arguments: b=%d T=%d blk_start=%d B=%d", b, T, blk_start, B);
+    return DLLM_EINVAL;
+  }
+  SelectRule r;
+  CKS(to_rule(sel, &r));
+  SelectParams p{conf, arg, x, count, T, blk_start, B, mask_id, r};
+  select_kernel<<<b, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  CK(cudaGetLastError());
+  return DLLM_OK;
+}
+
+// ====================================================================== misc
+extern "C" const char* dllm_last_error(void) { return g_err; }
+
+extern "C" const char* dllm_status_string(int32_t st) {
+  switch (st) {
+    case DLLM_OK: return "ok";
+    case DLLM_EINVAL: return "invalid argument";
+    case DLLM_ENOMEM: return "out of memory";
+    case DLLM_ECUDA: return "CUDA error";
+    case DLLM_EIO: return "I/O error";
+    case DLLM_ESTATE: return "invalid state";
+    case DLLM_ETIMEOUT: return "kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int32_t dllm_version(void) { return 100; }

@@ -1,0 +1,28 @@
+// Instantiations of the block-attention kernel (head_dim 64/128, 2 or 4 query warps).
+#include "launch.h"
+
+namespace dllm {
+
+template <int HD, int WQ>
+static cudaError_t go_attn(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
+                           cudaStream_t st, bool pdl) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, WQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AttnCfg<HD>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(attn_kernel<HD, WQ>, grid, dim3(128), AttnCfg<HD>::SMEM_BYTES, st, pdl, tk, tv, p);
+}
+
+cudaError_t launch_attention(int hd, int wq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                             dim3 grid, cudaStream_t st, bool pdl) {
+  if (hd == 64 && wq == 2) return go_attn<64, 2>(tk, tv, p, grid, st, pdl);
+  if (hd == 64 && wq == 4) return go_attn<64, 4>(tk, tv, p, grid, st, pdl);
+  if (hd == 128 && wq == 2) return go_attn<128, 2>(tk, tv, p, grid, st, pdl);
+  if (hd == 128 && wq == 4) return go_attn<128, 4>(tk, tv, p, grid, st, pdl);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dllm

@@ -1,0 +1,356 @@
+// Non-causal block attention over the K/V cache (the zhongzhuzhou.org notes,
+// section 2, eq. 3, with every query reading every key: section 3, Algorithm
+// 1 step 7 - fresh block K/V plus cached prefix/suffix K/V).
+//
+// A denoise step has only block-many queries per head, so the keys are split
+// across CTAs (flash-decoding): CTA (split, q-tile, head, seq) streams its key
+// range through a two-stage TMA ring (3-D tensor map over the cache, 128-byte
+// swizzle), computes S = Q K^T and O = P V on the tensor cores
+// (mma.sync m16n8k16 bf16 -> f32; the products are small, the K/V bytes are
+// what bound the kernel), keeps an online softmax (running max and sum, base-2
+// exponentials), merges the warps' key halves through shared memory and the
+// key splits through a workspace: the last split to finish combines all
+// partials in split order.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace dllm {
+
+struct AttnParams {
+  const uint16_t* q;   // [b*R][H][HD]
+  uint16_t* o;         // [b*R][H*HD]
+  int R, b, H, T;      // query rows per sequence, sequences, heads, valid keys
+  int z_k0, z_v0;      // plane of (seq 0, head 0) in the K and V maps; plane = z0 + seq*H + head
+  int q_tiles, splits, kps;  // query tiles per (seq, head), key splits, keys per split (multiple of 64)
+  float scale_log2;    // log2(e) / sqrt(HD)
+  float* ws_o;         // [works][splits][QT][HD]
+  float* ws_ml;        // [works][splits][QT][2]
+  int* counters;       // [works]
+  int* err;
+};
+
+template <int HD>
+struct AttnCfg {
+  static constexpr int KT = 64;                      // keys per smem tile
+  static constexpr int TILE_BYTES = KT * HD * 2;     // one of K or V
+  static constexpr int STAGES = 2;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * TILE_BYTES + 32 * HD * 4 + 32 * 2 * 4 + 64;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of the 16-byte chunk `ch` (8 bf16 along the head dim) of key row
+// `r` in a TMA 128B-swizzled tile stored as HD/64 boxes of [64 keys][128 B].
+__device__ __forceinline__ uint32_t swz_off(int r, int ch) {
+  return (uint32_t)((ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+// WQ warps along queries (16 rows each), 4/WQ warp groups along each key tile.
+template <int HD, int WQ>
+__global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using C = AttnCfg<HD>;
+  constexpr int WK = 4 / WQ;
+  constexpr int QT = 16 * WQ;
+  constexpr int KW = C::KT / WK;   // keys per warp per tile
+  constexpr int NT = KW / 8;       // n8 tiles of S per warp
+  constexpr int KS = HD / 16;      // k16 steps of Q K^T
+  constexpr int OT = HD / 8;       // n8 tiles of O
+  static_assert(QT <= 64, "query tile");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::STAGES * C::TILE_BYTES;
+  float* xo = reinterpret_cast<float*>(sV + C::STAGES * C::TILE_BYTES);   // [32][HD] group-1 O (WK == 2)
+  float* xml = xo + 32 * HD;                                               // [32][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(xml + 64);
+  int* bcast = reinterpret_cast<int*>(full + C::STAGES);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wq = warp % WQ, wk = warp / WQ;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int split = blockIdx.x;
+  const int qt = blockIdx.y % p.q_tiles;
+  const int head = blockIdx.y / p.q_tiles;
+  const int seq = blockIdx.z;
+  const int k_beg = split * p.kps;
+  const int k_end = min(p.T, k_beg + p.kps);
+  const int ntiles = (k_end - k_beg + C::KT - 1) / C::KT;
+  const int zk = p.z_k0 + seq * p.H + head, zv = p.z_v0 + seq * p.H + head;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  __syncthreads();
+  griddep_launch_dependents();
+  griddep_wait();
+
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int t, int s) {
+    const int key0 = k_beg + t * C::KT;
+    mbar_arrive_expect_tx(&full[s], 2 * C::TILE_BYTES);
+#pragma unroll
+    for (int bx = 0; bx < HD / 64; ++bx) {
+      tma_load_3d(sK + s * C::TILE_BYTES + bx * 8192, &tmK, &full[s], bx * 64, key0, zk, pol);
+      tma_load_3d(sV + s * C::TILE_BYTES + bx * 8192, &tmV, &full[s], bx * 64, key0, zv, pol);
+    }
+  };
+  if (tid == 0)
+    for (int t = 0; t < C::STAGES && t < ntiles; ++t) issue(t, t);
+
+  // Q fragments of this warp's 16 query rows
+  const int qrow0 = qt * QT + wq * 16;
+  uint32_t qa[KS][4];
+  {
+    const long long base_lo = (((long long)seq * p.R + qrow0 + g) * p.H + head) * HD;
+    const long long base_hi = base_lo + 8LL * p.H * HD;
+    const bool lo_ok = qrow0 + g < p.R, hi_ok = qrow0 + g + 8 < p.R;
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const int c0 = kk * 16 + 2 * t4;
+      qa[kk][0] = lo_ok ? q32[(base_lo + c0) >> 1] : 0u;
+      qa[kk][1] = hi_ok ? q32[(base_hi + c0) >> 1] : 0u;
+      qa[kk][2] = lo_ok ? q32[(base_lo + c0 + 8) >> 1] : 0u;
+      qa[kk][3] = hi_ok ? q32[(base_hi + c0 + 8) >> 1] : 0u;
+    }
+  }
+
+  float oacc[OT][4];
+#pragma unroll
+  for (int i = 0; i < OT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.0f;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.0f, l_hi = 0.0f;
+  bool failed = false;
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % C::STAGES;
+    if (!failed && !mbar_wait(&full[s], (uint32_t)((t / C::STAGES) & 1), nullptr, p.err, ERR_ATTN_FULL))
+      failed = true;
+    if (!failed) {
+      const uint32_t kb = smem_u32(sK + s * C::TILE_BYTES);
+      const uint32_t vb = smem_u32(sV + s * C::TILE_BYTES);
+      const int key_w = wk * KW;       // first key of this warp inside the tile
+      // S = Q K^T
+      float sacc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+        const int r = key_w + nt * 8 + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < KS; kk += 2) {
+          const int ch = 2 * kk + (lane >> 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + swz_off(r, ch), b0, b1, b2, b3);
+          mma16816(sacc[nt], qa[kk], b0, b1);
+          mma16816(sacc[nt], qa[kk + 1], b2, b3);
+        }
+      }
+      // online softmax (base 2)
+      const int key_base = k_beg + t * C::KT + key_w;
+      float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = key_base + nt * 8 + 2 * t4 + e;
+          const bool ok = key < k_end;
+          sacc[nt][e] = ok ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+          sacc[nt][2 + e] = ok ? sacc[nt][2 + e] * p.scale_log2 : -INFINITY;
+          mx_lo = fmaxf(mx_lo, sacc[nt][e]);
+          mx_hi = fmaxf(mx_hi, sacc[nt][2 + e]);
+        }
+      }
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      const float use_lo = (mn_lo == -INFINITY) ? 0.0f : mn_lo;
+      const float use_hi = (mn_hi == -INFINITY) ? 0.0f : mn_hi;
+      const float corr_lo = exp2f(m_lo - use_lo), corr_hi = exp2f(m_hi - use_hi);
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      float sum_lo = 0.0f, sum_hi = 0.0f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        sacc[nt][0] = exp2f(sacc[nt][0] - use_lo);
+        sacc[nt][1] = exp2f(sacc[nt][1] - use_lo);
+        sacc[nt][2] = exp2f(sacc[nt][2] - use_hi);
+        sacc[nt][3] = exp2f(sacc[nt][3] - use_hi);
+        sum_lo += sacc[nt][0] + sacc[nt][1];
+        sum_hi += sacc[nt][2] + sacc[nt][3];
+      }
+      sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, 1);
+      sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, 2);
+      sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 1);
+      sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 2);
+      l_lo = l_lo * corr_lo + sum_lo;
+      l_hi = l_hi * corr_hi + sum_hi;
+#pragma unroll
+      for (int i = 0; i < OT; ++i) {
+        oacc[i][0] *= corr_lo;
+        oacc[i][1] *= corr_lo;
+        oacc[i][2] *= corr_hi;
+        oacc[i][3] *= corr_hi;
+      }
+      // O += P V
+#pragma unroll
+      for (int j = 0; j < KW / 16; ++j) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16(sacc[2 * j][0], sacc[2 * j][1]);
+        pa[1] = pack_bf16(sacc[2 * j][2], sacc[2 * j][3]);
+        pa[2] = pack_bf16(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
+        pa[3] = pack_bf16(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
+        const int mi = lane >> 3;
+        const int r = key_w + j * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int ot = 0; ot < OT; ot += 2) {
+          const int ch = ot + (mi >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + swz_off(r, ch), b0, b1, b2, b3);
+          mma16816(oacc[ot], pa, b0, b1);
+          mma16816(oacc[ot + 1], pa, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && !failed && t + C::STAGES < ntiles) issue(t + C::STAGES, s);
+  }
+
+  // combine the key groups of a CTA (WK == 2): group 1 hands its state to group 0
+  if constexpr (WK == 2) {
+    if (wk == 1) {
+      const int rl = wq * 16 + g;
+#pragma unroll
+      for (int i = 0; i < OT; ++i) {
+        const int col = i * 8 + 2 * t4;
+        xo[rl * HD + col] = oacc[i][0];
+        xo[rl * HD + col + 1] = oacc[i][1];
+        xo[(rl + 8) * HD + col] = oacc[i][2];
+        xo[(rl + 8) * HD + col + 1] = oacc[i][3];
+      }
+      if (t4 == 0) {
+        xml[rl * 2] = m_lo;
+        xml[rl * 2 + 1] = l_lo;
+        xml[(rl + 8) * 2] = m_hi;
+        xml[(rl + 8) * 2 + 1] = l_hi;
+      }
+    }
+    __syncthreads();
+    if (wk == 0) {
+      const int rl = wq * 16 + g;
+      const float m1_lo = xml[rl * 2], l1_lo = xml[rl * 2 + 1];
+      const float m1_hi = xml[(rl + 8) * 2], l1_hi = xml[(rl + 8) * 2 + 1];
+      const float M_lo = fmaxf(m_lo, m1_lo), M_hi = fmaxf(m_hi, m1_hi);
+      const float u_lo = (M_lo == -INFINITY) ? 0.0f : M_lo, u_hi = (M_hi == -INFINITY) ? 0.0f : M_hi;
+      const float a0_lo = exp2f(m_lo - u_lo), a1_lo = exp2f(m1_lo - u_lo);
+      const float a0_hi = exp2f(m_hi - u_hi), a1_hi = exp2f(m1_hi - u_hi);
+#pragma unroll
+      for (int i = 0; i < OT; ++i) {
+        const int col = i * 8 + 2 * t4;
+        oacc[i][0] = oacc[i][0] * a0_lo + xo[rl * HD + col] * a1_lo;
+        oacc[i][1] = oacc[i][1] * a0_lo + xo[rl * HD + col + 1] * a1_lo;
+        oacc[i][2] = oacc[i][2] * a0_hi + xo[(rl + 8) * HD + col] * a1_hi;
+        oacc[i][3] = oacc[i][3] * a0_hi + xo[(rl + 8) * HD + col + 1] * a1_hi;
+      }
+      l_lo = l_lo * a0_lo + l1_lo * a1_lo;
+      l_hi = l_hi * a0_hi + l1_hi * a1_hi;
+      m_lo = M_lo;
+      m_hi = M_hi;
+    }
+  }
+
+  const bool writer = (wk == 0);
+  const int row_lo = qrow0 + g, row_hi = qrow0 + g + 8;
+  if (p.splits == 1) {
+    if (writer) {
+      const float il = l_lo > 0.0f ? 1.0f / l_lo : 0.0f, ih = l_hi > 0.0f ? 1.0f / l_hi : 0.0f;
+#pragma unroll
+      for (int i = 0; i < OT; ++i) {
+        const int col = i * 8 + 2 * t4;
+        if (row_lo < p.R)
+          *reinterpret_cast<uint32_t*>(&p.o[((long long)seq * p.R + row_lo) * p.H * HD + head * HD + col]) =
+              pack_bf16(oacc[i][0] * il, oacc[i][1] * il);
+        if (row_hi < p.R)
+          *reinterpret_cast<uint32_t*>(&p.o[((long long)seq * p.R + row_hi) * p.H * HD + head * HD + col]) =
+              pack_bf16(oacc[i][2] * ih, oacc[i][3] * ih);
+      }
+    }
+    return;
+  }
+
+  const long long work = ((long long)seq * p.H + head) * p.q_tiles + qt;
+  const long long wbase = work * p.splits + split;
+  if (writer) {
+    float* wo = p.ws_o + wbase * QT * HD;
+    float* wml = p.ws_ml + wbase * QT * 2;
+    const int rl = wq * 16 + g;
+#pragma unroll
+    for (int i = 0; i < OT; ++i) {
+      const int col = i * 8 + 2 * t4;
+      __stcg(reinterpret_cast<float2*>(&wo[rl * HD + col]), make_float2(oacc[i][0], oacc[i][1]));
+      __stcg(reinterpret_cast<float2*>(&wo[(rl + 8) * HD + col]), make_float2(oacc[i][2], oacc[i][3]));
+    }
+    if (t4 == 0) {
+      __stcg(reinterpret_cast<float2*>(&wml[rl * 2]), make_float2(m_lo, l_lo));
+      __stcg(reinterpret_cast<float2*>(&wml[(rl + 8) * 2]), make_float2(m_hi, l_hi));
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int old = atomicAdd(&p.counters[work], 1);
+    const int last = (old == p.splits - 1);
+    if (last) p.counters[work] = 0;
+    *bcast = last;
+  }
+  __syncthreads();
+  if (!*bcast) return;
+  __threadfence();
+  const float* base_o = p.ws_o + work * p.splits * QT * HD;
+  const float* base_ml = p.ws_ml + work * p.splits * QT * 2;
+  for (int e = tid; e < QT * HD; e += 128) {
+    const int rl = e / HD, col = e - rl * HD;
+    const int row = qt * QT + rl;
+    if (row >= p.R) continue;
+    float M = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(&base_ml[(s * QT + rl) * 2]));
+    const float u = (M == -INFINITY) ? 0.0f : M;
+    float L = 0.0f, O = 0.0f;
+    for (int s = 0; s < p.splits; ++s) {
+      const float ms = __ldcg(&base_ml[(s * QT + rl) * 2]);
+      const float ls = __ldcg(&base_ml[(s * QT + rl) * 2 + 1]);
+      const float a = exp2f(ms - u);
+      L += ls * a;
+      O += __ldcg(&base_o[(s * QT + rl) * HD + col]) * a;
+    }
+    p.o[((long long)seq * p.R + row) * p.H * HD + head * HD + col] = f32_to_bf16_bits(L > 0.0f ? O / L : 0.0f);
+  }
+}
+
+}  // namespace dllm

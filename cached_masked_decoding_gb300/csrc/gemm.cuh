@@ -1,0 +1,521 @@
+// Weight-streaming tensor-core GEMM with fused epilogues.
+//
+//   D[m][r] = sum_k W[m][k] * X[r][k]     (W: weights [M][K], X: activations [N][K], bf16)
+//
+// "Swap-AB" form: the weights are the 128-row A operand, the N activation rows
+// the narrow B operand, so a denoise step with n = batch*block rows is one
+// pass over the weights with n MACs per weight element.  One CTA per SM:
+//   warp 0  TMA producer (A and B tiles into an smem ring, 128-byte swizzle),
+//   warp 1  tcgen05.mma issuer (M=128, N=BN, K=16 per instruction, f32 in TMEM,
+//           two TMEM accumulators so the epilogue of one tile overlaps the
+//           main loop of the next),
+//   warps 2-5  epilogue (tcgen05.ld, 32 columns at a time).
+// Work split ("stream-K"): the m_tiles*n_tiles*kc chunks of 64 reduction
+// elements are cut into gridDim.x equal contiguous ranges, so every SM streams
+// the same number of weight bytes.  A tile cut between CTAs is finished by the
+// last contributor to arrive, which sums every contributor's partial in
+// contributor order: results do not depend on arrival order.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace dllm {
+
+enum GemmKind : int { GEMM_PLAIN = 0, GEMM_QKV = 1, GEMM_RESID = 2, GEMM_SWIGLU = 3, GEMM_LMHEAD = 4 };
+
+struct GemmParams {
+  int M, N, K;            // weight rows, activation rows, reduction length
+  int m_tiles, n_tiles, kc;
+  long long total;        // m_tiles * n_tiles * kc
+  float* ws;              // fix-up partials [grid][2][BN][128]
+  int* counters;          // [m_tiles * n_tiles], zero between launches
+  int* err;
+  // RMSNorm row factor of the activation rows: rsqrt(sum_t ss_in[r][t] * inv_d + eps)
+  const float* ss_in;
+  int ss_in_tiles;
+  float inv_d, eps;
+  // row r of X <-> sequence r / R, position row0 + r % R
+  int R, row0;
+  // GEMM_QKV
+  uint16_t* q_out;        // [N][d]
+  uint16_t* kv;           // cache [L][2][b][H][T_pad][hd]
+  const float2* rope_cs;  // [T_pad][hd/2] (cos, sin)
+  int d_model, head_dim, n_heads, T_pad, b_seqs, layer;
+  // GEMM_RESID
+  float* h;               // residual [N][d]
+  const uint16_t* g_next; // next RMSNorm gain [d]
+  uint16_t* xn_out;       // bf16(h * g_next) [rows][d]
+  float* ss_out;          // per-128-column sums of h^2 [rows][d/128]
+  int remap;              // 1: output rows are the block rows (final layer)
+  int blk_start, blk_len;
+  // GEMM_SWIGLU
+  uint16_t* act;          // [N][act_ld]
+  int act_ld;
+  // GEMM_LMHEAD
+  float* st_m;            // [m_tiles][N] tile max logit
+  float* st_s;            // [m_tiles][N] tile sum exp(l - max)
+  int* st_a;              // [m_tiles][N] tile argmax (lowest id)
+  // GEMM_PLAIN
+  float* y;
+  int ldy;
+};
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int STAGES = BN <= 64 ? 8 : (BN == 128 ? 6 : 4);
+  static constexpr int A_BYTES = 128 * 64 * 2;
+  static constexpr int B_BYTES = BN * 64 * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;   // two accumulators; 64..512, a power of two
+  static constexpr int XCH_FLOATS = 128 * 33;
+  static constexpr int RED_FLOATS = 4 * 32 * 3;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCH_FLOATS * 4 + 256 * 4 + RED_FLOATS * 4 +
+                                    (2 * STAGES + 4) * 8 + 64;
+};
+
+__device__ __forceinline__ long long sk_owner(long long i, long long G, long long total) {
+  return ((i + 1) * G + total - 1) / total - 1;
+}
+
+// Sum over the 32 lanes of a warp of 32 per-lane columns: afterwards v[0] on
+// lane c holds the total of column c.  Fixed pairing order (deterministic).
+__device__ __forceinline__ void warp_transpose_sum(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      float send = up ? v[i] : v[i + s];
+      float keep = up ? v[i + s] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+}
+
+// Max with lowest-index tie-break, transposed like warp_transpose_sum.
+__device__ __forceinline__ void warp_transpose_argmax(float (&v)[32], int (&id)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      float sv = up ? v[i] : v[i + s];
+      int si = up ? id[i] : id[i + s];
+      float kv = up ? v[i + s] : v[i];
+      int ki = up ? id[i + s] : id[i];
+      float rv = __shfl_xor_sync(0xffffffffu, sv, s);
+      int ri = __shfl_xor_sync(0xffffffffu, si, s);
+      const bool take = (rv > kv) || (rv == kv && ri < ki);
+      v[i] = take ? rv : kv;
+      id[i] = take ? ri : ki;
+    }
+  }
+}
+
+// Epilogue of 32 consecutive activation rows (columns of the accumulator) for
+// the thread's weight row m = m_idx*128 + l128.  v holds raw sums.  Every
+// epilogue thread of the CTA calls this with the same (m_idx, r0).
+template <int KIND>
+__device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], int m_idx, int r0, int l128,
+                                          int lane, int q, float* xch, const float* rs, float* red) {
+  const int m = m_idx * 128 + l128;
+  if constexpr (KIND == GEMM_PLAIN) {
+    if (m < p.M) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int r = r0 + c;
+        if (r < p.N) p.y[(long long)r * p.ldy + m] = p.ss_in ? v[c] * rs[c] : v[c];
+      }
+    }
+  } else if constexpr (KIND == GEMM_QKV) {
+    const int d = p.d_model, hd = p.head_dim, half = hd >> 1;
+    const int sec = (m_idx * 128) / d;          // uniform over the tile: 0 q, 1 k, 2 v
+    const int mr = m - sec * d;
+    const int head = mr / hd, j = mr - head * hd;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] *= rs[c];
+    if (sec < 2) {
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) xch[l128 * 33 + c] = v[c];
+      named_bar_sync(1, 128);
+      const int partner = l128 ^ half;
+      const int jj = j & (half - 1);
+      const float sgn = (j < half) ? -1.0f : 1.0f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int r = r0 + c;
+        const int rr = r < p.N ? r : 0;
+        const int pos = p.row0 + rr % p.R;
+        const float2 cs = p.rope_cs[(long long)pos * half + jj];
+        v[c] = v[c] * cs.x + sgn * xch[partner * 33 + c] * cs.y;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int r = r0 + c;
+      if (r >= p.N) continue;
+      const uint16_t bits = f32_to_bf16_bits(v[c]);
+      if (sec == 0) {
+        p.q_out[(long long)r * d + mr] = bits;
+      } else {
+        const int seq = r / p.R;
+        const int pos = p.row0 + r % p.R;
+        const long long plane = (((long long)p.layer * 2 + (sec - 1)) * p.b_seqs + seq) * p.n_heads + head;
+        p.kv[(plane * p.T_pad + pos) * hd + j] = bits;
+      }
+    }
+  } else if constexpr (KIND == GEMM_RESID) {
+    const int d = p.d_model;
+    const float g = bf16_bits_to_f32(p.g_next[m]);
+    float sq[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int r = r0 + c;
+      sq[c] = 0.0f;
+      if (r < p.N) {
+        const long long idx = (long long)r * d + m;
+        const float hv = p.h[idx] + v[c];
+        p.h[idx] = hv;
+        int ro = r;
+        if (p.remap) {
+          const int seq = r / p.R, pos = p.row0 + r % p.R;
+          const int bi = pos - p.blk_start;
+          ro = (bi >= 0 && bi < p.blk_len) ? seq * p.blk_len + bi : -1;
+        }
+        if (ro >= 0) {
+          p.xn_out[(long long)ro * d + m] = f32_to_bf16_bits(hv * g);
+          sq[c] = hv * hv;
+        }
+      }
+    }
+    warp_transpose_sum(sq, lane);
+    named_bar_sync(1, 128);
+    red[q * 32 + lane] = sq[0];
+    named_bar_sync(1, 128);
+    if (l128 < 32) {
+      const int r = r0 + l128;
+      if (r < p.N) {
+        int ro = r;
+        if (p.remap) {
+          const int seq = r / p.R, pos = p.row0 + r % p.R;
+          const int bi = pos - p.blk_start;
+          ro = (bi >= 0 && bi < p.blk_len) ? seq * p.blk_len + bi : -1;
+        }
+        if (ro >= 0)
+          p.ss_out[(long long)ro * (d >> 7) + m_idx] = ((red[l128] + red[32 + l128]) + red[64 + l128]) + red[96 + l128];
+      }
+    }
+  } else if constexpr (KIND == GEMM_SWIGLU) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] *= rs[c];
+    named_bar_sync(1, 128);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) xch[l128 * 33 + c] = v[c];
+    named_bar_sync(1, 128);
+    if (l128 < 64) {
+      const int f = m_idx * 64 + l128;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int r = r0 + c;
+        if (r >= p.N) continue;
+        const float gt = v[c];
+        const float up = xch[(l128 + 64) * 33 + c];
+        const float a = gt / (1.0f + __expf(-gt)) * up;
+        p.act[(long long)r * p.act_ld + f] = f32_to_bf16_bits(a);
+      }
+    }
+  } else if constexpr (KIND == GEMM_LMHEAD) {
+    float lg[32];
+    int id[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      lg[c] = (m < p.M) ? v[c] * rs[c] : -INFINITY;
+      id[c] = m;
+    }
+    float mx[32];
+    int ax[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) { mx[c] = lg[c]; ax[c] = id[c]; }
+    warp_transpose_argmax(mx, ax, lane);
+    // mx[0]/ax[0] on lane c: this warp's max / argmax of column c
+    float e[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float mc = __shfl_sync(0xffffffffu, mx[0], c);
+      e[c] = exp2f((lg[c] - mc) * kLog2e);
+    }
+    warp_transpose_sum(e, lane);
+    named_bar_sync(1, 128);
+    red[(q * 32 + lane) * 3 + 0] = mx[0];
+    red[(q * 32 + lane) * 3 + 1] = e[0];
+    red[(q * 32 + lane) * 3 + 2] = __int_as_float(ax[0]);
+    named_bar_sync(1, 128);
+    if (l128 < 32) {
+      const int r = r0 + l128;
+      if (r < p.N) {
+        float M = red[(0 * 32 + l128) * 3 + 0];
+        int A = __float_as_int(red[(0 * 32 + l128) * 3 + 2]);
+#pragma unroll
+        for (int w = 1; w < 4; ++w) {
+          const float mw = red[(w * 32 + l128) * 3 + 0];
+          if (mw > M) { M = mw; A = __float_as_int(red[(w * 32 + l128) * 3 + 2]); }
+        }
+        float S = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float mw = red[(w * 32 + l128) * 3 + 0];
+          const float sw = red[(w * 32 + l128) * 3 + 1];
+          S += (mw == -INFINITY) ? 0.0f : sw * exp2f((mw - M) * kLog2e);
+        }
+        const long long o = (long long)m_idx * p.N + r;
+        p.st_m[o] = M;
+        p.st_s[o] = S;
+        p.st_a[o] = A;
+      }
+    }
+  }
+}
+
+template <int BN, int KIND>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+  using C = GemmCfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::A_BYTES;
+  float* xch = reinterpret_cast<float*>(sB + STAGES * C::B_BYTES);
+  float* rs_s = xch + C::XCH_FLOATS;
+  float* red = rs_s + 256;
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + C::RED_FLOATS);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* bcast = reinterpret_cast<int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long G = gridDim.x, cta = blockIdx.x;
+  const long long start = cta * p.total / G;
+  const long long end = (cta + 1) * p.total / G;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_launch_dependents();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const long long n = end - start;
+      const int pre = (int)(n < STAGES ? n : STAGES);
+      // weights do not depend on the previous kernel: start streaming them
+      // before waiting for its activations
+      for (int i = 0; i < pre; ++i) {
+        const long long gch = start + i;
+        const long long tile = gch / p.kc;
+        const int k = (int)(gch - tile * p.kc);
+        const int m_idx = (int)(tile / p.n_tiles);
+        mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+        tma_load_2d(sA + i * C::A_BYTES, &tmA, &full[i], k * 64, m_idx * 128, pol_w);
+      }
+      griddep_wait();
+      for (int i = 0; i < pre; ++i) {
+        const long long gch = start + i;
+        const long long tile = gch / p.kc;
+        const int k = (int)(gch - tile * p.kc);
+        const int n_idx = (int)(tile % p.n_tiles);
+        tma_load_2d(sB + i * C::B_BYTES, &tmB, &full[i], k * 64, n_idx * BN, pol_x);
+      }
+      long long issued = pre;
+      for (long long i = pre; i < n; ++i) {
+        const int s = (int)(i % STAGES);
+        const uint32_t ph = (uint32_t)((i / STAGES) & 1);
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, ERR_GEMM_EMPTY)) break;
+        const long long gch = start + i;
+        const long long tile = gch / p.kc;
+        const int k = (int)(gch - tile * p.kc);
+        const int m_idx = (int)(tile / p.n_tiles);
+        const int n_idx = (int)(tile % p.n_tiles);
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], k * 64, m_idx * 128, pol_w);
+        tma_load_2d(sB + s * C::B_BYTES, &tmB, &full[s], k * 64, n_idx * BN, pol_x);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before the CTA's smem goes away
+        const long long lo = issued > STAGES ? issued - STAGES : 0;
+        for (long long i = lo; i < issued; ++i)
+          mbar_wait(&full[i % STAGES], (uint32_t)((i / STAGES) & 1), nullptr, p.err, ERR_GEMM_DRAIN);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      long long g = start, i = 0;
+      int seg = 0;
+      bool ok = true;
+      while (ok && g < end) {
+        const long long tile = g / p.kc;
+        const long long seg_first = g;
+        const long long seg_end = ((tile + 1) * p.kc < end) ? (tile + 1) * p.kc : end;
+        const int buf = seg & 1;
+        const uint32_t use = (uint32_t)(seg >> 1);
+        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, ERR_GEMM_TEMPTY)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        for (; g < seg_end; ++g, ++i) {
+          const int s = (int)(i % STAGES);
+          if (!mbar_wait(&full[s], (uint32_t)((i / STAGES) & 1), abort_flag, p.err, ERR_GEMM_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
+                        (g > seg_first || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&tfull[buf]);
+        ++seg;
+      }
+    }
+  } else {
+    // -------------------------------------------------- epilogue (warps 2..5)
+    griddep_wait();
+    const int q = warp & 3;
+    const int l128 = q * 32 + lane;
+    long long g = start;
+    int seg = 0;
+    while (g < end) {
+      const long long tile = g / p.kc;
+      const long long seg_first = g;
+      const long long seg_end = ((tile + 1) * p.kc < end) ? (tile + 1) * p.kc : end;
+      const bool full_tile = (seg_first == tile * p.kc) && (seg_end == (tile + 1) * p.kc);
+      const int m_idx = (int)(tile / p.n_tiles);
+      const int n_idx = (int)(tile % p.n_tiles);
+      const int buf = seg & 1;
+      const uint32_t use = (uint32_t)(seg >> 1);
+
+      named_bar_sync(1, 128);
+      for (int c = l128; c < BN; c += 128) {
+        const int r = n_idx * BN + c;
+        float f = 1.0f;
+        if (p.ss_in) {
+          f = 0.0f;
+          if (r < p.N) {
+            float s = 0.0f;
+            for (int t = 0; t < p.ss_in_tiles; ++t) s += p.ss_in[(long long)r * p.ss_in_tiles + t];
+            f = rsqrtf(s * p.inv_d + p.eps);
+          }
+        }
+        rs_s[c] = f;
+      }
+      named_bar_sync(1, 128);
+
+      // every epilogue warp takes the same decision: a warp whose wait gave up
+      // raised *abort_flag before this barrier
+      mbar_wait(&tfull[buf], use & 1u, abort_flag, p.err, ERR_GEMM_TFULL);
+      named_bar_sync(1, 128);
+      if (*abort_flag) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      if (full_tile) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + (uint32_t)c0, v);
+          if (c0 + 32 == BN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+          }
+          epi_chunk<KIND>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red);
+        }
+      } else {
+        const int slot = (seg_first == start) ? 0 : 1;
+        float* wsp = p.ws + ((cta * 2 + slot) * (long long)BN) * 128;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) __stcg(&wsp[(long long)(c0 + j) * 128 + l128], v[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        const long long t0 = tile * p.kc, t1 = (tile + 1) * p.kc - 1;
+        const long long c_first = sk_owner(t0, G, p.total), c_last = sk_owner(t1, G, p.total);
+        if (l128 == 0) {
+          const int contributors = (int)(c_last - c_first + 1);
+          const int old = atomicAdd(&p.counters[tile], 1);
+          const int last = (old == contributors - 1);
+          if (last) p.counters[tile] = 0;
+          *bcast = last;
+        }
+        named_bar_sync(1, 128);
+        if (*bcast) {
+          __threadfence();
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+            for (long long ctr = c_first; ctr <= c_last; ++ctr) {
+              const long long st = ctr * p.total / G;
+              const long long sstart = st > t0 ? st : t0;
+              const int sl = (sstart == st) ? 0 : 1;
+              const float* src = p.ws + ((ctr * 2 + sl) * (long long)BN) * 128;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += __ldcg(&src[(long long)(c0 + j) * 128 + l128]);
+            }
+            epi_chunk<KIND>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red);
+          }
+        }
+      }
+      g = seg_end;
+      ++seg;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace dllm

@@ -1,0 +1,83 @@
+// Host-side launchers of the kernel templates (one translation unit per GEMM
+// epilogue kind so the build compiles them in parallel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attention.cuh"
+#include "gemm.cuh"
+
+namespace dllm {
+
+// Launch with programmatic dependent launch allowed (pdl) on stream st.
+template <typename Kern, typename... Args>
+inline cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+cudaError_t launch_gemm_plain(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                              cudaStream_t st, bool pdl);
+cudaError_t launch_gemm_qkv(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                            cudaStream_t st, bool pdl);
+cudaError_t launch_gemm_resid(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                              cudaStream_t st, bool pdl);
+cudaError_t launch_gemm_swiglu(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                               cudaStream_t st, bool pdl);
+cudaError_t launch_gemm_lmhead(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                               cudaStream_t st, bool pdl);
+
+inline cudaError_t launch_gemm(int kind, int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                               int grid, cudaStream_t st, bool pdl) {
+  switch (kind) {
+    case GEMM_PLAIN: return launch_gemm_plain(bn, a, b, p, grid, st, pdl);
+    case GEMM_QKV: return launch_gemm_qkv(bn, a, b, p, grid, st, pdl);
+    case GEMM_RESID: return launch_gemm_resid(bn, a, b, p, grid, st, pdl);
+    case GEMM_SWIGLU: return launch_gemm_swiglu(bn, a, b, p, grid, st, pdl);
+    case GEMM_LMHEAD: return launch_gemm_lmhead(bn, a, b, p, grid, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_attention(int hd, int wq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                             dim3 grid, cudaStream_t st, bool pdl);
+
+}  // namespace dllm
+
+// Instantiate launch_gemm_<name> for the four activation-tile widths.
+#define DLLM_GEMM_LAUNCHER(NAME, KIND)                                                                            \
+  namespace dllm {                                                                                              \
+  template <int BN>                                                                                             \
+  static cudaError_t go_##NAME(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,       \
+                               cudaStream_t st, bool pdl) {                                                     \
+    static bool attr_set = false;                                                                               \
+    if (!attr_set) {                                                                                            \
+      cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                           GemmCfg<BN>::SMEM_BYTES);                                            \
+      if (e != cudaSuccess) return e;                                                                           \
+      attr_set = true;                                                                                          \
+    }                                                                                                           \
+    return launch_ex(gemm_kernel<BN, KIND>, dim3(grid), dim3(192), GemmCfg<BN>::SMEM_BYTES, st, pdl, a, b, p);  \
+  }                                                                                                             \
+  cudaError_t launch_gemm_##NAME(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,       \
+                                 int grid, cudaStream_t st, bool pdl) {                                         \
+    switch (bn) {                                                                                               \
+      case 32: return go_##NAME<32>(a, b, p, grid, st, pdl);                                                    \
+      case 64: return go_##NAME<64>(a, b, p, grid, st, pdl);                                                    \
+      case 128: return go_##NAME<128>(a, b, p, grid, st, pdl);                                                  \
+      case 256: return go_##NAME<256>(a, b, p, grid, st, pdl);                                                  \
+      default: return cudaErrorInvalidValue;                                                                    \
+    }                                                                                                           \
+  }                                                                                                             \
+  }

@@ -1,0 +1,241 @@
+// Embedding gather, LM-head statistic merge and the select/commit rule.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace dllm {
+
+// ------------------------------------------------------------------ embedding
+// h[r] = E[x[seq][row0 + r % R]] (f32), xn[r] = bf16(h * g), ss[r][t] = sum of
+// h^2 over columns 128t..128t+127.  One CTA per row, d/8 threads, 8 columns each.
+struct EmbedParams {
+  const int32_t* x;       // canvas [b][T]
+  const uint16_t* embed;  // [V+1][d]
+  const uint16_t* g;      // first RMSNorm gain [d]
+  float* h;
+  uint16_t* xn;
+  float* ss;
+  int d, R, row0, T;
+};
+
+__global__ void __launch_bounds__(1024) embed_kernel(const EmbedParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int r = blockIdx.x;
+  const int seq = r / p.R, pos = p.row0 + r % p.R;
+  const int tok = p.x[(long long)seq * p.T + pos];
+  const int c0 = threadIdx.x * 8;
+  const uint4 e = *reinterpret_cast<const uint4*>(p.embed + (long long)tok * p.d + c0);
+  const uint4 gg = *reinterpret_cast<const uint4*>(p.g + c0);
+  const uint16_t* ev = reinterpret_cast<const uint16_t*>(&e);
+  const uint16_t* gv = reinterpret_cast<const uint16_t*>(&gg);
+  float hv[8];
+  uint16_t ov[8];
+  float sq = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    hv[i] = bf16_bits_to_f32(ev[i]);
+    ov[i] = f32_to_bf16_bits(hv[i] * bf16_bits_to_f32(gv[i]));
+    sq += hv[i] * hv[i];
+  }
+  float4* hp = reinterpret_cast<float4*>(p.h + (long long)r * p.d + c0);
+  hp[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+  hp[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+  *reinterpret_cast<uint4*>(p.xn + (long long)r * p.d + c0) = *reinterpret_cast<const uint4*>(ov);
+  // 16 threads cover one 128-column tile
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, s);
+  if ((threadIdx.x & 15) == 0) p.ss[(long long)r * (p.d >> 7) + (c0 >> 7)] = sq;
+}
+
+// ------------------------------------------------------------------ selection
+struct SelectRule {
+  int policy;   // 0 threshold, 1 fixed-k, 2 factor, 3 budget
+  float tau;
+  int k;
+  float factor;
+};
+
+// Select among the B positions of one sequence's block and commit.  Runs on
+// the whole CTA (any blockDim multiple of 32); conf_s / arg_s / flags in smem.
+// Writes x and returns the count through *count_out (thread 0).
+__device__ __forceinline__ void select_commit_cta(const float* conf_s, const int* arg_s, int* rank_s, float* eps_s,
+                                                  int B, int32_t* xblk, int mask_id, const SelectRule rule,
+                                                  int32_t* count_out, int* shared_best) {
+  const int tid = threadIdx.x;
+  // eligibility and confidence rank (descending confidence, ties by position)
+  for (int i = tid; i < B; i += blockDim.x) {
+    const bool e = xblk[i] == mask_id;
+    int rank = -1;
+    if (e) {
+      rank = 0;
+      const float ci = conf_s[i];
+      for (int j = 0; j < B; ++j) {
+        if (j == i || xblk[j] != mask_id) continue;
+        const float cj = conf_s[j];
+        rank += (cj > ci || (cj == ci && j < i)) ? 1 : 0;
+      }
+    }
+    rank_s[i] = rank;
+  }
+  if (tid == 0) *shared_best = 0;
+  __syncthreads();
+  int n_sel = 0;  // select ranks < n_sel
+  if (rule.policy == 0) {
+    // threshold: count qualifying positions
+    for (int i = tid; i < B; i += blockDim.x)
+      if (rank_s[i] >= 0 && conf_s[i] >= rule.tau) atomicAdd(shared_best, 1);
+    __syncthreads();
+    const int nq = *shared_best;
+    __syncthreads();
+    for (int i = tid; i < B; i += blockDim.x) {
+      const int rk = rank_s[i];
+      bool sel = false;
+      if (rk >= 0) sel = (nq > 0) ? (conf_s[i] >= rule.tau) : (rk == 0);
+      eps_s[i] = sel ? 1.0f : 0.0f;
+    }
+  } else {
+    if (rule.policy == 1) {
+      n_sel = rule.k;
+    } else if (rule.policy == 2) {
+      // factor: largest n with (n+1)(1 - c_(n)) < f, c_(n) = confidence of rank n-1
+      for (int i = tid; i < B; i += blockDim.x) {
+        const int rk = rank_s[i];
+        if (rk >= 0) {
+          const float lhs = __fmul_rn((float)(rk + 2), __fsub_rn(1.0f, conf_s[i]));
+          if (lhs < rule.factor) atomicMax(shared_best, rk + 1);
+        }
+      }
+      __syncthreads();
+      n_sel = max(*shared_best, 1);
+    } else {
+      // eq. 9 budget: sequential float32 prefix sum in rank order
+      for (int i = tid; i < B; i += blockDim.x)
+        if (rank_s[i] >= 0) eps_s[rank_s[i]] = __fsub_rn(1.0f, conf_s[i]);
+      __syncthreads();
+      if (tid == 0) {
+        int m = 0;
+        for (int i = 0; i < B; ++i) m += rank_s[i] >= 0 ? 1 : 0;
+        float total = 0.0f;
+        int best = 0;
+        for (int n = 1; n <= m; ++n) {
+          const float e = eps_s[n - 1];
+          total = __fadd_rn(total, e);
+          if (__fadd_rn(total, e) < 1.0f) best = n;
+        }
+        *shared_best = best;
+      }
+      __syncthreads();
+      n_sel = max(*shared_best, 1);
+    }
+    __syncthreads();
+    for (int i = tid; i < B; i += blockDim.x) {
+      const int rk = rank_s[i];
+      eps_s[i] = (rk >= 0 && rk < n_sel) ? 1.0f : 0.0f;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) *shared_best = 0;
+  __syncthreads();
+  for (int i = tid; i < B; i += blockDim.x) {
+    if (eps_s[i] != 0.0f) {
+      xblk[i] = arg_s[i];
+      atomicAdd(shared_best, 1);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) *count_out = *shared_best;
+}
+
+// LM-head tile statistics -> (conf, arg) per block row, then select/commit.
+// One CTA (256 threads) per sequence.
+struct MergeParams {
+  const float* st_m;
+  const float* st_s;
+  const int* st_a;
+  int v_tiles, n_rows;    // tiles, rows of the stat arrays (= b * B)
+  int B, T, blk_start, mask_id;
+  int32_t* x;             // canvas [b][T]
+  float* conf;            // [b][B]
+  int32_t* arg;           // [b][B]
+  int32_t* count;         // [b]
+  SelectRule rule;
+};
+
+constexpr int kMaxBlock = 256;
+
+__global__ void __launch_bounds__(256) merge_select_kernel(const MergeParams p) {
+  __shared__ float conf_s[kMaxBlock];
+  __shared__ int arg_s[kMaxBlock];
+  __shared__ int rank_s[kMaxBlock];
+  __shared__ float eps_s[kMaxBlock];
+  __shared__ int best;
+  griddep_launch_dependents();
+  griddep_wait();
+  const int seq = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < p.B; i += 8) {
+    const int row = seq * p.B + i;
+    float M = -INFINITY, S = 0.0f;
+    int A = 0x7fffffff;
+    for (int t = lane; t < p.v_tiles; t += 32) {
+      const long long o = (long long)t * p.n_rows + row;
+      const float mt = p.st_m[o], stt = p.st_s[o];
+      const int at = p.st_a[o];
+      const float Mn = fmaxf(M, mt);
+      S = (M == -INFINITY ? 0.0f : S * exp2f((M - Mn) * kLog2e)) + stt * exp2f((mt - Mn) * kLog2e);
+      A = (mt > M) ? at : A;   // tiles visited in increasing id order: keep the first maximum
+      M = Mn;
+    }
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const float Mo = __shfl_xor_sync(0xffffffffu, M, s);
+      const float So = __shfl_xor_sync(0xffffffffu, S, s);
+      const int Ao = __shfl_xor_sync(0xffffffffu, A, s);
+      const float Mn = fmaxf(M, Mo);
+      const float Sa = (M == -INFINITY) ? 0.0f : S * exp2f((M - Mn) * kLog2e);
+      const float Sb = (Mo == -INFINITY) ? 0.0f : So * exp2f((Mo - Mn) * kLog2e);
+      // keep the pair order fixed (lower lane first) so every lane sums alike
+      S = (lane & s) ? (Sb + Sa) : (Sa + Sb);
+      A = (Mo > M || (Mo == M && Ao < A)) ? Ao : A;
+      M = Mn;
+    }
+    if (lane == 0) {
+      conf_s[i] = 1.0f / S;
+      arg_s[i] = A;
+      p.conf[(long long)seq * p.B + i] = 1.0f / S;
+      p.arg[(long long)seq * p.B + i] = A;
+    }
+  }
+  __syncthreads();
+  select_commit_cta(conf_s, arg_s, rank_s, eps_s, p.B, p.x + (long long)seq * p.T + p.blk_start, p.mask_id,
+                    p.rule, p.count + seq, &best);
+}
+
+// Standalone select/commit on given confidences (the K7 unit).
+struct SelectParams {
+  const float* conf;
+  const int32_t* arg;
+  int32_t* x;
+  int32_t* count;
+  int T, blk_start, B, mask_id;
+  SelectRule rule;
+};
+
+__global__ void __launch_bounds__(256) select_kernel(const SelectParams p) {
+  __shared__ float conf_s[kMaxBlock];
+  __shared__ int arg_s[kMaxBlock];
+  __shared__ int rank_s[kMaxBlock];
+  __shared__ float eps_s[kMaxBlock];
+  __shared__ int best;
+  const int seq = blockIdx.x;
+  for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+    conf_s[i] = p.conf[(long long)seq * p.B + i];
+    arg_s[i] = p.arg[(long long)seq * p.B + i];
+  }
+  __syncthreads();
+  select_commit_cta(conf_s, arg_s, rank_s, eps_s, p.B, p.x + (long long)seq * p.T + p.blk_start, p.mask_id,
+                    p.rule, p.count + seq, &best);
+}
+
+}  // namespace dllm

@@ -1,0 +1,258 @@
+/*
+ * dllm.h - C ABI of the GB300 (sm_103a) block-cached, confidence-threshold
+ * masked-diffusion decoder.
+ *
+ * The method (Fast-dLLM, as described in the zhongzhuzhou.org reading notes,
+ * sections 3-6, and the dian8dian summary): the answer of length gen_len is
+ * split into blocks of B positions decoded left to right (Algorithm 1).  While
+ * the current block still holds MASK, one denoise step runs a bidirectional
+ * transformer forward over the recomputed rows only - the current block
+ * (DualCache), the block and the suffix (PrefixCache) or every position (no
+ * cache) - reading cached K/V for the other positions; it takes, for every
+ * masked position of the block, the largest softmax probability c_i and the
+ * argmax token y_i over the vocabulary, and commits every position with
+ * c_i >= tau, or only the single most confident one if none qualifies
+ * (Algorithm 2).  A committed token is never changed again.  At each block
+ * boundary a full-sequence forward rewrites every cached K/V in place.
+ *
+ * Conventions
+ *  - Every call returns a dllm_status (dllm_denoise_step returns a count, or a
+ *    negative status).  On failure dllm_last_error() holds a message (per
+ *    thread) and no state has changed unless the text says otherwise.
+ *  - Host pointers are owned by the caller and only read/written during the
+ *    call.  Device memory of models and states is owned by the library and
+ *    freed by dllm_free_model / dllm_free_state.
+ *  - A dllm_state is used by one host thread at a time.  Calls are
+ *    synchronous with respect to the host outputs they return.
+ *  - Token ids are int32 in [0, vocab); the MASK id is `vocab`.
+ *  - The dllm_op_* calls take device pointers, run on the given CUDA stream
+ *    (NULL = legacy default stream) and return after the launch (asynchronous).
+ */
+#ifndef DLLM_H
+#define DLLM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dllm_status {
+    DLLM_OK = 0,
+    DLLM_EINVAL = 1,    /* bad argument; nothing was changed */
+    DLLM_ENOMEM = 2,    /* device or host allocation failed */
+    DLLM_ECUDA = 3,     /* a CUDA runtime/driver call failed */
+    DLLM_EIO = 4,       /* weight file missing, short or malformed */
+    DLLM_ESTATE = 5,    /* a step committed nothing while MASK remained, or the
+                           call does not fit the state (e.g. wrong block) */
+    DLLM_ETIMEOUT = 6   /* a kernel gave up a bounded wait; outputs are invalid */
+} dllm_status;
+
+typedef enum dllm_cache_mode {
+    DLLM_CACHE_NONE = 0,    /* every step recomputes all T positions */
+    DLLM_CACHE_PREFIX = 1,  /* recompute the current block and the suffix */
+    DLLM_CACHE_DUAL = 2     /* recompute only the current block */
+} dllm_cache_mode;
+
+typedef enum dllm_sel_policy {
+    DLLM_SEL_THRESHOLD = 0, /* Algorithm 2: c >= tau, else the single best */
+    DLLM_SEL_FIXED_K = 1,   /* the k most confident (min(k, remaining)) */
+    DLLM_SEL_FACTOR = 2,    /* Algorithm 3 / eq. 13: largest n with (n+1)(1-c_(n)) < f */
+    DLLM_SEL_BUDGET = 3     /* eq. 9: largest prefix with sum eps + max eps < 1 */
+} dllm_sel_policy;
+
+/* Selection rule.  Ties in confidence go to the lowest position, ties in the
+ * argmax to the lowest token id; every comparison is made in float32 on the
+ * float32 confidence.  Only MASK positions of the current block are eligible. */
+typedef struct dllm_select {
+    int32_t policy;   /* dllm_sel_policy */
+    float tau;        /* THRESHOLD: threshold (> 1 gives one token per step) */
+    int32_t k;        /* FIXED_K: tokens per step, >= 1 */
+    float factor;     /* FACTOR: f > 0 */
+} dllm_select;
+
+/* Model shape (LLaMA-style, non-causal, MHA with n_heads * head_dim = d_model,
+ * rotate-half RoPE, RMSNorm, SwiGLU FFN, untied embedding [vocab+1][d] and
+ * LM head [vocab][d]).  head_dim must be 64 or 128; d_model a multiple of 128. */
+typedef struct dllm_config {
+    int32_t n_layers, d_model, n_heads, head_dim, d_ffn, vocab;
+    float rope_theta, norm_eps;
+} dllm_config;
+
+/* Logical weight tensors, row-major [out][in] bf16 (uint16 bit patterns). */
+typedef enum dllm_tensor {
+    DLLM_T_EMBED = 1,       /* [vocab+1][d]  (row `vocab` is MASK)   */
+    DLLM_T_ATTN_NORM = 2,   /* [d]    per layer                        */
+    DLLM_T_WQ = 3,          /* [d][d] per layer, out = head*head_dim+j */
+    DLLM_T_WK = 4,
+    DLLM_T_WV = 5,
+    DLLM_T_WO = 6,          /* [d][d] per layer                        */
+    DLLM_T_FFN_NORM = 7,    /* [d]    per layer                        */
+    DLLM_T_WG = 8,          /* [d_ffn][d] per layer                    */
+    DLLM_T_WU = 9,          /* [d_ffn][d] per layer                    */
+    DLLM_T_WD = 10,         /* [d][d_ffn] per layer                    */
+    DLLM_T_FINAL_NORM = 11, /* [d]                                     */
+    DLLM_T_LM_HEAD = 12     /* [vocab][d]                              */
+} dllm_tensor;
+
+/* Timings and counts of one dllm_run / dllm_generate (eq. 15 of the notes:
+ * T_fast ~ S * C_active + R + T_selection; selection runs inside the step). */
+typedef struct dllm_stats {
+    double wall_ms;       /* whole call, host clock                             */
+    double refresh_ms;    /* R: prefill + block-boundary refreshes (CUDA events) */
+    double step_ms;       /* S * C_active: all denoise steps (CUDA events)       */
+    int32_t steps;        /* S: denoise steps run                                */
+    int32_t refreshes;    /* full-sequence forwards (prefill included)           */
+    int32_t blocks;
+    int32_t max_steps_per_block;
+    int64_t committed;    /* tokens committed over all sequences                 */
+    double tau_bar;       /* committed / sum over sequences of active steps      */
+} dllm_stats;
+
+typedef struct dllm_model dllm_model;
+typedef struct dllm_state dllm_state;
+
+/* ------------------------------------------------------------------ model */
+
+/* Allocate a model's device weights (uninitialised) on the current device.
+ * Fill every tensor with dllm_model_set_tensor before use. */
+dllm_status dllm_model_create(const dllm_config* cfg, dllm_model** out);
+
+/* Copy one logical tensor (count bf16 values, row-major [out][in]) into the
+ * model's device layout.  src is a host pointer (src_on_device = 0) or a
+ * device pointer (1).  count must equal the tensor's element count. */
+dllm_status dllm_model_set_tensor(dllm_model* m, int32_t tensor, int32_t layer,
+                                  const uint16_t* src, int64_t count, int32_t src_on_device);
+
+/* Read a weight file (8-byte magic "DLLMW001", int32 n_layers, d_model,
+ * n_heads, head_dim, d_ffn, vocab, float32 rope_theta, norm_eps, then every
+ * tensor's bf16 bits: embed; per layer attn_norm wq wk wv wo ffn_norm wg wu wd;
+ * final_norm; lm_head) and upload it.  DLLM_EIO on a short/malformed file. */
+dllm_status dllm_load(const char* path, dllm_model** out);
+
+dllm_status dllm_model_config(const dllm_model* m, dllm_config* cfg);
+void dllm_free_model(dllm_model* m);
+
+/* ------------------------------------------------------------------ state */
+
+/* Create the decoding state of b sequences: canvas x = prompt ++ MASK*gen_len
+ * (Algorithm 1, step 1), K/V cache [layer][K|V][b][head][T][head_dim] bf16 with
+ * T = P + gen_len, activations and workspaces.  prompts: host [b][P] int32, or
+ * NULL to leave the prompt part for dllm_state_set_prompts_device.
+ * gen_len % block == 0 and 1 <= block <= 256 are required.  cuda_stream is a
+ * cudaStream_t (NULL = create a private stream).  Nothing runs on the GPU. */
+dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, int32_t b, int32_t P,
+                              int32_t gen_len, int32_t block, void* cuda_stream,
+                              dllm_state** out);
+
+/* Reset the canvas to prompt ++ MASK (prompts: host [b][P], or NULL to keep
+ * the current prompt part) and forget the cache contents and counters. */
+dllm_status dllm_state_reset(dllm_state* s, const int32_t* prompts);
+
+/* Copy prompts already on the device ([b][P] int32) into the canvas and reset
+ * the answer part to MASK (stream-ordered, no host synchronisation). */
+dllm_status dllm_state_set_prompts_device(dllm_state* s, const int32_t* prompts_dev);
+
+void dllm_free_state(dllm_state* s);
+
+/* Full-sequence forward over all T positions of the current canvas; writes
+ * every layer's K and V for every position into the cache in place (Algorithm
+ * 1, steps 2 and 11).  Commits nothing; skips the last layer's attention/FFN
+ * and the LM head, which K/V do not need. */
+dllm_status dllm_prefill_refresh(dllm_state* s);
+
+/* One denoise step of block block_idx with the threshold rule (Algorithm 2)
+ * and the given cache mode.  committed_per_seq: host [b] or NULL.  Returns the
+ * total number of tokens committed (>= 0), or -status on error.  A sequence
+ * whose block has no MASK left commits 0.  block_idx must be in
+ * [0, gen_len/block).  The cached modes read whatever the cache holds: call
+ * dllm_prefill_refresh first. */
+int32_t dllm_denoise_step(dllm_state* s, int32_t block_idx, float tau, int32_t cache_mode,
+                          int32_t* committed_per_seq);
+
+/* Same with any selection rule. */
+dllm_status dllm_denoise_step_ex(dllm_state* s, int32_t block_idx, const dllm_select* sel,
+                                 int32_t cache_mode, int32_t* committed_per_seq);
+
+/* Algorithm 1 on the state's canvas: prefill refresh (cached modes), then for
+ * each block, denoise steps until it has no MASK, then a refresh before the
+ * next block (cached modes).  Tokens stay on the device (read them with
+ * dllm_read_state).  refresh_interval > 0 also refreshes after every
+ * refresh_interval steps inside a block (0 = only at block boundaries).
+ * stats may be NULL. */
+dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t cache_mode,
+                     int32_t refresh_interval, dllm_stats* stats);
+
+/* End-to-end call: prompts (host [b][P]) in, answers (host [b][gen_len]) out.
+ * Creates a state on a private stream, runs Algorithm 1 with the threshold
+ * rule, copies the answer back and frees the state. */
+dllm_status dllm_generate(dllm_model* m, const int32_t* prompts, int32_t b, int32_t P,
+                          int32_t gen_len, int32_t block, float tau, int32_t cache_mode,
+                          int32_t* out_tokens, dllm_stats* stats);
+
+/* Copy state to the host: tokens [b][T] (the whole canvas), and the last
+ * step's conf [b][block] (float32 max-softmax) and arg [b][block] (argmax id).
+ * Any pointer may be NULL. */
+dllm_status dllm_read_state(const dllm_state* s, int32_t* tokens, float* conf, int32_t* arg);
+
+/* The last denoise step's residual stream after the last layer for the block
+ * rows, host float32 [b][block][d_model]. */
+dllm_status dllm_read_hidden(const dllm_state* s, float* h);
+
+/* Copy the cached K and V of one layer as float32, host [b][n_heads][T][head_dim] each. */
+dllm_status dllm_read_kv(const dllm_state* s, int32_t layer, float* k, float* v);
+
+/* Record the residual stream after the embedding and after every layer on the
+ * next steps (1) or stop (0).  dllm_read_trace copies the last step's record,
+ * host float32 [n_layers+1][rows][d_model], rows = b * rows_per_seq as
+ * returned.  Tracing adds copies between layers: not for timing. */
+dllm_status dllm_state_set_trace(dllm_state* s, int32_t enable);
+dllm_status dllm_read_trace(const dllm_state* s, float* out, int64_t capacity_floats,
+                            int32_t* rows_per_seq, int32_t* first_pos);
+
+/* Accumulate per-kernel-class device time of the next calls with CUDA events
+ * (enable 1), or stop (0).  dllm_kernel_times returns, per class (0 embed,
+ * 1 qkv_gemm, 2 attention, 3 o_gemm, 4 gateup_gemm, 5 down_gemm, 6 lm_head_gemm,
+ * 7 merge_select), the summed milliseconds, launch counts and algorithmic
+ * bytes.  The events serialise the kernels: not for the headline time. */
+dllm_status dllm_state_set_kernel_timing(dllm_state* s, int32_t enable);
+dllm_status dllm_kernel_times(const dllm_state* s, double* ms, int64_t* launches,
+                              double* bytes, int32_t n_classes);
+
+/* ------------------------------------------------------------------ kernels */
+
+/* Y[N][M] (float32) = X[N][K] * W[M][K]^T on the tensor cores (tcgen05, TMA,
+ * stream-K split with a deterministic fix-up).  W, X bf16 row-major, 16-byte
+ * aligned, K % 8 == 0.  Uses a library-owned workspace allocated on first use. */
+dllm_status dllm_op_gemm(const uint16_t* W, const uint16_t* X, float* Y, int32_t M, int32_t N,
+                         int32_t K, void* cuda_stream);
+
+/* Non-causal attention, eq. 3: for every sequence s, head h and query row i,
+ * out[s*R+i][h*hd..] = softmax(q k^T / sqrt(hd)) v over the T keys of
+ * k_cache/v_cache [b][H][T][hd].  q: [b*R][H][hd] bf16, out [b*R][H*hd] bf16.
+ * hd in {64, 128}.  Splits the keys across CTAs and merges the partial
+ * softmax states deterministically (library-owned workspace). */
+dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                              uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R,
+                              int32_t T, void* cuda_stream);
+
+/* The selection/commit kernel alone: given conf [b][B] float32 and arg [b][B]
+ * int32 (device), select on the MASK positions x[s][blk_start .. +B) of the
+ * canvas x [b][T] (device int32), write the chosen arg ids into x and the
+ * per-sequence counts into count [b] (device). */
+dllm_status dllm_op_select_commit(const float* conf, const int32_t* arg, int32_t* x,
+                                  int32_t b, int32_t T, int32_t blk_start, int32_t B,
+                                  int32_t mask_id, const dllm_select* sel, int32_t* count,
+                                  void* cuda_stream);
+
+/* ------------------------------------------------------------------ misc */
+
+const char* dllm_last_error(void);
+const char* dllm_status_string(int32_t status);
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t dllm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLLM_H */

@@ -1,0 +1,108 @@
+"""Trajectory comparison of the GPU decoder against the CPU oracle.
+
+Trajectory-sync rule: at every step the oracle recomputes the step from the
+GPU's canvas.  The GPU's per-position max-prob must match the oracle within
+2e-3 and its argmax must match unless the oracle's top-1/top-2 logit margin is
+below 2e-3; the GPU's commit must be exactly the selection rule applied to
+the GPU's own confidences; where the oracle's own confidences would select
+differently, the oracle's decision must sit within 2e-3 of a decision boundary
+(a near tie, counted and reported).  The oracle then adopts the GPU's commit
+and both continue.
+"""
+import numpy as np
+
+from cached_masked_decoding_gb300 import binding
+from oracle import sampler as OS
+
+TOL = 2e-3
+
+
+def to_gpu_rule(rule: OS.Rule):
+    return binding.make_select(rule.policy, rule.tau, rule.k, rule.factor)
+
+
+def decision_margin(rule: OS.Rule, conf: np.ndarray, elig: np.ndarray) -> float:
+    """Distance (in confidence) of the rule's decision from its nearest boundary."""
+    c = np.sort(conf[elig].astype(np.float64))[::-1]
+    if c.size == 0:
+        return np.inf
+    gaps = np.diff(c) * -1 if c.size > 1 else np.array([np.inf])
+    rank_gap = float(gaps.min()) if gaps.size else np.inf
+    if rule.policy == OS.THRESHOLD:
+        return min(float(np.abs(c - rule.tau).min()), rank_gap)
+    if rule.policy == OS.FIXED_K:
+        return rank_gap
+    if rule.policy == OS.FACTOR:
+        n = np.arange(1, c.size + 1)
+        return min(float(np.abs((n + 1) * (1 - c) - rule.factor).min() / (c.size + 1)), rank_gap)
+    e = 1 - c
+    cs = np.cumsum(e)
+    return min(float(np.abs(cs + e - 1).min() / (c.size + 1)), rank_gap)
+
+
+class Report:
+    def __init__(self):
+        self.steps = 0
+        self.decisions = 0
+        self.near_ties = 0
+        self.arg_near_ties = 0
+        self.max_conf_err = 0.0
+        self.max_hidden_rel = 0.0
+
+    def __repr__(self):
+        return (f"steps={self.steps} decisions={self.decisions} near_ties={self.near_ties} "
+                f"arg_near_ties={self.arg_near_ties} max_conf_err={self.max_conf_err:.2e} "
+                f"max_hidden_rel={self.max_hidden_rel:.2e}")
+
+
+def run_synced(gpu: binding.State, dec: OS.Decoder, rule: OS.Rule, mode: str, check_hidden: bool = True,
+               max_steps: int | None = None) -> Report:
+    rep = Report()
+    grule = to_gpu_rule(rule)
+    mask = dec.cfg.mask_id
+    cached = mode != "none"
+    if cached:
+        gpu.refresh()
+        dec.refresh()
+    for j in range(dec.n_blocks):
+        s = dec.block_start(j)
+        while True:
+            x_before = gpu.tokens()
+            np.testing.assert_array_equal(x_before, dec.x, err_msg="trajectories out of sync")
+            elig = x_before[:, s:s + dec.B] == mask
+            if not elig.any():
+                break
+            gpu.step_ex(j, grule, mode)
+            x_after, conf_g, arg_g = gpu.read()
+            conf_o, arg_o, margin, hb, _ = dec.compute(j)
+            rep.steps += 1
+            err = np.abs(conf_g.astype(np.float64) - conf_o)[elig]
+            rep.max_conf_err = max(rep.max_conf_err, float(err.max()))
+            assert err.max() <= TOL, f"block {j} step {rep.steps}: max-prob error {err.max():.3e}"
+            mism = elig & (arg_g != arg_o)
+            assert (margin[mism] < TOL).all(), f"argmax differs at a clear margin: {margin[mism]}"
+            rep.arg_near_ties += int(mism.sum())
+            if check_hidden:
+                hg = gpu.hidden().astype(np.float64)
+                rel = np.linalg.norm(hg - hb, axis=-1) / np.linalg.norm(hb, axis=-1)
+                rep.max_hidden_rel = max(rep.max_hidden_rel, float(rel.max()))
+                assert rel.max() <= 1e-2, f"final hidden relative error {rel.max():.3e}"
+            for i in range(dec.b):
+                sel_g = OS.select(rule, conf_g[i], elig[i])
+                expect = x_before[i].copy()
+                expect[s + np.flatnonzero(sel_g)] = arg_g[i, np.flatnonzero(sel_g)]
+                np.testing.assert_array_equal(x_after[i], expect, err_msg="commit is not the rule on GPU conf")
+                sel_o = OS.select(rule, conf_o[i].astype(np.float32), elig[i])
+                rep.decisions += int(elig[i].sum())
+                if not np.array_equal(sel_o, sel_g):
+                    dm = decision_margin(rule, conf_o[i], elig[i])
+                    assert dm < TOL + rep.max_conf_err, \
+                        f"selection differs with decision margin {dm:.3e} (seq {i}, block {j})"
+                    rep.near_ties += 1
+            dec.x = x_after.astype(np.int64).copy()
+            if max_steps is not None and rep.steps >= max_steps:
+                return rep
+        if cached and j + 1 < dec.n_blocks:
+            gpu.refresh()
+            dec.refresh()
+    return rep

@@ -1,0 +1,229 @@
+"""Model-level parity on the GPU: the refresh K/V, one step per cache mode
+layer by layer, whole trajectories under the trajectory-sync rule for every
+selection rule, determinism, batching and edge cases (tiny model)."""
+import numpy as np
+import pytest
+
+from cached_masked_decoding_gb300 import binding, configs, synth
+from gpu_util import torch_cuda
+from oracle import model as OM
+from oracle import sampler as OS
+from parity import run_synced
+
+pytestmark = pytest.mark.gpu
+
+CFG = configs.TINY_SPREAD
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = torch_cuda()
+    binding.lib()
+    return t
+
+
+@pytest.fixture(scope="module")
+def gmodel(torch):
+    m = binding.Model.from_synth(CFG, seed=0, random_norms=True)
+    yield m
+    m.free()
+
+
+@pytest.fixture(scope="module")
+def omodel():
+    return OM.load_weights(CFG, 0, random_norms=True)
+
+
+def test_refresh_writes_oracle_kv(gmodel, omodel):
+    P, gen, B = 32, 64, 16
+    pr = synth.prompts(CFG, 0, 2, P)
+    st = binding.State(gmodel, pr, 2, P, gen, B)
+    st.refresh()
+    dec = OS.Decoder(omodel, pr, gen, B, "dual")
+    dec.refresh()
+    for l in range(CFG.n_layers):
+        k, v = st.kv(l)
+        for i in range(2):
+            ko = dec.k_cache[i][l].transpose(1, 0, 2)   # [H][T][hd]
+            vo = dec.v_cache[i][l].transpose(1, 0, 2)
+            for got, ref in ((k[i], ko), (v[i], vo)):
+                rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+                assert rel < 1e-2, f"layer {l} seq {i}: relative K/V error {rel:.3e}"
+    st.free()
+
+
+@pytest.mark.parametrize("mode", ["dual", "prefix", "none"])
+def test_one_step_layer_by_layer(gmodel, omodel, mode):
+    P, gen, B = 32, 64, 16
+    pr = synth.prompts(CFG, 0, 1, P)
+    st = binding.State(gmodel, pr, 1, P, gen, B)
+    st.set_trace(True)
+    dec = OS.Decoder(omodel, pr, gen, B, mode)
+    if mode != "none":
+        st.refresh()
+        dec.refresh()
+    cnt = st.step(0, 0.9, mode)
+    tr, R, p0 = st.trace()
+    conf_o, arg_o, margin, hb, layers = dec.compute(0, keep_layers=True)
+    rows = dec.rows_of(0)
+    assert R == rows.size and p0 == rows[0]
+    for l, ref in enumerate(layers[0]):
+        got = tr[l, 0].astype(np.float64)
+        rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+        assert rel.max() < 1e-2, f"{mode}: layer {l} output relative error {rel.max():.3e}"
+    _, conf_g, arg_g = st.read()
+    assert np.abs(conf_g[0] - conf_o[0]).max() <= 2e-3
+    assert ((arg_g[0] == arg_o[0]) | (margin[0] < 2e-3)).all()
+    assert cnt.sum() >= 1
+    st.free()
+
+
+RULES = {
+    "threshold": OS.Rule(OS.THRESHOLD, 0.9),
+    "tau_gt_1": OS.Rule(OS.THRESHOLD, 1.5),
+    "fixed1": OS.Rule(OS.FIXED_K, k=1),
+    "fixed4": OS.Rule(OS.FIXED_K, k=4),
+    "factor": OS.Rule(OS.FACTOR, factor=1.0),
+    "budget": OS.Rule(OS.BUDGET),
+}
+
+
+@pytest.mark.parametrize("mode", ["dual", "prefix", "none"])
+@pytest.mark.parametrize("rule", ["threshold", "fixed4", "factor"])
+def test_trajectory_matches_oracle(gmodel, omodel, mode, rule):
+    P, gen, B = 32, 64, 16
+    pr = synth.prompts(CFG, 0, 1, P)
+    st = binding.State(gmodel, pr, 1, P, gen, B)
+    dec = OS.Decoder(omodel, pr, gen, B, mode)
+    rep = run_synced(st, dec, RULES[rule], mode)
+    print(mode, rule, rep)
+    assert rep.near_ties <= max(2, rep.steps // 10)
+    assert (st.tokens()[:, P:] != CFG.mask_id).all()
+    st.free()
+
+
+@pytest.mark.parametrize("rule", ["tau_gt_1", "fixed1", "budget"])
+def test_other_rules_dual(gmodel, omodel, rule):
+    P, gen, B = 32, 32, 16
+    pr = synth.prompts(CFG, 0, 1, P)
+    st = binding.State(gmodel, pr, 1, P, gen, B)
+    dec = OS.Decoder(omodel, pr, gen, B, "dual")
+    rep = run_synced(st, dec, RULES[rule], "dual")
+    if rule in ("tau_gt_1", "fixed1"):
+        assert rep.steps == gen       # exactly one token per step
+    st.free()
+
+
+def test_stated_tiny_model_x8(torch):
+    cfg = configs.TINY
+    m = binding.Model.from_synth(cfg, seed=0)
+    w = OM.load_weights(cfg, 0)
+    pr = synth.prompts(cfg, 0, 1, 32)
+    st = binding.State(m, pr, 1, 32, 64, 16)
+    dec = OS.Decoder(w, pr, 64, 16, "dual")
+    rep = run_synced(st, dec, OS.Rule(OS.THRESHOLD, 0.9), "dual")
+    assert rep.steps == 64            # x8 never reaches 0.9: one fallback commit per step
+    st.free()
+    m.free()
+
+
+def test_batch_lockstep_and_ragged_prompt(gmodel, omodel):
+    P, gen, B, b = 45, 48, 16, 3
+    pr = synth.prompts(CFG, 3, b, P)
+    st = binding.State(gmodel, pr, b, P, gen, B)
+    dec = OS.Decoder(omodel, pr, gen, B, "dual")
+    rep = run_synced(st, dec, OS.Rule(OS.THRESHOLD, 0.9), "dual")
+    assert rep.steps >= gen // B
+    st.free()
+
+
+def test_run_is_deterministic_and_generate_agrees(gmodel):
+    P, gen, B = 32, 64, 16
+    pr = synth.prompts(CFG, 1, 2, P)
+    outs = []
+    for _ in range(2):
+        st = binding.State(gmodel, pr, 2, P, gen, B)
+        stats = st.run(binding.make_select(binding.SEL_THRESHOLD, 0.9), "dual")
+        t, c, a = st.read()
+        outs.append((t, c, a, stats))
+        st.free()
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+    assert outs[0][3]["steps"] == outs[1][3]["steps"]
+    assert outs[0][3]["committed"] == 2 * gen
+    toks, stats = binding.generate(gmodel, pr, gen, B, 0.9, "dual")
+    np.testing.assert_array_equal(toks, outs[0][0][:, P:])
+    assert stats["steps"] == outs[0][3]["steps"] and stats["tau_bar"] > 0
+
+
+def test_refresh_every_step_equals_no_cache_on_gpu(gmodel):
+    """Refreshing before every step makes DualCache read exactly the no-cache K/V:
+    the trajectories agree (the GPU computes both; near ties aside they match)."""
+    P, gen, B = 32, 32, 16
+    pr = synth.prompts(CFG, 2, 1, P)
+    st = binding.State(gmodel, pr, 1, P, gen, B)
+    st.run(binding.make_select(binding.SEL_THRESHOLD, 0.9), "none")
+    t_none = st.tokens()
+    st.free()
+    st = binding.State(gmodel, pr, 1, P, gen, B)
+    st.run(binding.make_select(binding.SEL_THRESHOLD, 0.9), "dual", refresh_interval=1)
+    t_dual = st.tokens()
+    st.free()
+    assert (t_none == t_dual).mean() > 0.95
+
+
+def test_edge_cases(gmodel, omodel):
+    # one block covering the whole answer (no refresh between blocks)
+    pr = synth.prompts(CFG, 4, 1, 20)
+    st = binding.State(gmodel, pr, 1, 20, 32, 32)
+    dec = OS.Decoder(omodel, pr, 32, 32, "dual")
+    run_synced(st, dec, OS.Rule(OS.THRESHOLD, 0.9), "dual")
+    st.free()
+    # no prompt at all
+    st = binding.State(gmodel, np.zeros((1, 0), dtype=np.int32), 1, 0, 32, 16)
+    dec = OS.Decoder(omodel, np.zeros((1, 0), dtype=np.int64), 32, 16, "prefix")
+    run_synced(st, dec, OS.Rule(OS.THRESHOLD, 0.9), "prefix")
+    st.free()
+    # block of one position: autoregressive-like order
+    st = binding.State(gmodel, pr, 1, 20, 4, 1)
+    dec = OS.Decoder(omodel, pr, 4, 1, "dual")
+    rep = run_synced(st, dec, OS.Rule(OS.THRESHOLD, 0.9), "dual")
+    assert rep.steps == 4
+    st.free()
+    # empty answer: nothing to do
+    st = binding.State(gmodel, pr, 1, 20, 0, 16)
+    stats = st.run(binding.make_select(), "dual")
+    assert stats["steps"] == 0 and stats["committed"] == 0
+    st.free()
+
+
+def test_invalid_arguments_leave_state_unchanged(gmodel):
+    pr = synth.prompts(CFG, 0, 1, 8)
+    with pytest.raises(binding.DllmError) as e:
+        binding.State(gmodel, pr, 1, 8, 30, 16)            # gen_len % block != 0
+    assert e.value.status == binding.EINVAL
+    bad = pr.copy()
+    bad[0, 3] = CFG.vocab                                   # MASK id in the prompt
+    with pytest.raises(binding.DllmError):
+        binding.State(gmodel, bad, 1, 8, 32, 16)
+    st = binding.State(gmodel, pr, 1, 8, 32, 16)
+    before = st.tokens()
+    with pytest.raises(binding.DllmError):
+        st.step(2, 0.9, "dual")                             # block index out of range
+    with pytest.raises(binding.DllmError):
+        st.step(0, float("nan"), "dual")
+    with pytest.raises(binding.DllmError):
+        st.step_ex(0, binding.make_select(binding.SEL_FIXED_K, k=0), "dual")
+    np.testing.assert_array_equal(st.tokens(), before)
+    st.free()
+
+
+def test_weight_file_round_trip(tmp_path, gmodel, torch):
+    path = str(tmp_path / "tiny.bin")
+    synth.write_weight_file(path, CFG, 0, random_norms=True)
+    m2 = binding.Model.load(path)
+    pr = synth.prompts(CFG, 0, 1, 32)
+    a, _ = binding.generate(gmodel, pr, 32, 16, 0.9, "dual")
+    b, _ = binding.generate(m2, pr, 32, 16, 0.9, "dual")
+    np.testing.assert_array_equal(a, b)
+    m2.free()
