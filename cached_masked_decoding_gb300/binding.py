@@ -21,10 +21,12 @@ OK, EINVAL, ENOMEM, ECUDA, EIO, ESTATE, ETIMEOUT = range(7)
 CACHE_NONE, CACHE_PREFIX, CACHE_DUAL = 0, 1, 2
 MODES = {"none": CACHE_NONE, "prefix": CACHE_PREFIX, "dual": CACHE_DUAL}
 SEL_THRESHOLD, SEL_FIXED_K, SEL_FACTOR, SEL_BUDGET = 0, 1, 2, 3
+PREC_SPLIT, PREC_BF16 = 0, 1
 TENSOR_IDS = {"embed": 1, "attn_norm": 2, "wq": 3, "wk": 4, "wv": 5, "wo": 6, "ffn_norm": 7, "wg": 8, "wu": 9,
               "wd": 10, "final_norm": 11, "lm_head": 12}
 KERNEL_CLASSES = ("embed", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lm_head_gemm",
-                  "merge_select")
+                  "merge_select", "refresh_embed", "refresh_qkv_gemm", "refresh_attention", "refresh_o_gemm",
+                  "refresh_gateup_gemm", "refresh_down_gemm", "refresh_unused_6", "refresh_unused_7")
 
 
 class DllmError(RuntimeError):
@@ -48,7 +50,7 @@ class Stats(ctypes.Structure):
     _fields_ = [("wall_ms", ctypes.c_double), ("refresh_ms", ctypes.c_double), ("step_ms", ctypes.c_double),
                 ("steps", ctypes.c_int32), ("refreshes", ctypes.c_int32), ("blocks", ctypes.c_int32),
                 ("max_steps_per_block", ctypes.c_int32), ("committed", ctypes.c_int64),
-                ("tau_bar", ctypes.c_double)]
+                ("tau_bar", ctypes.c_double), ("kernel_launches", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -82,7 +84,9 @@ SIGNATURES = {
     "dllm_read_trace": (_I32, [_P, _P, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "dllm_state_set_kernel_timing": (_I32, [_P, _I32]),
     "dllm_kernel_times": (_I32, [_P, _P, _P, _P, _I32]),
-    "dllm_op_gemm": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
+    "dllm_op_gemm": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _P]),
+    "dllm_state_set_precision": (_I32, [_P, _I32]),
+    "dllm_op_gemm_trace": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _P, ctypes.POINTER(_I32), _P]),
     "dllm_op_attention": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
     "dllm_op_select_commit": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(Select), _P, _P]),
     "dllm_last_error": (ctypes.c_char_p, []),
@@ -253,6 +257,9 @@ class State:
         check(lib().dllm_read_kv(self.h, layer, _ptr(k), _ptr(v)))
         return k, v
 
+    def set_precision(self, mode: str):
+        check(lib().dllm_state_set_precision(self.h, {"split": PREC_SPLIT, "bf16": PREC_BF16}[mode]))
+
     def set_trace(self, on: bool):
         check(lib().dllm_state_set_trace(self.h, 1 if on else 0))
 
@@ -299,9 +306,19 @@ def generate(model: Model, prompts: np.ndarray, gen_len: int, block: int, tau: f
     return out, st.as_dict()
 
 
-def op_gemm(W_ptr: int, X_ptr: int, Y_ptr: int, M: int, N: int, K: int, stream: int = 0):
-    check(lib().dllm_op_gemm(ctypes.c_void_p(W_ptr), ctypes.c_void_p(X_ptr), ctypes.c_void_p(Y_ptr), M, N, K,
+def op_gemm(W_ptr: int, X_ptr: int, Y_ptr: int, M: int, N: int, K: int, stream: int = 0, X_lo_ptr: int = 0):
+    check(lib().dllm_op_gemm(ctypes.c_void_p(W_ptr), ctypes.c_void_p(X_ptr),
+                             ctypes.c_void_p(X_lo_ptr) if X_lo_ptr else None, ctypes.c_void_p(Y_ptr), M, N, K,
                              ctypes.c_void_p(stream)))
+
+
+def op_gemm_trace(W_ptr: int, X_ptr: int, Y_ptr: int, M: int, N: int, K: int, trace_ptr: int, stream: int = 0,
+                  X_lo_ptr: int = 0) -> int:
+    grid = ctypes.c_int32()
+    check(lib().dllm_op_gemm_trace(ctypes.c_void_p(W_ptr), ctypes.c_void_p(X_ptr),
+                                   ctypes.c_void_p(X_lo_ptr) if X_lo_ptr else None, ctypes.c_void_p(Y_ptr), M, N, K,
+                                   ctypes.c_void_p(trace_ptr), ctypes.byref(grid), ctypes.c_void_p(stream)))
+    return grid.value
 
 
 def op_attention(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, b: int, H: int, hd: int, R: int, T: int,

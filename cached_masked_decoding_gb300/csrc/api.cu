@@ -146,10 +146,10 @@ dllm_status map_kv(CUtensorMap* m, const void* base, uint64_t hd, uint64_t T, ui
 int round_up(int a, int b) { return (a + b - 1) / b * b; }
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-int pick_bn(int n) {
+int pick_bn(int n, bool split = false) {
   if (n <= 32) return 32;
   if (n <= 64) return 64;
-  if (n <= 128) return 128;
+  if (n <= 128 || split) return 128;
   return 256;
 }
 
@@ -171,9 +171,12 @@ AttnPlan plan_attention(int b, int H, int R, int T, int sms) {
   a.q_tiles = ceil_div(R, QT);
   const long long items = (long long)b * H * a.q_tiles;
   const int max_splits = std::max(1, ceil_div(T, 64));
+  // about two CTAs per SM; at most 32 splits (the merge keeps QT x splits
+  // weights in shared memory)
   int splits = 1;
-  const long long target = 3LL * sms;
-  if (items < target) splits = std::min<long long>(max_splits, (target + items - 1) / items);
+  const long long target = 2LL * sms;
+  if (items < target) splits = (int)std::min<long long>(max_splits, (target + items - 1) / items);
+  splits = std::min(splits, 32);
   a.kps = round_up(ceil_div(T, splits), 64);
   a.splits = ceil_div(T, a.kps);
   return a;
@@ -442,7 +445,8 @@ extern "C" dllm_status dllm_load(const char* path, dllm_model** out) {
 }
 
 // ====================================================================== state
-enum KClass { KC_EMBED = 0, KC_QKV, KC_ATTN, KC_O, KC_GU, KC_D, KC_LM, KC_MERGE, KC_N };
+// kernel classes of a denoise step; a refresh's launches use class + KC_REFRESH
+enum KClass { KC_EMBED = 0, KC_QKV, KC_ATTN, KC_O, KC_GU, KC_D, KC_LM, KC_MERGE, KC_REFRESH = 8, KC_N = 16 };
 
 struct dllm_state {
   dllm_model* m = nullptr;
@@ -454,17 +458,23 @@ struct dllm_state {
   uint16_t* kv = nullptr;
   float* h = nullptr;
   uint16_t* xn = nullptr;
+  uint16_t* xn_lo = nullptr;
   float* ss = nullptr;
   uint16_t* q = nullptr;
   uint16_t* ao = nullptr;
+  uint16_t* ao_lo = nullptr;
   uint16_t* act = nullptr;
+  uint16_t* act_lo = nullptr;
   uint16_t* xf = nullptr;
+  uint16_t* xf_lo = nullptr;
+  bool split = true;              // activations as hi/lo bf16 pairs
   float* ssf = nullptr;
   float *st_m = nullptr, *st_s = nullptr;
   int* st_a = nullptr;
   float* conf = nullptr;
   int32_t* arg = nullptr;
   int32_t* count_err = nullptr;   // [b] counts, then the error word
+  int* seq_done = nullptr;        // [b] merge arrival counters
   float* gemm_ws = nullptr;
   int* gemm_cnt = nullptr;
   float* attn_o = nullptr;
@@ -489,8 +499,8 @@ struct dllm_state {
   double kt_ms[KC_N] = {0};
   long long kt_n[KC_N] = {0};
   double kt_bytes[KC_N] = {0};
-  double pend_bytes[64] = {0};
   cudaEvent_t ev_a = nullptr, ev_b = nullptr;
+  long long launches = 0;         // kernels launched by this state
 };
 
 namespace {
@@ -564,7 +574,7 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
   const size_t T = s->T, n_max = (size_t)b * T, n_lm = (size_t)b * block;
   const size_t v_tiles = (V + 127) / 128, d_tiles = d / 128;
   // fix-up counters: the largest tile grid of any GEMM of this state
-  auto nt = [&](size_t n) { return (n + pick_bn((int)n) - 1) / pick_bn((int)n); };
+  auto nt = [&](size_t n) { return (n + pick_bn((int)n, true) - 1) / pick_bn((int)n, true); };
   size_t cnt_n = std::max({(3 * d / 128) * nt(n_max), (2 * F / 128) * nt(n_max), (d / 128) * nt(n_max),
                            v_tiles * nt(n_lm)});
   // attention workspace: the largest plan among the row counts this state can use
@@ -585,12 +595,12 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
   const size_t o_x = total; total += al(n_max * 4);
   const size_t o_kv = total; total += al(L * 2 * b * H * T * hd * 2);
   const size_t o_h = total; total += al(n_max * d * 4);
-  const size_t o_xn = total; total += al(n_max * d * 2);
+  const size_t o_xn = total; total += al(2 * n_max * d * 2);
   const size_t o_ss = total; total += al(n_max * d_tiles * 4);
   const size_t o_q = total; total += al(n_max * d * 2);
-  const size_t o_ao = total; total += al(n_max * d * 2);
-  const size_t o_act = total; total += al(n_max * F * 2);
-  const size_t o_xf = total; total += al(n_lm * d * 2);
+  const size_t o_ao = total; total += al(2 * n_max * d * 2);
+  const size_t o_act = total; total += al(2 * n_max * F * 2);
+  const size_t o_xf = total; total += al(2 * n_lm * d * 2);
   const size_t o_ssf = total; total += al(n_lm * d_tiles * 4);
   const size_t o_stm = total; total += al(v_tiles * n_lm * 4);
   const size_t o_sts = total; total += al(v_tiles * n_lm * 4);
@@ -598,6 +608,7 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
   const size_t o_conf = total; total += al(n_lm * 4);
   const size_t o_arg = total; total += al(n_lm * 4);
   const size_t o_ce = total; total += al((b + 1) * 4);
+  const size_t o_sd = total; total += al(b * 4);
   const size_t o_gc = total; total += al(cnt_n * 4);
   const size_t o_ao2 = total; total += al(attn_floats * 4);
   const size_t o_ac = total; total += al(attn_cnt * 4);
@@ -619,11 +630,15 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
   s->kv = reinterpret_cast<uint16_t*>(a + o_kv);
   s->h = reinterpret_cast<float*>(a + o_h);
   s->xn = reinterpret_cast<uint16_t*>(a + o_xn);
+  s->xn_lo = s->xn + n_max * d;
   s->ss = reinterpret_cast<float*>(a + o_ss);
   s->q = reinterpret_cast<uint16_t*>(a + o_q);
   s->ao = reinterpret_cast<uint16_t*>(a + o_ao);
+  s->ao_lo = s->ao + n_max * d;
   s->act = reinterpret_cast<uint16_t*>(a + o_act);
+  s->act_lo = s->act + n_max * F;
   s->xf = reinterpret_cast<uint16_t*>(a + o_xf);
+  s->xf_lo = s->xf + n_lm * d;
   s->ssf = reinterpret_cast<float*>(a + o_ssf);
   s->st_m = reinterpret_cast<float*>(a + o_stm);
   s->st_s = reinterpret_cast<float*>(a + o_sts);
@@ -631,6 +646,7 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
   s->conf = reinterpret_cast<float*>(a + o_conf);
   s->arg = reinterpret_cast<int32_t*>(a + o_arg);
   s->count_err = reinterpret_cast<int32_t*>(a + o_ce);
+  s->seq_done = reinterpret_cast<int*>(a + o_sd);
   s->gemm_cnt = reinterpret_cast<int*>(a + o_gc);
   s->attn_o = reinterpret_cast<float*>(a + o_ao2);
   s->attn_ml = s->attn_o;   // carved per launch from the same block (see run_attention)
@@ -731,6 +747,7 @@ extern "C" dllm_status dllm_state_set_prompts_device(dllm_state* s, const int32_
   const int grid = (int)std::min<long long>((n + 255) / 256, 4096);
   set_prompts_kernel<<<grid, 256, 0, s->st>>>(s->x, prompts_dev, s->b, s->P, s->T, s->m->cfg.vocab);
   CK(cudaGetLastError());
+  ++s->launches;
   return DLLM_OK;
 }
 
@@ -757,7 +774,6 @@ struct Timed {
       e1 = next_event(s);
       cudaEventRecord(e0, s->st);
       s->pending.push_back({cls, {e0, e1}});
-      if (s->pending.size() <= 64) s->pend_bytes[s->pending.size() - 1] = bytes;
     }
   }
   ~Timed() {
@@ -787,12 +803,34 @@ const CUtensorMap* act_map(dllm_state* s, const void* base, int K, int N, int BN
   return &(s->act_maps[key] = m);
 }
 
-dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int K, const uint16_t* X, int N,
-                     GemmParams p, int cls, double bytes) {
-  const int BN = pick_bn(N);
+// Same L1/shared split for the small kernels as for the GEMM and attention.
+dllm_status pin_carveouts() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    const void* ks[] = {(const void*)embed_kernel, (const void*)merge_select_kernel};
+    for (const void* k : ks) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) err = e;
+    }
+  });
+  CK(err);
+  return DLLM_OK;
+}
+
+dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int K, const uint16_t* X,
+                     const uint16_t* X_lo, int N, GemmParams p, int cls, double bytes) {
+  const int BN = pick_bn(N, s->split);
   dllm_status st = DLLM_OK;
   const CUtensorMap* tmB = act_map(s, X, K, N, BN, &st);
   if (!tmB) return st;
+  const CUtensorMap* tmBlo = tmB;
+  if (s->split) {
+    tmBlo = act_map(s, X_lo, K, N, BN, &st);
+    if (!tmBlo) return st;
+  }
+  p.split = s->split ? 1 : 0;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -806,18 +844,20 @@ dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int
   const int grid = (int)std::min<long long>(s->m->sms, p.total);
   if (s->timing) s->kt_bytes[cls] += bytes;
   Timed t(s, cls, bytes);
-  CK(launch_gemm(kind, BN, tmA, *tmB, p, grid, s->st, true));
+  CK(launch_gemm(kind, BN, tmA, *tmB, *tmBlo, p, grid, s->st, true));
+  ++s->launches;
   return DLLM_OK;
 }
 
-dllm_status run_attention(dllm_state* s, int layer, int R, double bytes) {
+dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes) {
   const dllm_config& c = s->m->cfg;
   AttnPlan a = plan_attention(s->b, c.n_heads, R, s->T, s->m->sms);
   const int QT = 16 * a.wq;
   const long long works = (long long)s->b * c.n_heads * a.q_tiles;
-  AttnParams p;
+  AttnParams p = {};
   p.q = s->q;
   p.o = s->ao;
+  p.o_lo = s->split ? s->ao_lo : nullptr;
   p.R = R;
   p.b = s->b;
   p.H = c.n_heads;
@@ -832,10 +872,11 @@ dllm_status run_attention(dllm_state* s, int layer, int R, double bytes) {
   p.ws_ml = s->attn_o + works * a.splits * QT * c.head_dim;
   p.counters = s->attn_cnt;
   p.err = s->count_err + s->b;
-  if (s->timing) s->kt_bytes[KC_ATTN] += bytes;
-  Timed t(s, KC_ATTN, bytes);
+  if (s->timing) s->kt_bytes[cls] += bytes;
+  Timed t(s, cls, bytes);
   CK(launch_attention(c.head_dim, a.wq, s->tm_kv, s->tm_kv, p, dim3(a.splits, a.q_tiles * c.n_heads, s->b), s->st,
                       true));
+  ++s->launches;
   return DLLM_OK;
 }
 
@@ -848,14 +889,18 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
   const int d = c.d_model, L = c.n_layers, F = m->F_pad, V = c.vocab;
   const int n = s->b * R, n_lm = s->b * s->B;
   const double wb = 2.0;  // bf16
+  const int co = refresh ? KC_REFRESH : 0;
+  CKS(pin_carveouts());
   s->last_row0 = row0;
   s->last_R = R;
   s->last_blk = blk;
   {
-    EmbedParams e{s->x, m->embed, m->layers[0].attn_norm, s->h, s->xn, s->ss, d, R, row0, s->T};
-    Timed t(s, KC_EMBED, (double)n * d * (2 + 4 + 2));
-    if (s->timing) s->kt_bytes[KC_EMBED] += (double)n * d * 8;
+    EmbedParams e{s->x, m->embed, m->layers[0].attn_norm, s->h, s->xn, s->split ? s->xn_lo : nullptr, s->ss,
+                  d, R, row0, s->T};
+    Timed t(s, co + KC_EMBED, (double)n * d * (2 + 4 + 2));
+    if (s->timing) s->kt_bytes[co + KC_EMBED] += (double)n * d * 8;
     CK(launch_ex(embed_kernel, dim3(n), dim3(d / 8), 0, s->st, true, e));
+    ++s->launches;
   }
   if (s->trace) CK(cudaMemcpyAsync(s->trace_buf, s->h, (size_t)n * d * 4, cudaMemcpyDeviceToDevice, s->st));
   const double kv_bytes = (double)s->b * s->T * d * 2 * 2;
@@ -878,10 +923,10 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
     p.T_pad = s->T;
     p.b_seqs = s->b;
     p.layer = l;
-    CKS(run_gemm(s, GEMM_QKV, w.tm_qkv, 3 * d, d, s->xn, n, p, KC_QKV,
+    CKS(run_gemm(s, GEMM_QKV, w.tm_qkv, 3 * d, d, s->xn, s->xn_lo, n, p, co + KC_QKV,
                  3.0 * d * d * wb + (double)n * d * wb * 4));
     if (refresh && last) break;
-    CKS(run_attention(s, l, R, kv_bytes + (double)n * d * wb * 2));
+    CKS(run_attention(s, l, R, co + KC_ATTN, kv_bytes + (double)n * d * wb * 2));
     GemmParams o = {};
     o.R = R;
     o.row0 = row0;
@@ -889,8 +934,9 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
     o.h = s->h;
     o.g_next = w.ffn_norm;
     o.xn_out = s->xn;
+    o.xn_out_lo = s->split ? s->xn_lo : nullptr;
     o.ss_out = s->ss;
-    CKS(run_gemm(s, GEMM_RESID, w.tm_o, d, d, s->ao, n, o, KC_O,
+    CKS(run_gemm(s, GEMM_RESID, w.tm_o, d, d, s->ao, s->ao_lo, n, o, co + KC_O,
                  (double)d * d * wb + (double)n * d * (wb + 8 + wb)));
     GemmParams gu = {};
     gu.ss_in = s->ss;
@@ -898,8 +944,9 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
     gu.inv_d = 1.0f / d;
     gu.eps = c.norm_eps;
     gu.act = s->act;
+    gu.act_lo = s->split ? s->act_lo : nullptr;
     gu.act_ld = F;
-    CKS(run_gemm(s, GEMM_SWIGLU, w.tm_gu, 2 * F, d, s->xn, n, gu, KC_GU,
+    CKS(run_gemm(s, GEMM_SWIGLU, w.tm_gu, 2 * F, d, s->xn, s->xn_lo, n, gu, co + KC_GU,
                  2.0 * F * d * wb + (double)n * (d + F) * wb));
     GemmParams dn = {};
     dn.R = R;
@@ -909,6 +956,7 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
     if (last) {
       dn.g_next = m->final_norm;
       dn.xn_out = s->xf;
+      dn.xn_out_lo = s->split ? s->xf_lo : nullptr;
       dn.ss_out = s->ssf;
       dn.remap = 1;
       dn.blk_start = blk;
@@ -916,9 +964,10 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
     } else {
       dn.g_next = m->layers[l + 1].attn_norm;
       dn.xn_out = s->xn;
+      dn.xn_out_lo = s->split ? s->xn_lo : nullptr;
       dn.ss_out = s->ss;
     }
-    CKS(run_gemm(s, GEMM_RESID, w.tm_d, d, F, s->act, n, dn, KC_D,
+    CKS(run_gemm(s, GEMM_RESID, w.tm_d, d, F, s->act, s->act_lo, n, dn, co + KC_D,
                  (double)d * F * wb + (double)n * (F * wb + 8.0 * d + wb * d)));
     if (s->trace)
       CK(cudaMemcpyAsync(s->trace_buf + (size_t)(l + 1) * n * d, s->h, (size_t)n * d * 4, cudaMemcpyDeviceToDevice,
@@ -933,8 +982,8 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
   lm.st_m = s->st_m;
   lm.st_s = s->st_s;
   lm.st_a = s->st_a;
-  CKS(run_gemm(s, GEMM_LMHEAD, m->tm_lm, V, d, s->xf, n_lm, lm, KC_LM, (double)V * d * wb + (double)n_lm * d * wb));
-  MergeParams mp;
+  CKS(run_gemm(s, GEMM_LMHEAD, m->tm_lm, V, d, s->xf, s->xf_lo, n_lm, lm, KC_LM, (double)V * d * wb + (double)n_lm * d * wb));
+  MergeParams mp = {};
   mp.st_m = s->st_m;
   mp.st_s = s->st_s;
   mp.st_a = s->st_a;
@@ -948,11 +997,13 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
   mp.conf = s->conf;
   mp.arg = s->arg;
   mp.count = s->count_err;
+  mp.seq_done = s->seq_done;
   mp.rule = rule;
   {
     Timed t(s, KC_MERGE, (double)mp.v_tiles * n_lm * 12);
     if (s->timing) s->kt_bytes[KC_MERGE] += (double)mp.v_tiles * n_lm * 12;
-    CK(launch_ex(merge_select_kernel, dim3(s->b), dim3(256), 0, s->st, true, mp));
+    CK(launch_ex(merge_select_kernel, dim3(n_lm), dim3(256), 0, s->st, true, mp));
+    ++s->launches;
   }
   return DLLM_OK;
 }
@@ -1088,6 +1139,7 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
     return DLLM_EINVAL;
   }
   const auto t0 = std::chrono::steady_clock::now();
+  const long long launches0 = s->launches;
   double refresh_ms = 0, step_ms = 0;
   int steps = 0, refreshes = 0, max_spb = 0;
   long long committed = 0, active = 0;
@@ -1136,6 +1188,7 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
     stats->max_steps_per_block = max_spb;
     stats->committed = committed;
     stats->tau_bar = active > 0 ? (double)committed / (double)active : 0.0;
+    stats->kernel_launches = s->launches - launches0;
   }
   return DLLM_OK;
 }
@@ -1216,6 +1269,15 @@ extern "C" dllm_status dllm_read_kv(const dllm_state* s, int32_t layer, float* k
       std::memcpy(&dst[i], &u, 4);
     }
   }
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode) {
+  if (!s || (mode != DLLM_PREC_SPLIT && mode != DLLM_PREC_BF16)) {
+    set_error("bad precision mode %d", mode);
+    return DLLM_EINVAL;
+  }
+  s->split = mode == DLLM_PREC_SPLIT;
   return DLLM_OK;
 }
 
@@ -1336,15 +1398,27 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
-extern "C" dllm_status dllm_op_gemm(const uint16_t* W, const uint16_t* X, float* Y, int32_t M, int32_t N, int32_t K,
-                                    void* stream) {
-  if (!W || !X || !Y || M < 1 || N < 1 || K < 8 || K % 8 != 0 || !aligned16(W) || !aligned16(X)) {
+extern "C" dllm_status dllm_op_gemm_trace(const uint16_t* W, const uint16_t* X, const uint16_t* X_lo, float* Y,
+                                          int32_t M, int32_t N, int32_t K, uint64_t* trace, int32_t* grid_out,
+                                          void* stream);
+
+extern "C" dllm_status dllm_op_gemm(const uint16_t* W, const uint16_t* X, const uint16_t* X_lo, float* Y, int32_t M,
+                                    int32_t N, int32_t K, void* stream) {
+  return dllm_op_gemm_trace(W, X, X_lo, Y, M, N, K, nullptr, nullptr, stream);
+}
+
+extern "C" dllm_status dllm_op_gemm_trace(const uint16_t* W, const uint16_t* X, const uint16_t* X_lo, float* Y,
+                                          int32_t M, int32_t N, int32_t K, uint64_t* trace, int32_t* grid_out,
+                                          void* stream) {
+  if (!W || !X || !Y || M < 1 || N < 1 || K < 8 || K % 8 != 0 || !aligned16(W) || !aligned16(X) ||
+      (X_lo && !aligned16(X_lo))) {
     set_error("bad gemm arguments: M=%d N=%d K=%d (K %% 8 == 0, 16-byte aligned operands)", M, N, K);
     return DLLM_EINVAL;
   }
   std::lock_guard<std::mutex> lk(g_op_mu);
-  const int BN = pick_bn(N);
+  const int BN = pick_bn(N, X_lo != nullptr);
   GemmParams p = {};
+  p.split = X_lo != nullptr;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -1359,11 +1433,15 @@ extern "C" dllm_status dllm_op_gemm(const uint16_t* W, const uint16_t* X, float*
   p.err = w->err;
   p.y = Y;
   p.ldy = M;
-  CUtensorMap ta, tb;
+  p.trace = reinterpret_cast<unsigned long long*>(trace);
+  CUtensorMap ta, tb, tbl;
   CKS(map_2d(&ta, W, K, M, 128));
   CKS(map_2d(&tb, X, K, N, BN));
+  tbl = tb;
+  if (X_lo) CKS(map_2d(&tbl, X_lo, K, N, BN));
   const int grid = (int)std::min<long long>(device_sms(), p.total);
-  CK(launch_gemm(GEMM_PLAIN, BN, ta, tb, p, grid, static_cast<cudaStream_t>(stream), false));
+  if (grid_out) *grid_out = grid;
+  CK(launch_gemm(GEMM_PLAIN, BN, ta, tb, tbl, p, grid, static_cast<cudaStream_t>(stream), false));
   return DLLM_OK;
 }
 
@@ -1385,9 +1463,10 @@ extern "C" dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_ca
   CUtensorMap tk, tv;
   CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H));
   CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H));
-  AttnParams p;
+  AttnParams p = {};
   p.q = q;
   p.o = out;
+  p.o_lo = nullptr;
   p.R = R;
   p.b = b;
   p.H = H;

@@ -11,6 +11,11 @@ static cudaError_t go_attn(const CUtensorMap& tk, const CUtensorMap& tv, const A
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, WQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          AttnCfg<HD>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // every kernel of the step asks for the same L1/shared split, so an SM
+    // never has to drain and reconfigure between them
+    e = cudaFuncSetAttribute(attn_kernel<HD, WQ>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     attr_set = true;
   }
   return launch_ex(attn_kernel<HD, WQ>, grid, dim3(128), AttnCfg<HD>::SMEM_BYTES, st, pdl, tk, tv, p);

@@ -20,6 +20,7 @@ namespace dllm {
 struct AttnParams {
   const uint16_t* q;   // [b*R][H][HD]
   uint16_t* o;         // [b*R][H*HD]
+  uint16_t* o_lo;      // low halves (o - bf16(o)), or null
   int R, b, H, T;      // query rows per sequence, sequences, heads, valid keys
   int z_k0, z_v0;      // plane of (seq 0, head 0) in the K and V maps; plane = z0 + seq*H + head
   int q_tiles, splits, kps;  // query tiles per (seq, head), key splits, keys per split (multiple of 64)
@@ -58,6 +59,16 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store a pair of outputs as bf16 and, when o_lo is set, their bf16 residuals.
+__device__ __forceinline__ void store_pair(uint16_t* o, uint16_t* o_lo, long long idx, float a, float b) {
+  const uint32_t hv = pack_bf16(a, b);
+  *reinterpret_cast<uint32_t*>(&o[idx]) = hv;
+  if (o_lo) {
+    const float ah = __uint_as_float(hv << 16), bh = __uint_as_float(hv & 0xffff0000u);
+    *reinterpret_cast<uint32_t*>(&o_lo[idx]) = pack_bf16(a - ah, b - bh);
+  }
 }
 
 // Byte offset of the 16-byte chunk `ch` (8 bf16 along the head dim) of key row
@@ -294,11 +305,11 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
       for (int i = 0; i < OT; ++i) {
         const int col = i * 8 + 2 * t4;
         if (row_lo < p.R)
-          *reinterpret_cast<uint32_t*>(&p.o[((long long)seq * p.R + row_lo) * p.H * HD + head * HD + col]) =
-              pack_bf16(oacc[i][0] * il, oacc[i][1] * il);
+          store_pair(p.o, p.o_lo, ((long long)seq * p.R + row_lo) * p.H * HD + head * HD + col, oacc[i][0] * il,
+                     oacc[i][1] * il);
         if (row_hi < p.R)
-          *reinterpret_cast<uint32_t*>(&p.o[((long long)seq * p.R + row_hi) * p.H * HD + head * HD + col]) =
-              pack_bf16(oacc[i][2] * ih, oacc[i][3] * ih);
+          store_pair(p.o, p.o_lo, ((long long)seq * p.R + row_hi) * p.H * HD + head * HD + col, oacc[i][2] * ih,
+                     oacc[i][3] * ih);
       }
     }
     return;
@@ -332,24 +343,41 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
   __syncthreads();
   if (!*bcast) return;
   __threadfence();
+  // combine the splits: per row, weights exp2(m_s - M) / L computed once, then
+  // every output element is an independent weighted sum over the splits
   const float* base_o = p.ws_o + work * p.splits * QT * HD;
   const float* base_ml = p.ws_ml + work * p.splits * QT * 2;
-  for (int e = tid; e < QT * HD; e += 128) {
-    const int rl = e / HD, col = e - rl * HD;
-    const int row = qt * QT + rl;
-    if (row >= p.R) continue;
+  float* wn = xo;   // [QT][splits] normalised split weights (the key-group buffer is free now)
+  for (int rl = tid; rl < QT; rl += 128) {
     float M = -INFINITY;
     for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(&base_ml[(s * QT + rl) * 2]));
     const float u = (M == -INFINITY) ? 0.0f : M;
-    float L = 0.0f, O = 0.0f;
+    float L = 0.0f;
     for (int s = 0; s < p.splits; ++s) {
-      const float ms = __ldcg(&base_ml[(s * QT + rl) * 2]);
-      const float ls = __ldcg(&base_ml[(s * QT + rl) * 2 + 1]);
-      const float a = exp2f(ms - u);
-      L += ls * a;
-      O += __ldcg(&base_o[(s * QT + rl) * HD + col]) * a;
+      const float a = exp2f(__ldcg(&base_ml[(s * QT + rl) * 2]) - u);
+      wn[rl * p.splits + s] = a;
+      L += __ldcg(&base_ml[(s * QT + rl) * 2 + 1]) * a;
     }
-    p.o[((long long)seq * p.R + row) * p.H * HD + head * HD + col] = f32_to_bf16_bits(L > 0.0f ? O / L : 0.0f);
+    const float il = L > 0.0f ? 1.0f / L : 0.0f;
+    for (int s = 0; s < p.splits; ++s) wn[rl * p.splits + s] *= il;
+  }
+  __syncthreads();
+  for (int e4 = tid; e4 < QT * HD / 4; e4 += 128) {
+    const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
+    const int row = qt * QT + rl;
+    if (row >= p.R) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < p.splits; ++s) {
+      const float w = wn[rl * p.splits + s];
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(&base_o[(s * QT + rl) * HD + col]));
+      acc.x += v.x * w;
+      acc.y += v.y * w;
+      acc.z += v.z * w;
+      acc.w += v.w * w;
+    }
+    const long long oi = ((long long)seq * p.R + row) * p.H * HD + head * HD + col;
+    store_pair(p.o, p.o_lo, oi, acc.x, acc.y);
+    store_pair(p.o, p.o_lo, oi + 2, acc.z, acc.w);
   }
 }
 

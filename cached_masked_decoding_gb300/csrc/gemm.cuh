@@ -10,6 +10,12 @@
 //           two TMEM accumulators so the epilogue of one tile overlaps the
 //           main loop of the next),
 //   warps 2-5  epilogue (tcgen05.ld, 32 columns at a time).
+// Activation precision: with p.split the activations arrive as two bf16
+// arrays, x = hi + lo (lo = bf16(x - hi), so the pair carries ~16 mantissa
+// bits); both land in one B tile of 2*BN rows and one MMA of width 2*BN
+// yields W.hi and W.lo side by side in TMEM, summed in the epilogue.  The
+// weights are read once either way; while the GEMM is bound by HBM the extra
+// MMA width is free.
 // Work split ("stream-K"): the m_tiles*n_tiles*kc chunks of 64 reduction
 // elements are cut into gridDim.x equal contiguous ranges, so every SM streams
 // the same number of weight bytes.  A tile cut between CTAs is finished by the
@@ -30,6 +36,8 @@ struct GemmParams {
   float* ws;              // fix-up partials [grid][2][BN][128]
   int* counters;          // [m_tiles * n_tiles], zero between launches
   int* err;
+  unsigned long long* trace;  // optional [grid][8] per-CTA timeline (diagnostics), or null
+  int split;              // activations as a hi/lo bf16 pair (BN <= 128)
   // RMSNorm row factor of the activation rows: rsqrt(sum_t ss_in[r][t] * inv_d + eps)
   const float* ss_in;
   int ss_in_tiles;
@@ -45,11 +53,13 @@ struct GemmParams {
   float* h;               // residual [N][d]
   const uint16_t* g_next; // next RMSNorm gain [d]
   uint16_t* xn_out;       // bf16(h * g_next) [rows][d]
+  uint16_t* xn_out_lo;    // bf16(h * g_next - hi), or null
   float* ss_out;          // per-128-column sums of h^2 [rows][d/128]
   int remap;              // 1: output rows are the block rows (final layer)
   int blk_start, blk_len;
   // GEMM_SWIGLU
   uint16_t* act;          // [N][act_ld]
+  uint16_t* act_lo;       // low halves, or null
   int act_ld;
   // GEMM_LMHEAD
   float* st_m;            // [m_tiles][N] tile max logit
@@ -62,11 +72,12 @@ struct GemmParams {
 
 template <int BN>
 struct GemmCfg {
-  static constexpr int STAGES = BN <= 64 ? 8 : (BN == 128 ? 6 : 4);
+  static constexpr int B_ROWS = BN <= 128 ? 2 * BN : BN;   // room for the lo rows when BN <= 128
   static constexpr int A_BYTES = 128 * 64 * 2;
-  static constexpr int B_BYTES = BN * 64 * 2;
+  static constexpr int B_BYTES = B_ROWS * 64 * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int TMEM_COLS = 2 * BN;   // two accumulators; 64..512, a power of two
+  static constexpr int STAGES = STAGE_BYTES <= 24576 ? 8 : (STAGE_BYTES <= 32768 ? 6 : 4);
+  static constexpr int TMEM_COLS = 2 * B_ROWS;   // two accumulators; 128..512, a power of two
   static constexpr int XCH_FLOATS = 128 * 33;
   static constexpr int RED_FLOATS = 4 * 32 * 3;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCH_FLOATS * 4 + 256 * 4 + RED_FLOATS * 4 +
@@ -184,7 +195,10 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
           ro = (bi >= 0 && bi < p.blk_len) ? seq * p.blk_len + bi : -1;
         }
         if (ro >= 0) {
-          p.xn_out[(long long)ro * d + m] = f32_to_bf16_bits(hv * g);
+          const float xv = hv * g;
+          const uint16_t hb = f32_to_bf16_bits(xv);
+          p.xn_out[(long long)ro * d + m] = hb;
+          if (p.xn_out_lo) p.xn_out_lo[(long long)ro * d + m] = f32_to_bf16_bits(xv - bf16_bits_to_f32(hb));
           sq[c] = hv * hv;
         }
       }
@@ -222,7 +236,9 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
         const float gt = v[c];
         const float up = xch[(l128 + 64) * 33 + c];
         const float a = gt / (1.0f + __expf(-gt)) * up;
-        p.act[(long long)r * p.act_ld + f] = f32_to_bf16_bits(a);
+        const uint16_t hb = f32_to_bf16_bits(a);
+        p.act[(long long)r * p.act_ld + f] = hb;
+        if (p.act_lo) p.act_lo[(long long)r * p.act_ld + f] = f32_to_bf16_bits(a - bf16_bits_to_f32(hb));
       }
     }
   } else if constexpr (KIND == GEMM_LMHEAD) {
@@ -277,10 +293,19 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
   }
 }
 
+// v += the low-half accumulator columns (BN + c0 ..) of the same rows.
+template <int BN>
+__device__ __forceinline__ void add_lo(uint32_t taddr, int c0, float (&v)[32]) {
+  float w[32];
+  tmem_ld32(taddr + (uint32_t)(BN + c0), w);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] += w[j];
+}
+
 template <int BN, int KIND>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmBlo, const GemmParams p) {
   using C = GemmCfg<BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -302,7 +327,16 @@ __global__ void __launch_bounds__(192, 1)
   const long long G = gridDim.x, cta = blockIdx.x;
   const long long start = cta * p.total / G;
   const long long end = (cta + 1) * p.total / G;
+  const bool split = BN <= 128 && p.split != 0;
+  const int n_rows = split ? 2 * BN : BN;                      // MMA width
+  const uint32_t stage_tx = (uint32_t)(C::A_BYTES + n_rows * 128);
 
+  if (p.trace && threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    p.trace[cta * 8 + 0] = smid;
+    p.trace[cta * 8 + 1] = globaltimer();
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -316,6 +350,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    if (p.split) prefetch_tensormap(&tmBlo);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -341,7 +376,7 @@ __global__ void __launch_bounds__(192, 1)
         const long long tile = gch / p.kc;
         const int k = (int)(gch - tile * p.kc);
         const int m_idx = (int)(tile / p.n_tiles);
-        mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+        mbar_arrive_expect_tx(&full[i], stage_tx);
         tma_load_2d(sA + i * C::A_BYTES, &tmA, &full[i], k * 64, m_idx * 128, pol_w);
       }
       griddep_wait();
@@ -351,6 +386,7 @@ __global__ void __launch_bounds__(192, 1)
         const int k = (int)(gch - tile * p.kc);
         const int n_idx = (int)(tile % p.n_tiles);
         tma_load_2d(sB + i * C::B_BYTES, &tmB, &full[i], k * 64, n_idx * BN, pol_x);
+        if (split) tma_load_2d(sB + i * C::B_BYTES + BN * 128, &tmBlo, &full[i], k * 64, n_idx * BN, pol_x);
       }
       long long issued = pre;
       for (long long i = pre; i < n; ++i) {
@@ -362,9 +398,10 @@ __global__ void __launch_bounds__(192, 1)
         const int k = (int)(gch - tile * p.kc);
         const int m_idx = (int)(tile / p.n_tiles);
         const int n_idx = (int)(tile % p.n_tiles);
-        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        mbar_arrive_expect_tx(&full[s], stage_tx);
         tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], k * 64, m_idx * 128, pol_w);
         tma_load_2d(sB + s * C::B_BYTES, &tmB, &full[s], k * 64, n_idx * BN, pol_x);
+        if (split) tma_load_2d(sB + s * C::B_BYTES + BN * 128, &tmBlo, &full[s], k * 64, n_idx * BN, pol_x);
         issued = i + 1;
       }
       if (*abort_flag) {
@@ -377,7 +414,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      const uint32_t idesc = idesc_bf16_f32(128, n_rows);
       long long g = start, i = 0;
       int seg = 0;
       bool ok = true;
@@ -389,13 +426,14 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t use = (uint32_t)(seg >> 1);
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, ERR_GEMM_TEMPTY)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        const uint32_t d = tmem + (uint32_t)(buf * C::B_ROWS);
         for (; g < seg_end; ++g, ++i) {
           const int s = (int)(i % STAGES);
           if (!mbar_wait(&full[s], (uint32_t)((i / STAGES) & 1), abort_flag, p.err, ERR_GEMM_FULL)) {
             ok = false;
             break;
           }
+          if (p.trace && i == 0) p.trace[cta * 8 + 2] = globaltimer();
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
           const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
@@ -409,6 +447,7 @@ __global__ void __launch_bounds__(192, 1)
         mma_commit(&tfull[buf]);
         ++seg;
       }
+      if (p.trace) p.trace[cta * 8 + 3] = globaltimer();
     }
   } else {
     // -------------------------------------------------- epilogue (warps 2..5)
@@ -449,12 +488,13 @@ __global__ void __launch_bounds__(192, 1)
       named_bar_sync(1, 128);
       if (*abort_flag) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::B_ROWS);
       if (full_tile) {
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
           tmem_ld32(taddr + (uint32_t)c0, v);
+          if (split) add_lo<BN>(taddr, c0, v);
           if (c0 + 32 == BN) {
             tc_fence_before();
             __syncwarp();
@@ -469,6 +509,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
           tmem_ld32(taddr + (uint32_t)c0, v);
+          if (split) add_lo<BN>(taddr, c0, v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) __stcg(&wsp[(long long)(c0 + j) * 128 + l128], v[j]);
         }
@@ -509,9 +550,11 @@ __global__ void __launch_bounds__(192, 1)
       g = seg_end;
       ++seg;
     }
+    if (p.trace && l128 == 0) p.trace[cta * 8 + 4] = globaltimer();
   }
   tc_fence_before();
   __syncthreads();
+  if (p.trace && threadIdx.x == 0) p.trace[cta * 8 + 5] = globaltimer();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);

@@ -27,25 +27,25 @@ inline cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cu
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-cudaError_t launch_gemm_plain(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+cudaError_t launch_gemm_plain(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p, int grid,
                               cudaStream_t st, bool pdl);
-cudaError_t launch_gemm_qkv(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+cudaError_t launch_gemm_qkv(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p, int grid,
                             cudaStream_t st, bool pdl);
-cudaError_t launch_gemm_resid(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+cudaError_t launch_gemm_resid(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p, int grid,
                               cudaStream_t st, bool pdl);
-cudaError_t launch_gemm_swiglu(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+cudaError_t launch_gemm_swiglu(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p, int grid,
                                cudaStream_t st, bool pdl);
-cudaError_t launch_gemm_lmhead(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+cudaError_t launch_gemm_lmhead(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p, int grid,
                                cudaStream_t st, bool pdl);
 
-inline cudaError_t launch_gemm(int kind, int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+inline cudaError_t launch_gemm(int kind, int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p,
                                int grid, cudaStream_t st, bool pdl) {
   switch (kind) {
-    case GEMM_PLAIN: return launch_gemm_plain(bn, a, b, p, grid, st, pdl);
-    case GEMM_QKV: return launch_gemm_qkv(bn, a, b, p, grid, st, pdl);
-    case GEMM_RESID: return launch_gemm_resid(bn, a, b, p, grid, st, pdl);
-    case GEMM_SWIGLU: return launch_gemm_swiglu(bn, a, b, p, grid, st, pdl);
-    case GEMM_LMHEAD: return launch_gemm_lmhead(bn, a, b, p, grid, st, pdl);
+    case GEMM_PLAIN: return launch_gemm_plain(bn, a, b, blo, p, grid, st, pdl);
+    case GEMM_QKV: return launch_gemm_qkv(bn, a, b, blo, p, grid, st, pdl);
+    case GEMM_RESID: return launch_gemm_resid(bn, a, b, blo, p, grid, st, pdl);
+    case GEMM_SWIGLU: return launch_gemm_swiglu(bn, a, b, blo, p, grid, st, pdl);
+    case GEMM_LMHEAD: return launch_gemm_lmhead(bn, a, b, blo, p, grid, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -59,24 +59,27 @@ cudaError_t launch_attention(int hd, int wq, const CUtensorMap& tk, const CUtens
 #define DLLM_GEMM_LAUNCHER(NAME, KIND)                                                                            \
   namespace dllm {                                                                                              \
   template <int BN>                                                                                             \
-  static cudaError_t go_##NAME(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,       \
+  static cudaError_t go_##NAME(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p, int grid,       \
                                cudaStream_t st, bool pdl) {                                                     \
     static bool attr_set = false;                                                                               \
     if (!attr_set) {                                                                                            \
       cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                            GemmCfg<BN>::SMEM_BYTES);                                            \
       if (e != cudaSuccess) return e;                                                                           \
+      e = cudaFuncSetAttribute(gemm_kernel<BN, KIND>, cudaFuncAttributePreferredSharedMemoryCarveout,          \
+                               cudaSharedmemCarveoutMaxShared);                                                 \
+      if (e != cudaSuccess) return e;                                                                           \
       attr_set = true;                                                                                          \
     }                                                                                                           \
-    return launch_ex(gemm_kernel<BN, KIND>, dim3(grid), dim3(192), GemmCfg<BN>::SMEM_BYTES, st, pdl, a, b, p);  \
+    return launch_ex(gemm_kernel<BN, KIND>, dim3(grid), dim3(192), GemmCfg<BN>::SMEM_BYTES, st, pdl, a, b, blo, p);  \
   }                                                                                                             \
-  cudaError_t launch_gemm_##NAME(int bn, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,       \
+  cudaError_t launch_gemm_##NAME(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p,       \
                                  int grid, cudaStream_t st, bool pdl) {                                         \
     switch (bn) {                                                                                               \
-      case 32: return go_##NAME<32>(a, b, p, grid, st, pdl);                                                    \
-      case 64: return go_##NAME<64>(a, b, p, grid, st, pdl);                                                    \
-      case 128: return go_##NAME<128>(a, b, p, grid, st, pdl);                                                  \
-      case 256: return go_##NAME<256>(a, b, p, grid, st, pdl);                                                  \
+      case 32: return go_##NAME<32>(a, b, blo, p, grid, st, pdl);                                                    \
+      case 64: return go_##NAME<64>(a, b, blo, p, grid, st, pdl);                                                    \
+      case 128: return go_##NAME<128>(a, b, blo, p, grid, st, pdl);                                                  \
+      case 256: return go_##NAME<256>(a, b, blo, p, grid, st, pdl);                                                  \
       default: return cudaErrorInvalidValue;                                                                    \
     }                                                                                                           \
   }                                                                                                             \

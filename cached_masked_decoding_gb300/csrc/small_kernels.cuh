@@ -14,6 +14,7 @@ struct EmbedParams {
   const uint16_t* g;      // first RMSNorm gain [d]
   float* h;
   uint16_t* xn;
+  uint16_t* xn_lo;        // bf16(h * g - xn), or null
   float* ss;
   int d, R, row0, T;
 };
@@ -30,18 +31,21 @@ __global__ void __launch_bounds__(1024) embed_kernel(const EmbedParams p) {
   const uint16_t* ev = reinterpret_cast<const uint16_t*>(&e);
   const uint16_t* gv = reinterpret_cast<const uint16_t*>(&gg);
   float hv[8];
-  uint16_t ov[8];
+  uint16_t ov[8], lv[8];
   float sq = 0.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     hv[i] = bf16_bits_to_f32(ev[i]);
-    ov[i] = f32_to_bf16_bits(hv[i] * bf16_bits_to_f32(gv[i]));
+    const float xv = hv[i] * bf16_bits_to_f32(gv[i]);
+    ov[i] = f32_to_bf16_bits(xv);
+    lv[i] = f32_to_bf16_bits(xv - bf16_bits_to_f32(ov[i]));
     sq += hv[i] * hv[i];
   }
   float4* hp = reinterpret_cast<float4*>(p.h + (long long)r * p.d + c0);
   hp[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
   hp[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
   *reinterpret_cast<uint4*>(p.xn + (long long)r * p.d + c0) = *reinterpret_cast<const uint4*>(ov);
+  if (p.xn_lo) *reinterpret_cast<uint4*>(p.xn_lo + (long long)r * p.d + c0) = *reinterpret_cast<const uint4*>(lv);
   // 16 threads cover one 128-column tile
 #pragma unroll
   for (int s = 8; s >= 1; s >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, s);
@@ -148,7 +152,9 @@ __device__ __forceinline__ void select_commit_cta(const float* conf_s, const int
 }
 
 // LM-head tile statistics -> (conf, arg) per block row, then select/commit.
-// One CTA (256 threads) per sequence.
+// One CTA (256 threads) per block row merges that row's v_tiles statistics
+// (fixed assignment and tree: deterministic); the last CTA of a sequence to
+// finish runs the selection over the sequence's B rows.
 struct MergeParams {
   const float* st_m;
   const float* st_s;
@@ -159,53 +165,72 @@ struct MergeParams {
   float* conf;            // [b][B]
   int32_t* arg;           // [b][B]
   int32_t* count;         // [b]
+  int* seq_done;          // [b] arrival counters, zero between launches
   SelectRule rule;
 };
 
 constexpr int kMaxBlock = 256;
 
+struct MaxSumArg {
+  float m, s;
+  int a;
+};
+
+// (m1, s1, a1) + (m2, s2, a2): the larger maximum wins, sums rescaled to it,
+// equal maxima keep the lower id.  The argument order fixes the rounding.
+__device__ __forceinline__ MaxSumArg msa_merge(MaxSumArg x, MaxSumArg y) {
+  const float M = fmaxf(x.m, y.m);
+  const float sx = (x.m == -INFINITY) ? 0.0f : x.s * exp2f((x.m - M) * kLog2e);
+  const float sy = (y.m == -INFINITY) ? 0.0f : y.s * exp2f((y.m - M) * kLog2e);
+  MaxSumArg r;
+  r.m = M;
+  r.s = sx + sy;
+  r.a = (y.m > x.m || (y.m == x.m && y.a < x.a)) ? y.a : x.a;
+  return r;
+}
+
 __global__ void __launch_bounds__(256) merge_select_kernel(const MergeParams p) {
+  __shared__ MaxSumArg part[8];
   __shared__ float conf_s[kMaxBlock];
   __shared__ int arg_s[kMaxBlock];
   __shared__ int rank_s[kMaxBlock];
   __shared__ float eps_s[kMaxBlock];
   __shared__ int best;
+  __shared__ int last;
   griddep_launch_dependents();
   griddep_wait();
-  const int seq = blockIdx.x;
+  const int row = blockIdx.x;              // seq * B + i
+  const int seq = row / p.B;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = warp; i < p.B; i += 8) {
-    const int row = seq * p.B + i;
-    float M = -INFINITY, S = 0.0f;
-    int A = 0x7fffffff;
-    for (int t = lane; t < p.v_tiles; t += 32) {
-      const long long o = (long long)t * p.n_rows + row;
-      const float mt = p.st_m[o], stt = p.st_s[o];
-      const int at = p.st_a[o];
-      const float Mn = fmaxf(M, mt);
-      S = (M == -INFINITY ? 0.0f : S * exp2f((M - Mn) * kLog2e)) + stt * exp2f((mt - Mn) * kLog2e);
-      A = (mt > M) ? at : A;   // tiles visited in increasing id order: keep the first maximum
-      M = Mn;
-    }
+  MaxSumArg acc{-INFINITY, 0.0f, 0x7fffffff};
+  for (int t = threadIdx.x; t < p.v_tiles; t += 256) {
+    const long long o = (long long)t * p.n_rows + row;
+    acc = msa_merge(acc, MaxSumArg{__ldcg(&p.st_m[o]), __ldcg(&p.st_s[o]), __ldcg(&p.st_a[o])});
+  }
 #pragma unroll
-    for (int s = 1; s < 32; s <<= 1) {
-      const float Mo = __shfl_xor_sync(0xffffffffu, M, s);
-      const float So = __shfl_xor_sync(0xffffffffu, S, s);
-      const int Ao = __shfl_xor_sync(0xffffffffu, A, s);
-      const float Mn = fmaxf(M, Mo);
-      const float Sa = (M == -INFINITY) ? 0.0f : S * exp2f((M - Mn) * kLog2e);
-      const float Sb = (Mo == -INFINITY) ? 0.0f : So * exp2f((Mo - Mn) * kLog2e);
-      // keep the pair order fixed (lower lane first) so every lane sums alike
-      S = (lane & s) ? (Sb + Sa) : (Sa + Sb);
-      A = (Mo > M || (Mo == M && Ao < A)) ? Ao : A;
-      M = Mn;
-    }
-    if (lane == 0) {
-      conf_s[i] = 1.0f / S;
-      arg_s[i] = A;
-      p.conf[(long long)seq * p.B + i] = 1.0f / S;
-      p.arg[(long long)seq * p.B + i] = A;
-    }
+  for (int s = 1; s < 32; s <<= 1) {
+    MaxSumArg o{__shfl_xor_sync(0xffffffffu, acc.m, s), __shfl_xor_sync(0xffffffffu, acc.s, s),
+                __shfl_xor_sync(0xffffffffu, acc.a, s)};
+    acc = (lane & s) ? msa_merge(o, acc) : msa_merge(acc, o);
+  }
+  if (lane == 0) part[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    MaxSumArg r = part[0];
+    for (int w = 1; w < 8; ++w) r = msa_merge(r, part[w]);
+    p.conf[row] = 1.0f / r.s;
+    p.arg[row] = r.a;
+    __threadfence();
+    const int old = atomicAdd(&p.seq_done[seq], 1);
+    last = (old == p.B - 1);
+    if (last) p.seq_done[seq] = 0;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < p.B; i += 256) {
+    conf_s[i] = __ldcg(&p.conf[(long long)seq * p.B + i]);
+    arg_s[i] = __ldcg(&p.arg[(long long)seq * p.B + i]);
   }
   __syncthreads();
   select_commit_cta(conf_s, arg_s, rank_s, eps_s, p.B, p.x + (long long)seq * p.T + p.blk_start, p.mask_id,

@@ -107,6 +107,7 @@ typedef struct dllm_stats {
     int32_t max_steps_per_block;
     int64_t committed;    /* tokens committed over all sequences                 */
     double tau_bar;       /* committed / sum over sequences of active steps      */
+    int64_t kernel_launches; /* kernels this call launched                       */
 } dllm_stats;
 
 typedef struct dllm_model dllm_model;
@@ -202,6 +203,15 @@ dllm_status dllm_read_hidden(const dllm_state* s, float* h);
 /* Copy the cached K and V of one layer as float32, host [b][n_heads][T][head_dim] each. */
 dllm_status dllm_read_kv(const dllm_state* s, int32_t layer, float* k, float* v);
 
+/* Precision of the activations fed to the tensor cores.  DLLM_PREC_SPLIT
+ * (default) carries every GEMM input as a pair of bf16 arrays hi + lo with
+ * lo = bf16(x - hi) (about 16 mantissa bits; the weights are read once, the
+ * MMA is twice as wide).  DLLM_PREC_BF16 rounds activations to bf16 (half the
+ * tensor work: for the compute-bound batch regime).  K/V cache, q and the
+ * attention probabilities are bf16 in both modes; accumulation is float32. */
+typedef enum dllm_precision { DLLM_PREC_SPLIT = 0, DLLM_PREC_BF16 = 1 } dllm_precision;
+dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode);
+
 /* Record the residual stream after the embedding and after every layer on the
  * next steps (1) or stop (0).  dllm_read_trace copies the last step's record,
  * host float32 [n_layers+1][rows][d_model], rows = b * rows_per_seq as
@@ -211,10 +221,13 @@ dllm_status dllm_read_trace(const dllm_state* s, float* out, int64_t capacity_fl
                             int32_t* rows_per_seq, int32_t* first_pos);
 
 /* Accumulate per-kernel-class device time of the next calls with CUDA events
- * (enable 1), or stop (0).  dllm_kernel_times returns, per class (0 embed,
- * 1 qkv_gemm, 2 attention, 3 o_gemm, 4 gateup_gemm, 5 down_gemm, 6 lm_head_gemm,
- * 7 merge_select), the summed milliseconds, launch counts and algorithmic
- * bytes.  The events serialise the kernels: not for the headline time. */
+ * (enable 1), or stop (0).  dllm_kernel_times returns, per class, the summed
+ * milliseconds, launch counts and algorithmic bytes (weights, K/V and
+ * activations each counted once).  Classes of a denoise step: 0 embed,
+ * 1 qkv_gemm, 2 attention, 3 o_gemm, 4 gateup_gemm, 5 down_gemm,
+ * 6 lm_head_gemm, 7 merge_select; a refresh's launches use 8 + the same index.
+ * 16 classes in all.  The events serialise the kernels: not for the headline
+ * time. */
 dllm_status dllm_state_set_kernel_timing(dllm_state* s, int32_t enable);
 dllm_status dllm_kernel_times(const dllm_state* s, double* ms, int64_t* launches,
                               double* bytes, int32_t n_classes);
@@ -223,9 +236,19 @@ dllm_status dllm_kernel_times(const dllm_state* s, double* ms, int64_t* launches
 
 /* Y[N][M] (float32) = X[N][K] * W[M][K]^T on the tensor cores (tcgen05, TMA,
  * stream-K split with a deterministic fix-up).  W, X bf16 row-major, 16-byte
- * aligned, K % 8 == 0.  Uses a library-owned workspace allocated on first use. */
-dllm_status dllm_op_gemm(const uint16_t* W, const uint16_t* X, float* Y, int32_t M, int32_t N,
-                         int32_t K, void* cuda_stream);
+ * aligned, K % 8 == 0.  X_lo (nullable) is a second bf16 array added to X
+ * (the hi/lo activation pair).  Uses a library-owned workspace allocated on
+ * first use. */
+dllm_status dllm_op_gemm(const uint16_t* W, const uint16_t* X, const uint16_t* X_lo, float* Y,
+                         int32_t M, int32_t N, int32_t K, void* cuda_stream);
+
+/* dllm_op_gemm with a per-CTA timeline for diagnostics: trace (device,
+ * uint64 [grid][8], grid <= the SM count, returned in *grid_out) receives per
+ * CTA {SM id, start, first operand tile landed, last MMA issued, epilogue done,
+ * end} in %globaltimer nanoseconds (entries 6-7 unused).  trace may be NULL. */
+dllm_status dllm_op_gemm_trace(const uint16_t* W, const uint16_t* X, const uint16_t* X_lo, float* Y,
+                               int32_t M, int32_t N, int32_t K, uint64_t* trace, int32_t* grid_out,
+                               void* cuda_stream);
 
 /* Non-causal attention, eq. 3: for every sequence s, head h and query row i,
  * out[s*R+i][h*hd..] = softmax(q k^T / sqrt(hd)) v over the T keys of

@@ -55,24 +55,31 @@ GEMM_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["bf16", "split"])
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
-def test_gemm_matches_fp64(torch, M, N, K):
+def test_gemm_matches_fp64(torch, M, N, K, split):
     rng = np.random.default_rng(M * 7 + N * 3 + K)
     Wb = bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
-    Xb = bf16_bits(rng.standard_normal((N, K)).astype(np.float32))
-    W, X = to_dev(torch, Wb), to_dev(torch, Xb)
+    xf = rng.standard_normal((N, K)).astype(np.float32)
+    Xb = bf16_bits(xf)
+    Xl = bf16_bits(xf - bits_to_f64(Xb).astype(np.float32))
+    W, X, XL = to_dev(torch, Wb), to_dev(torch, Xb), to_dev(torch, Xl)
     Y = torch.zeros((N, M), dtype=torch.float32, device="cuda")
-    binding.op_gemm(W.data_ptr(), X.data_ptr(), Y.data_ptr(), M, N, K)
+    binding.op_gemm(W.data_ptr(), X.data_ptr(), Y.data_ptr(), M, N, K, X_lo_ptr=XL.data_ptr() if split else 0)
     torch.cuda.synchronize()
     y = Y.cpu().numpy().astype(np.float64)
     w64, x64 = bits_to_f64(Wb), bits_to_f64(Xb)
+    if split:
+        x64 = x64 + bits_to_f64(Xl)
+        # the pair carries the float32 input to ~2^-16 relative
+        assert np.abs(x64 - xf).max() <= 2.0 ** -15 * np.abs(xf).max()
     ref = x64 @ w64.T
     bound = np.abs(x64) @ np.abs(w64).T          # sum_k |x_k w_k|
     err = np.abs(y - ref)
     assert (err <= 2e-6 * bound + 1e-6).all(), f"max err {err.max():.3e}, worst ratio {(err / (bound + 1e-30)).max():.3e}"
     # deterministic: a second launch gives the same bits
     Y2 = torch.zeros_like(Y)
-    binding.op_gemm(W.data_ptr(), X.data_ptr(), Y2.data_ptr(), M, N, K)
+    binding.op_gemm(W.data_ptr(), X.data_ptr(), Y2.data_ptr(), M, N, K, X_lo_ptr=XL.data_ptr() if split else 0)
     torch.cuda.synchronize()
     assert torch.equal(Y, Y2)
 
