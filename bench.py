@@ -188,6 +188,7 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
                               stream=stream.cuda_stream)
     state = binding.State(model, None, b, P, gen, B, stream=stream.cuda_stream)
     state.set_precision(args.precision)
+    state.set_persistent(args.persistent)
     sel = binding.make_select(binding.SEL_THRESHOLD, wl.tau)
     mode = args.mode
 
@@ -233,7 +234,7 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     kt = state.kernel_times()
     state.set_kernel_timing(False)
     step_classes = ("embed", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lm_head_gemm",
-                    "merge_select")
+                    "merge_select", "persistent_step")
     gemm_classes = ("qkv_gemm", "o_gemm", "gateup_gemm", "down_gemm", "lm_head_gemm")
     dom = max(step_classes, key=lambda k: kt[k]["ms"])
     per_launch_ms = kt[dom]["ms"] / max(kt[dom]["launches"], 1)
@@ -277,6 +278,8 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
             "model": f"{cfg.n_layers}L d{cfg.d_model} H{cfg.n_heads} F{cfg.d_ffn} V{cfg.vocab} (random init)",
             "global_batch": b * world, "seq_len": wl.T, "block": B, "tau": wl.tau, "cache_mode": mode,
             "precision": f"{args.precision} activations, bf16 weights and K/V, f32 accumulate",
+            "step_launch": "persistent (one cooperative launch per denoise step)" if args.persistent
+            else "one launch per kernel",
             "l2": "inputs larger than L2 (every step streams all weights)",
             "parallelism": f"replicas x{world} (no data-path collective)",
         },
@@ -376,6 +379,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (profiling captures of a small case)")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-persistent", dest="persistent", action="store_false",
+                    help="one launch per kernel instead of the persistent DualCache step")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
     import dataclasses

@@ -26,7 +26,7 @@ TENSOR_IDS = {"embed": 1, "attn_norm": 2, "wq": 3, "wk": 4, "wv": 5, "wo": 6, "f
               "wd": 10, "final_norm": 11, "lm_head": 12}
 KERNEL_CLASSES = ("embed", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lm_head_gemm",
                   "merge_select", "refresh_embed", "refresh_qkv_gemm", "refresh_attention", "refresh_o_gemm",
-                  "refresh_gateup_gemm", "refresh_down_gemm", "refresh_unused_6", "refresh_unused_7")
+                  "refresh_gateup_gemm", "refresh_down_gemm", "persistent_step", "unused_15")
 
 
 class DllmError(RuntimeError):
@@ -86,6 +86,9 @@ SIGNATURES = {
     "dllm_kernel_times": (_I32, [_P, _P, _P, _P, _I32]),
     "dllm_op_gemm": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _P]),
     "dllm_state_set_precision": (_I32, [_P, _I32]),
+    "dllm_state_set_persistent": (_I32, [_P, _I32]),
+    "dllm_state_set_step_timeline": (_I32, [_P, _I32]),
+    "dllm_read_step_timeline": (_I32, [_P, _P, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "dllm_op_gemm_trace": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _P, ctypes.POINTER(_I32), _P]),
     "dllm_op_attention": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
     "dllm_op_select_commit": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(Select), _P, _P]),
@@ -259,6 +262,20 @@ class State:
 
     def set_precision(self, mode: str):
         check(lib().dllm_state_set_precision(self.h, {"split": PREC_SPLIT, "bf16": PREC_BF16}[mode]))
+
+    def set_persistent(self, on: bool):
+        check(lib().dllm_state_set_persistent(self.h, 1 if on else 0))
+
+    def set_step_timeline(self, on: bool):
+        check(lib().dllm_state_set_step_timeline(self.h, 1 if on else 0))
+
+    def step_timeline(self) -> np.ndarray:
+        c = ctypes.c_int32()
+        ph = ctypes.c_int32()
+        check(lib().dllm_read_step_timeline(self.h, None, 0, ctypes.byref(c), ctypes.byref(ph)))
+        out = np.zeros((c.value, ph.value, 6), dtype=np.uint64)
+        check(lib().dllm_read_step_timeline(self.h, _ptr(out), out.size, ctypes.byref(c), ctypes.byref(ph)))
+        return out
 
     def set_trace(self, on: bool):
         check(lib().dllm_state_set_trace(self.h, 1 if on else 0))

@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-cudart", "shared"]
-LIB_UNITS = ["api", "attention", "gemm_plain", "gemm_qkv", "gemm_resid", "gemm_swiglu", "gemm_lmhead"]
+LIB_UNITS = ["api", "attention", "gemm_plain", "gemm_qkv", "gemm_resid", "gemm_swiglu", "gemm_lmhead",
+             "step_hd64", "step_hd128"]
 
 
 def _nvcc() -> str:

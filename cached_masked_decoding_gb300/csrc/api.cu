@@ -182,6 +182,20 @@ AttnPlan plan_attention(int b, int H, int R, int T, int sms) {
   return a;
 }
 
+// Attention plan of the persistent step: at most one work item per CTA.
+AttnPlan plan_attention_persistent(int b, int H, int R, int T, int ctas) {
+  AttnPlan a;
+  a.wq = 2;
+  a.q_tiles = ceil_div(R, 32);
+  const long long base = (long long)b * H * a.q_tiles;
+  const int max_splits = std::max(1, ceil_div(T, 64));
+  int splits = (int)std::max<long long>(1, std::min<long long>(max_splits, ctas / std::max<long long>(base, 1)));
+  splits = std::min(splits, 32);
+  a.kps = round_up(ceil_div(T, splits), 64);
+  a.splits = ceil_div(T, a.kps);
+  return a;
+}
+
 }  // namespace
 
 // ====================================================================== model
@@ -446,7 +460,7 @@ extern "C" dllm_status dllm_load(const char* path, dllm_model** out) {
 
 // ====================================================================== state
 // kernel classes of a denoise step; a refresh's launches use class + KC_REFRESH
-enum KClass { KC_EMBED = 0, KC_QKV, KC_ATTN, KC_O, KC_GU, KC_D, KC_LM, KC_MERGE, KC_REFRESH = 8, KC_N = 16 };
+enum KClass { KC_EMBED = 0, KC_QKV, KC_ATTN, KC_O, KC_GU, KC_D, KC_LM, KC_MERGE, KC_REFRESH = 8, KC_PSTEP = 14, KC_N = 16 };
 
 struct dllm_state {
   dllm_model* m = nullptr;
@@ -501,6 +515,20 @@ struct dllm_state {
   double kt_bytes[KC_N] = {0};
   cudaEvent_t ev_a = nullptr, ev_b = nullptr;
   long long launches = 0;         // kernels launched by this state
+  // persistent DualCache step (one cooperative launch per step)
+  bool persistent = true;
+  bool step_built = false;
+  bool step_split = true;
+  int step_bn = 0;
+  int n_phases = 0;
+  int map_kv = 0;
+  StepPhase* d_phases = nullptr;  // [n_blocks][n_phases]
+  CUtensorMap* d_maps = nullptr;
+  unsigned int* d_bar = nullptr;
+  AttnPlan step_attn = {};
+  int step_prefetch = 1 << 20;                // weight tiles loaded ahead of a phase barrier (ring depth cap)
+  unsigned long long* d_timeline = nullptr;   // persistent-step phase timeline (diagnostics)
+  bool timeline = false;
 };
 
 namespace {
@@ -509,6 +537,10 @@ dllm_status state_free_device(dllm_state* s) {
   if (s->arena) cudaFree(s->arena);
   if (s->gemm_ws) cudaFree(s->gemm_ws);
   if (s->trace_buf) cudaFree(s->trace_buf);
+  if (s->d_phases) cudaFree(s->d_phases);
+  if (s->d_maps) cudaFree(s->d_maps);
+  if (s->d_bar) cudaFree(s->d_bar);
+  if (s->d_timeline) cudaFree(s->d_timeline);
   if (s->host_ce) cudaFreeHost(s->host_ce);
   for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
   if (s->ev_a) cudaEventDestroy(s->ev_a);
@@ -589,6 +621,10 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
       attn_floats = std::max(attn_floats, works * a.splits * 16 * a.wq * (hd + 2));
       attn_cnt = std::max(attn_cnt, works);
     }
+    AttnPlan ap = plan_attention_persistent(b, (int)H, block, (int)T, m->sms);
+    const size_t pworks = (size_t)b * H * ap.q_tiles;
+    attn_floats = std::max(attn_floats, pworks * ap.splits * 16 * ap.wq * (hd + 2));
+    attn_cnt = std::max(attn_cnt, pworks);
   }
   auto al = [](size_t bytes) { return (bytes + 1023) / 1024 * 1024; };
   size_t total = 0;
@@ -819,6 +855,21 @@ dllm_status pin_carveouts() {
   return DLLM_OK;
 }
 
+// Shape, work split and workspace fields of a GEMM's parameters.
+void gemm_shape(dllm_state* s, GemmParams& p, int M, int K, int N, int BN) {
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = ceil_div(M, 128);
+  p.n_tiles = ceil_div(N, BN);
+  p.kc = ceil_div(K, 64);
+  p.total = (long long)p.m_tiles * p.n_tiles * p.kc;
+  p.ws = s->gemm_ws;
+  p.counters = s->gemm_cnt;
+  p.err = s->count_err + s->b;
+  p.split = s->split ? 1 : 0;
+}
+
 dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int K, const uint16_t* X,
                      const uint16_t* X_lo, int N, GemmParams p, int cls, double bytes) {
   const int BN = pick_bn(N, s->split);
@@ -830,17 +881,7 @@ dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int
     tmBlo = act_map(s, X_lo, K, N, BN, &st);
     if (!tmBlo) return st;
   }
-  p.split = s->split ? 1 : 0;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.m_tiles = ceil_div(M, 128);
-  p.n_tiles = ceil_div(N, BN);
-  p.kc = ceil_div(K, 64);
-  p.total = (long long)p.m_tiles * p.n_tiles * p.kc;
-  p.ws = s->gemm_ws;
-  p.counters = s->gemm_cnt;
-  p.err = s->count_err + s->b;
+  gemm_shape(s, p, M, K, N, BN);
   const int grid = (int)std::min<long long>(s->m->sms, p.total);
   if (s->timing) s->kt_bytes[cls] += bytes;
   Timed t(s, cls, bytes);
@@ -1008,6 +1049,251 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
   return DLLM_OK;
 }
 
+// Tensor-map table and per-block phase lists of the persistent DualCache step.
+dllm_status build_step(dllm_state* s) {
+  const dllm_model* m = s->m;
+  const dllm_config& c = m->cfg;
+  const int d = c.d_model, L = c.n_layers, F = m->F_pad, V = c.vocab;
+  const int n = s->b * s->B;
+  const int BN = pick_bn(n, true);
+  std::vector<CUtensorMap> maps;
+  auto add = [&](const CUtensorMap& t) {
+    maps.push_back(t);
+    return (int)maps.size() - 1;
+  };
+  std::vector<int> i_qkv(L), i_o(L), i_gu(L), i_d(L);
+  for (int l = 0; l < L; ++l) {
+    i_qkv[l] = add(m->layers[l].tm_qkv);
+    i_o[l] = add(m->layers[l].tm_o);
+    i_gu[l] = add(m->layers[l].tm_gu);
+    i_d[l] = add(m->layers[l].tm_d);
+  }
+  const int i_lm = add(m->tm_lm);
+  s->map_kv = add(s->tm_kv);
+  CUtensorMap t;
+  auto act = [&](const uint16_t* base, int K, int* idx) -> dllm_status {
+    CKS(map_2d(&t, base, K, n, BN));
+    *idx = add(t);
+    return DLLM_OK;
+  };
+  int i_xn, i_xnl, i_ao, i_aol, i_act, i_actl, i_xf, i_xfl;
+  CKS(act(s->xn, d, &i_xn));
+  CKS(act(s->xn_lo, d, &i_xnl));
+  CKS(act(s->ao, d, &i_ao));
+  CKS(act(s->ao_lo, d, &i_aol));
+  CKS(act(s->act, F, &i_act));
+  CKS(act(s->act_lo, F, &i_actl));
+  CKS(act(s->xf, d, &i_xf));
+  CKS(act(s->xf_lo, d, &i_xfl));
+
+  const int n_phases = 5 * L + 3;
+  std::vector<StepPhase> ph((size_t)s->n_blocks * n_phases);
+  for (int j = 0; j < s->n_blocks; ++j) {
+    const int blk = s->P + j * s->B;
+    StepPhase* P = &ph[(size_t)j * n_phases];
+    int k = 0;
+    P[k] = StepPhase{};
+    P[k++].kind = PH_EMBED;
+    for (int l = 0; l < L; ++l) {
+      const LayerW& w = m->layers[l];
+      const bool last = l == L - 1;
+      StepPhase q = {};
+      q.kind = PH_GEMM;
+      q.gemm_kind = GEMM_QKV;
+      q.map_a = i_qkv[l];
+      q.map_b = i_xn;
+      q.map_blo = i_xnl;
+      gemm_shape(s, q.g, 3 * d, d, n, BN);
+      q.g.ss_in = s->ss;
+      q.g.ss_in_tiles = d / 128;
+      q.g.inv_d = 1.0f / d;
+      q.g.eps = c.norm_eps;
+      q.g.R = s->B;
+      q.g.row0 = blk;
+      q.g.q_out = s->q;
+      q.g.kv = s->kv;
+      q.g.rope_cs = s->rope;
+      q.g.d_model = d;
+      q.g.head_dim = c.head_dim;
+      q.g.n_heads = c.n_heads;
+      q.g.T_pad = s->T;
+      q.g.b_seqs = s->b;
+      q.g.layer = l;
+      P[k++] = q;
+      StepPhase at = {};
+      at.kind = PH_ATTN;
+      at.layer = l;
+      P[k++] = at;
+      StepPhase o = {};
+      o.kind = PH_GEMM;
+      o.gemm_kind = GEMM_RESID;
+      o.map_a = i_o[l];
+      o.map_b = i_ao;
+      o.map_blo = i_aol;
+      gemm_shape(s, o.g, d, d, n, BN);
+      o.g.R = s->B;
+      o.g.row0 = blk;
+      o.g.d_model = d;
+      o.g.h = s->h;
+      o.g.g_next = w.ffn_norm;
+      o.g.xn_out = s->xn;
+      o.g.xn_out_lo = s->split ? s->xn_lo : nullptr;
+      o.g.ss_out = s->ss;
+      P[k++] = o;
+      StepPhase gu = {};
+      gu.kind = PH_GEMM;
+      gu.gemm_kind = GEMM_SWIGLU;
+      gu.map_a = i_gu[l];
+      gu.map_b = i_xn;
+      gu.map_blo = i_xnl;
+      gemm_shape(s, gu.g, 2 * F, d, n, BN);
+      gu.g.ss_in = s->ss;
+      gu.g.ss_in_tiles = d / 128;
+      gu.g.inv_d = 1.0f / d;
+      gu.g.eps = c.norm_eps;
+      gu.g.act = s->act;
+      gu.g.act_lo = s->split ? s->act_lo : nullptr;
+      gu.g.act_ld = F;
+      P[k++] = gu;
+      StepPhase dn = {};
+      dn.kind = PH_GEMM;
+      dn.gemm_kind = GEMM_RESID;
+      dn.map_a = i_d[l];
+      dn.map_b = i_act;
+      dn.map_blo = i_actl;
+      gemm_shape(s, dn.g, d, F, n, BN);
+      dn.g.R = s->B;
+      dn.g.row0 = blk;
+      dn.g.d_model = d;
+      dn.g.h = s->h;
+      if (last) {
+        dn.g.g_next = m->final_norm;
+        dn.g.xn_out = s->xf;
+        dn.g.xn_out_lo = s->split ? s->xf_lo : nullptr;
+        dn.g.ss_out = s->ssf;
+        dn.g.remap = 1;
+        dn.g.blk_start = blk;
+        dn.g.blk_len = s->B;
+      } else {
+        dn.g.g_next = m->layers[l + 1].attn_norm;
+        dn.g.xn_out = s->xn;
+        dn.g.xn_out_lo = s->split ? s->xn_lo : nullptr;
+        dn.g.ss_out = s->ss;
+      }
+      P[k++] = dn;
+    }
+    StepPhase lm = {};
+    lm.kind = PH_GEMM;
+    lm.gemm_kind = GEMM_LMHEAD;
+    lm.map_a = i_lm;
+    lm.map_b = i_xf;
+    lm.map_blo = i_xfl;
+    gemm_shape(s, lm.g, V, d, n, BN);
+    lm.g.ss_in = s->ssf;
+    lm.g.ss_in_tiles = d / 128;
+    lm.g.inv_d = 1.0f / d;
+    lm.g.eps = c.norm_eps;
+    lm.g.st_m = s->st_m;
+    lm.g.st_s = s->st_s;
+    lm.g.st_a = s->st_a;
+    P[k++] = lm;
+    P[k] = StepPhase{};
+    P[k++].kind = PH_MERGE;
+  }
+  if (s->d_phases) cudaFree(s->d_phases);
+  if (s->d_maps) cudaFree(s->d_maps);
+  s->d_phases = nullptr;
+  s->d_maps = nullptr;
+  CKS(dev_alloc((void**)&s->d_phases, ph.size() * sizeof(StepPhase)));
+  CKS(dev_alloc((void**)&s->d_maps, maps.size() * sizeof(CUtensorMap)));
+  if (!s->d_bar) CKS(dev_alloc((void**)&s->d_bar, 256));
+  CK(cudaMemcpy(s->d_phases, ph.data(), ph.size() * sizeof(StepPhase), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(s->d_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
+  s->n_phases = n_phases;
+  s->step_bn = BN;
+  s->step_split = s->split;
+  s->step_attn = plan_attention_persistent(s->b, c.n_heads, s->B, s->T, s->m->sms);
+  s->step_built = true;
+  return DLLM_OK;
+}
+
+bool use_persistent(const dllm_state* s, int mode) {
+  return s->persistent && mode == DLLM_CACHE_DUAL && !s->trace && s->b * s->B <= 128 && s->B <= 32;
+}
+
+// One DualCache denoise step of block j as a single cooperative launch.
+dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
+  if (!s->step_built || s->step_split != s->split) CKS(build_step(s));
+  const dllm_model* m = s->m;
+  const dllm_config& c = m->cfg;
+  const int d = c.d_model, V = c.vocab;
+  const int blk = s->P + j * s->B;
+  const int n = s->b * s->B;
+  s->last_row0 = blk;
+  s->last_R = s->B;
+  s->last_blk = blk;
+  StepArgs a = {};
+  a.phases = s->d_phases + (size_t)j * s->n_phases;
+  a.n_phases = s->n_phases;
+  a.maps = s->d_maps;
+  a.bar = s->d_bar;
+  a.err = s->count_err + s->b;
+  a.emb = EmbedParams{s->x, m->embed, m->layers[0].attn_norm, s->h, s->xn, s->split ? s->xn_lo : nullptr, s->ss,
+                      d, s->B, blk, s->T};
+  const AttnPlan& ap = s->step_attn;
+  const int QT = 32;
+  const long long works = (long long)s->b * c.n_heads * ap.q_tiles;
+  a.attn.q = s->q;
+  a.attn.o = s->ao;
+  a.attn.o_lo = s->split ? s->ao_lo : nullptr;
+  a.attn.R = s->B;
+  a.attn.b = s->b;
+  a.attn.H = c.n_heads;
+  a.attn.T = s->T;
+  a.attn.q_tiles = ap.q_tiles;
+  a.attn.splits = ap.splits;
+  a.attn.kps = ap.kps;
+  a.attn.scale_log2 = kLog2e / std::sqrt((float)c.head_dim);
+  a.attn.ws_o = s->attn_o;
+  a.attn.ws_ml = s->attn_o + works * ap.splits * QT * c.head_dim;
+  a.attn.counters = s->attn_cnt;
+  a.attn.err = s->count_err + s->b;
+  a.attn_map = s->map_kv;
+  a.attn_items = (int)(works * ap.splits);
+  a.merge.st_m = s->st_m;
+  a.merge.st_s = s->st_s;
+  a.merge.st_a = s->st_a;
+  a.merge.v_tiles = ceil_div(V, 128);
+  a.merge.n_rows = n;
+  a.merge.B = s->B;
+  a.merge.T = s->T;
+  a.merge.blk_start = blk;
+  a.merge.mask_id = V;
+  a.merge.x = s->x;
+  a.merge.conf = s->conf;
+  a.merge.arg = s->arg;
+  a.merge.count = s->count_err;
+  a.merge.seq_done = s->seq_done;
+  a.merge.rule = rule;
+  a.prefetch = s->step_prefetch;
+  if (s->timeline) {
+    if (!s->d_timeline) CKS(dev_alloc((void**)&s->d_timeline, (size_t)s->m->sms * s->n_phases * 6 * 8));
+    a.timeline = s->d_timeline;
+  }
+  CK(cudaMemsetAsync(s->d_bar, 0, 4, s->st));
+  const double bytes = (double)s->m->cfg.n_layers * 2.0 *
+                           (4.0 * d * d + 3.0 * (double)d * c.d_ffn) +
+                       2.0 * V * d + (double)s->b * s->T * d * 2 * 2 * c.n_layers;
+  if (s->timing) s->kt_bytes[KC_PSTEP] += bytes;
+  Timed t(s, KC_PSTEP, bytes);
+  const int grid = s->m->sms;
+  cudaError_t e = c.head_dim == 64 ? launch_step_hd64(s->step_bn, a, grid, s->st)
+                                   : launch_step_hd128(s->step_bn, a, grid, s->st);
+  CK(e);
+  ++s->launches;
+  return DLLM_OK;
+}
+
 dllm_status finish_sync(dllm_state* s) {
   CK(cudaMemcpyAsync(s->host_ce, s->count_err, (s->b + 1) * 4, cudaMemcpyDeviceToHost, s->st));
   CK(cudaStreamSynchronize(s->st));
@@ -1070,7 +1356,11 @@ dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int3
   }
   if (e0) CK(cudaEventRecord(e0, s->st));
   CK(cudaMemsetAsync(s->count_err, 0, (s->b + 1) * 4, s->st));
-  CKS(run_forward(s, row0, R, false, blk, rule));
+  if (use_persistent(s, mode)) {
+    CKS(run_step_persistent(s, j, rule));
+  } else {
+    CKS(run_forward(s, row0, R, false, blk, rule));
+  }
   if (e1) CK(cudaEventRecord(e1, s->st));
   CKS(finish_sync(s));
   int sum = 0;
@@ -1278,6 +1568,43 @@ extern "C" dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode) {
     return DLLM_EINVAL;
   }
   s->split = mode == DLLM_PREC_SPLIT;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  s->persistent = enable != 0;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_step_timeline(dllm_state* s, int32_t enable) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  s->timeline = enable != 0;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_read_step_timeline(const dllm_state* s, uint64_t* out, int64_t capacity, int32_t* ctas,
+                                               int32_t* phases) {
+  if (!s || !s->d_timeline) {
+    set_error("no persistent-step timeline was recorded");
+    return DLLM_ESTATE;
+  }
+  const size_t n = (size_t)s->m->sms * s->n_phases * 6;
+  if (ctas) *ctas = s->m->sms;
+  if (phases) *phases = s->n_phases;
+  if (!out) return DLLM_OK;
+  if ((size_t)capacity < n) {
+    set_error("timeline needs %zu values", n);
+    return DLLM_EINVAL;
+  }
+  CK(cudaStreamSynchronize(s->st));
+  CK(cudaMemcpy(out, s->d_timeline, n * 8, cudaMemcpyDeviceToHost));
   return DLLM_OK;
 }
 

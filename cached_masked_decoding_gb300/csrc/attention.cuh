@@ -77,62 +77,47 @@ __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
   return (uint32_t)((ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
-// WQ warps along queries (16 rows each), 4/WQ warp groups along each key tile.
-template <int HD, int WQ>
-__global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using C = AttnCfg<HD>;
+// One work item (key split, query tile, head, sequence) of block attention,
+// run by a group of 128 threads (tid 0..127, named barrier 2).  sK/sV hold ST
+// stages of [64 keys][HD] tiles (1024-byte aligned), xo at least 32*HD floats,
+// full[ST] mbarriers initialised to count 1.  tcount counts the tiles this
+// group has loaded through `full` so far (phase parity across items); it is
+// advanced by the item's tile count.
+template <int HD, int WQ, int ST>
+__device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
+                                          int split, int qt, int head, int seq, uint8_t* sK, uint8_t* sV, float* xo,
+                                          uint64_t* full, int* bcast, uint32_t& tcount, int tid) {
+  constexpr int KT = 64;
+  constexpr int TILE_BYTES = KT * HD * 2;
   constexpr int WK = 4 / WQ;
   constexpr int QT = 16 * WQ;
-  constexpr int KW = C::KT / WK;   // keys per warp per tile
+  constexpr int KW = KT / WK;      // keys per warp per tile
   constexpr int NT = KW / 8;       // n8 tiles of S per warp
   constexpr int KS = HD / 16;      // k16 steps of Q K^T
   constexpr int OT = HD / 8;       // n8 tiles of O
   static_assert(QT <= 64, "query tile");
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = smem;
-  uint8_t* sV = smem + C::STAGES * C::TILE_BYTES;
-  float* xo = reinterpret_cast<float*>(sV + C::STAGES * C::TILE_BYTES);   // [32][HD] group-1 O (WK == 2)
-  float* xml = xo + 32 * HD;                                               // [32][2]
-  uint64_t* full = reinterpret_cast<uint64_t*>(xml + 64);
-  int* bcast = reinterpret_cast<int*>(full + C::STAGES);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* xml = xo + 32 * HD;       // [32][2]
+  const int warp = tid >> 5, lane = tid & 31;
   const int wq = warp % WQ, wk = warp / WQ;
   const int g = lane >> 2, t4 = lane & 3;
-  const int split = blockIdx.x;
-  const int qt = blockIdx.y % p.q_tiles;
-  const int head = blockIdx.y / p.q_tiles;
-  const int seq = blockIdx.z;
   const int k_beg = split * p.kps;
   const int k_end = min(p.T, k_beg + p.kps);
-  const int ntiles = (k_end - k_beg + C::KT - 1) / C::KT;
+  const int ntiles = (k_end - k_beg + KT - 1) / KT;
   const int zk = p.z_k0 + seq * p.H + head, zv = p.z_v0 + seq * p.H + head;
-
-  if (tid == 0) {
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(&full[s], 1);
-    fence_mbar_init();
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-  }
-  __syncthreads();
-  griddep_launch_dependents();
-  griddep_wait();
 
   const uint64_t pol = policy_evict_first();
   auto issue = [&](int t, int s) {
-    const int key0 = k_beg + t * C::KT;
-    mbar_arrive_expect_tx(&full[s], 2 * C::TILE_BYTES);
+    const int key0 = k_beg + t * KT;
+    mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES);
 #pragma unroll
     for (int bx = 0; bx < HD / 64; ++bx) {
-      tma_load_3d(sK + s * C::TILE_BYTES + bx * 8192, &tmK, &full[s], bx * 64, key0, zk, pol);
-      tma_load_3d(sV + s * C::TILE_BYTES + bx * 8192, &tmV, &full[s], bx * 64, key0, zv, pol);
+      tma_load_3d(sK + s * TILE_BYTES + bx * 8192, tmK, &full[s], bx * 64, key0, zk, pol);
+      tma_load_3d(sV + s * TILE_BYTES + bx * 8192, tmV, &full[s], bx * 64, key0, zv, pol);
     }
   };
+  const uint32_t tc0 = tcount;
   if (tid == 0)
-    for (int t = 0; t < C::STAGES && t < ntiles; ++t) issue(t, t);
+    for (int t = 0; t < ST && t < ntiles; ++t) issue(t, (int)((tc0 + t) % ST));
 
   // Q fragments of this warp's 16 query rows
   const int qrow0 = qt * QT + wq * 16;
@@ -145,10 +130,11 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
       const int c0 = kk * 16 + 2 * t4;
-      qa[kk][0] = lo_ok ? q32[(base_lo + c0) >> 1] : 0u;
-      qa[kk][1] = hi_ok ? q32[(base_hi + c0) >> 1] : 0u;
-      qa[kk][2] = lo_ok ? q32[(base_lo + c0 + 8) >> 1] : 0u;
-      qa[kk][3] = hi_ok ? q32[(base_hi + c0 + 8) >> 1] : 0u;
+      // L2-coherent loads: q was written by other CTAs of the same launch (persistent step)
+      qa[kk][0] = lo_ok ? __ldcg(&q32[(base_lo + c0) >> 1]) : 0u;
+      qa[kk][1] = hi_ok ? __ldcg(&q32[(base_hi + c0) >> 1]) : 0u;
+      qa[kk][2] = lo_ok ? __ldcg(&q32[(base_lo + c0 + 8) >> 1]) : 0u;
+      qa[kk][3] = hi_ok ? __ldcg(&q32[(base_hi + c0 + 8) >> 1]) : 0u;
     }
   }
 
@@ -159,12 +145,13 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
   bool failed = false;
 
   for (int t = 0; t < ntiles; ++t) {
-    const int s = t % C::STAGES;
-    if (!failed && !mbar_wait(&full[s], (uint32_t)((t / C::STAGES) & 1), nullptr, p.err, ERR_ATTN_FULL))
+    const uint32_t tg = tc0 + t;
+    const int s = (int)(tg % ST);
+    if (!failed && !mbar_wait(&full[s], (tg / ST) & 1u, nullptr, p.err, ERR_ATTN_FULL))
       failed = true;
     if (!failed) {
-      const uint32_t kb = smem_u32(sK + s * C::TILE_BYTES);
-      const uint32_t vb = smem_u32(sV + s * C::TILE_BYTES);
+      const uint32_t kb = smem_u32(sK + s * TILE_BYTES);
+      const uint32_t vb = smem_u32(sV + s * TILE_BYTES);
       const int key_w = wk * KW;       // first key of this warp inside the tile
       // S = Q K^T
       float sacc[NT][4];
@@ -182,7 +169,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
         }
       }
       // online softmax (base 2)
-      const int key_base = k_beg + t * C::KT + key_w;
+      const int key_base = k_beg + t * KT + key_w;
       float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -249,9 +236,10 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
         }
       }
     }
-    __syncthreads();
-    if (tid == 0 && !failed && t + C::STAGES < ntiles) issue(t + C::STAGES, s);
+    named_bar_sync(2, 128);
+    if (tid == 0 && !failed && t + ST < ntiles) issue(t + ST, s);
   }
+  tcount = tc0 + ntiles;
 
   // combine the key groups of a CTA (WK == 2): group 1 hands its state to group 0
   if constexpr (WK == 2) {
@@ -272,7 +260,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
         xml[(rl + 8) * 2 + 1] = l_hi;
       }
     }
-    __syncthreads();
+    named_bar_sync(2, 128);
     if (wk == 0) {
       const int rl = wq * 16 + g;
       const float m1_lo = xml[rl * 2], l1_lo = xml[rl * 2 + 1];
@@ -332,17 +320,17 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
       __stcg(reinterpret_cast<float2*>(&wml[(rl + 8) * 2]), make_float2(m_hi, l_hi));
     }
   }
-  __threadfence();
-  __syncthreads();
+  // the barrier orders every thread's partial stores before thread 0's
+  // release; its acquire plus the next barrier order the reads after
+  named_bar_sync(2, 128);
   if (tid == 0) {
-    const int old = atomicAdd(&p.counters[work], 1);
+    const int old = atomic_add_acq_rel_gpu(&p.counters[work], 1);
     const int last = (old == p.splits - 1);
     if (last) p.counters[work] = 0;
     *bcast = last;
   }
-  __syncthreads();
+  named_bar_sync(2, 128);
   if (!*bcast) return;
-  __threadfence();
   // combine the splits: per row, weights exp2(m_s - M) / L computed once, then
   // every output element is an independent weighted sum over the splits
   const float* base_o = p.ws_o + work * p.splits * QT * HD;
@@ -361,7 +349,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
     const float il = L > 0.0f ? 1.0f / L : 0.0f;
     for (int s = 0; s < p.splits; ++s) wn[rl * p.splits + s] *= il;
   }
-  __syncthreads();
+  named_bar_sync(2, 128);
   for (int e4 = tid; e4 < QT * HD / 4; e4 += 128) {
     const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
     const int row = qt * QT + rl;
@@ -379,6 +367,32 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
     store_pair(p.o, p.o_lo, oi, acc.x, acc.y);
     store_pair(p.o, p.o_lo, oi + 2, acc.z, acc.w);
   }
+}
+
+// Standalone launch: one work item per CTA.
+template <int HD, int WQ>
+__global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using C = AttnCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::STAGES * C::TILE_BYTES;
+  float* xo = reinterpret_cast<float*>(sV + C::STAGES * C::TILE_BYTES);   // [32][HD] + [32][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(xo + 32 * HD + 64);
+  int* bcast = reinterpret_cast<int*>(full + C::STAGES);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  __syncthreads();
+  griddep_launch_dependents();
+  griddep_wait();
+  uint32_t tcount = 0;
+  attn_item<HD, WQ, C::STAGES>(&tmK, &tmV, p, blockIdx.x, blockIdx.y % p.q_tiles, blockIdx.y / p.q_tiles,
+                               blockIdx.z, sK, sV, xo, full, bcast, tcount, threadIdx.x);
 }
 
 }  // namespace dllm

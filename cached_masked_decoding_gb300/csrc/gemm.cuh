@@ -126,80 +126,115 @@ __device__ __forceinline__ void warp_transpose_argmax(float (&v)[32], int (&id)[
 // Epilogue of 32 consecutive activation rows (columns of the accumulator) for
 // the thread's weight row m = m_idx*128 + l128.  v holds raw sums.  Every
 // epilogue thread of the CTA calls this with the same (m_idx, r0).
+// Each epilogue reads everything it needs first (parameters into registers,
+// global loads as one batch, L2-coherent: other CTAs may have written the data
+// earlier in the same launch), computes, then stores: a store between loads
+// would force every later load to wait for it.
 template <int KIND>
 __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], int m_idx, int r0, int l128,
                                           int lane, int q, float* xch, const float* rs, float* red) {
   const int m = m_idx * 128 + l128;
+  const int N = p.N;
   if constexpr (KIND == GEMM_PLAIN) {
-    if (m < p.M) {
+    float* __restrict__ y = p.y;
+    const int ldy = p.ldy, M = p.M;
+    const bool scale = p.ss_in != nullptr;
+    if (m < M) {
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const int r = r0 + c;
-        if (r < p.N) p.y[(long long)r * p.ldy + m] = p.ss_in ? v[c] * rs[c] : v[c];
+        if (r < N) y[(long long)r * ldy + m] = scale ? v[c] * rs[c] : v[c];
       }
     }
   } else if constexpr (KIND == GEMM_QKV) {
     const int d = p.d_model, hd = p.head_dim, half = hd >> 1;
+    const int R = p.R, row0 = p.row0, T = p.T_pad, H = p.n_heads, layer = p.layer, b = p.b_seqs;
+    const float2* __restrict__ rope = p.rope_cs;
+    uint16_t* __restrict__ q_out = p.q_out;
+    uint16_t* __restrict__ kv = p.kv;
     const int sec = (m_idx * 128) / d;          // uniform over the tile: 0 q, 1 k, 2 v
     const int mr = m - sec * d;
     const int head = mr / hd, j = mr - head * hd;
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] *= rs[c];
+    const int seq0 = r0 / R, i0 = r0 - seq0 * R;   // rows r0.. walk (seq, i) without dividing
     if (sec < 2) {
+      const int jj = j & (half - 1);
+      float2 cs[32];
+      int i = i0;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        cs[c] = __ldg(&rope[(long long)(row0 + i) * half + jj]);
+        if (++i == R) i = 0;
+      }
       named_bar_sync(1, 128);
 #pragma unroll
       for (int c = 0; c < 32; ++c) xch[l128 * 33 + c] = v[c];
       named_bar_sync(1, 128);
       const int partner = l128 ^ half;
-      const int jj = j & (half - 1);
       const float sgn = (j < half) ? -1.0f : 1.0f;
+      float pv[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int r = r0 + c;
-        const int rr = r < p.N ? r : 0;
-        const int pos = p.row0 + rr % p.R;
-        const float2 cs = p.rope_cs[(long long)pos * half + jj];
-        v[c] = v[c] * cs.x + sgn * xch[partner * 33 + c] * cs.y;
-      }
+      for (int c = 0; c < 32; ++c) pv[c] = xch[partner * 33 + c];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) v[c] = v[c] * cs[c].x + sgn * pv[c] * cs[c].y;
     }
+    int seq = seq0, i = i0;
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       const int r = r0 + c;
-      if (r >= p.N) continue;
-      const uint16_t bits = f32_to_bf16_bits(v[c]);
-      if (sec == 0) {
-        p.q_out[(long long)r * d + mr] = bits;
-      } else {
-        const int seq = r / p.R;
-        const int pos = p.row0 + r % p.R;
-        const long long plane = (((long long)p.layer * 2 + (sec - 1)) * p.b_seqs + seq) * p.n_heads + head;
-        p.kv[(plane * p.T_pad + pos) * hd + j] = bits;
+      if (r < N) {
+        const uint16_t bits = f32_to_bf16_bits(v[c]);
+        if (sec == 0) {
+          q_out[(long long)r * d + mr] = bits;
+        } else {
+          const long long plane = (((long long)layer * 2 + (sec - 1)) * b + seq) * H + head;
+          kv[(plane * T + row0 + i) * hd + j] = bits;
+        }
+      }
+      if (++i == R) {
+        i = 0;
+        ++seq;
       }
     }
   } else if constexpr (KIND == GEMM_RESID) {
-    const int d = p.d_model;
-    const float g = bf16_bits_to_f32(p.g_next[m]);
-    float sq[32];
+    const int d = p.d_model, R = p.R, row0 = p.row0, blk0 = p.blk_start, blen = p.blk_len;
+    const bool remap = p.remap != 0;
+    float* __restrict__ h = p.h;
+    uint16_t* __restrict__ xo = p.xn_out;
+    uint16_t* __restrict__ xl = p.xn_out_lo;
+    float* __restrict__ sso = p.ss_out;
+    const float g = bf16_bits_to_f32(__ldg(&p.g_next[m]));
+    float hv[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       const int r = r0 + c;
+      hv[c] = r < N ? __ldcg(&h[(long long)r * d + m]) : 0.0f;
+    }
+    float sq[32];
+    int seq = r0 / R, i = r0 - (r0 / R) * R;      // rows r0.. walk (seq, i) without dividing
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int r = r0 + c;
+      hv[c] += v[c];
+      int ro = r;
+      if (remap) {
+        const int bi = row0 + i - blk0;
+        ro = (bi >= 0 && bi < blen) ? seq * blen + bi : -1;
+      }
+      if (++i == R) {
+        i = 0;
+        ++seq;
+      }
       sq[c] = 0.0f;
-      if (r < p.N) {
-        const long long idx = (long long)r * d + m;
-        const float hv = p.h[idx] + v[c];
-        p.h[idx] = hv;
-        int ro = r;
-        if (p.remap) {
-          const int seq = r / p.R, pos = p.row0 + r % p.R;
-          const int bi = pos - p.blk_start;
-          ro = (bi >= 0 && bi < p.blk_len) ? seq * p.blk_len + bi : -1;
-        }
+      if (r < N) {
+        h[(long long)r * d + m] = hv[c];
         if (ro >= 0) {
-          const float xv = hv * g;
+          const float xv = hv[c] * g;
           const uint16_t hb = f32_to_bf16_bits(xv);
-          p.xn_out[(long long)ro * d + m] = hb;
-          if (p.xn_out_lo) p.xn_out_lo[(long long)ro * d + m] = f32_to_bf16_bits(xv - bf16_bits_to_f32(hb));
-          sq[c] = hv * hv;
+          xo[(long long)ro * d + m] = hb;
+          if (xl) xl[(long long)ro * d + m] = f32_to_bf16_bits(xv - bf16_bits_to_f32(hb));
+          sq[c] = hv[c] * hv[c];
         }
       }
     }
@@ -209,18 +244,21 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
     named_bar_sync(1, 128);
     if (l128 < 32) {
       const int r = r0 + l128;
-      if (r < p.N) {
+      if (r < N) {
         int ro = r;
-        if (p.remap) {
-          const int seq = r / p.R, pos = p.row0 + r % p.R;
-          const int bi = pos - p.blk_start;
-          ro = (bi >= 0 && bi < p.blk_len) ? seq * p.blk_len + bi : -1;
+        if (remap) {
+          const int seq = r / R, pos = row0 + r % R;
+          const int bi = pos - blk0;
+          ro = (bi >= 0 && bi < blen) ? seq * blen + bi : -1;
         }
         if (ro >= 0)
-          p.ss_out[(long long)ro * (d >> 7) + m_idx] = ((red[l128] + red[32 + l128]) + red[64 + l128]) + red[96 + l128];
+          sso[(long long)ro * (d >> 7) + m_idx] = ((red[l128] + red[32 + l128]) + red[64 + l128]) + red[96 + l128];
       }
     }
   } else if constexpr (KIND == GEMM_SWIGLU) {
+    uint16_t* __restrict__ act = p.act;
+    uint16_t* __restrict__ act_lo = p.act_lo;
+    const int ld = p.act_ld;
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] *= rs[c];
     named_bar_sync(1, 128);
@@ -229,24 +267,27 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
     named_bar_sync(1, 128);
     if (l128 < 64) {
       const int f = m_idx * 64 + l128;
+      float up[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) up[c] = xch[(l128 + 64) * 33 + c];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const int r = r0 + c;
-        if (r >= p.N) continue;
+        if (r >= N) continue;
         const float gt = v[c];
-        const float up = xch[(l128 + 64) * 33 + c];
-        const float a = gt / (1.0f + __expf(-gt)) * up;
+        const float a = gt / (1.0f + __expf(-gt)) * up[c];
         const uint16_t hb = f32_to_bf16_bits(a);
-        p.act[(long long)r * p.act_ld + f] = hb;
-        if (p.act_lo) p.act_lo[(long long)r * p.act_ld + f] = f32_to_bf16_bits(a - bf16_bits_to_f32(hb));
+        act[(long long)r * ld + f] = hb;
+        if (act_lo) act_lo[(long long)r * ld + f] = f32_to_bf16_bits(a - bf16_bits_to_f32(hb));
       }
     }
   } else if constexpr (KIND == GEMM_LMHEAD) {
+    const int M = p.M;
     float lg[32];
     int id[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      lg[c] = (m < p.M) ? v[c] * rs[c] : -INFINITY;
+      lg[c] = (m < M) ? v[c] * rs[c] : -INFINITY;
       id[c] = m;
     }
     float mx[32];
@@ -269,23 +310,23 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
     named_bar_sync(1, 128);
     if (l128 < 32) {
       const int r = r0 + l128;
-      if (r < p.N) {
-        float M = red[(0 * 32 + l128) * 3 + 0];
+      if (r < N) {
+        float Mx = red[(0 * 32 + l128) * 3 + 0];
         int A = __float_as_int(red[(0 * 32 + l128) * 3 + 2]);
 #pragma unroll
         for (int w = 1; w < 4; ++w) {
           const float mw = red[(w * 32 + l128) * 3 + 0];
-          if (mw > M) { M = mw; A = __float_as_int(red[(w * 32 + l128) * 3 + 2]); }
+          if (mw > Mx) { Mx = mw; A = __float_as_int(red[(w * 32 + l128) * 3 + 2]); }
         }
         float S = 0.0f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const float mw = red[(w * 32 + l128) * 3 + 0];
           const float sw = red[(w * 32 + l128) * 3 + 1];
-          S += (mw == -INFINITY) ? 0.0f : sw * exp2f((mw - M) * kLog2e);
+          S += (mw == -INFINITY) ? 0.0f : sw * exp2f((mw - Mx) * kLog2e);
         }
-        const long long o = (long long)m_idx * p.N + r;
-        p.st_m[o] = M;
+        const long long o = (long long)m_idx * N + r;
+        p.st_m[o] = Mx;
         p.st_s[o] = S;
         p.st_a[o] = A;
       }
@@ -485,8 +526,7 @@ __global__ void __launch_bounds__(192, 1)
       // every epilogue warp takes the same decision: a warp whose wait gave up
       // raised *abort_flag before this barrier
       mbar_wait(&tfull[buf], use & 1u, abort_flag, p.err, ERR_GEMM_TFULL);
-      named_bar_sync(1, 128);
-      if (*abort_flag) break;
+      if (named_bar_or(1, 128, *abort_flag != 0)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::B_ROWS);
       if (full_tile) {
@@ -516,20 +556,22 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
-        __threadfence();
         named_bar_sync(1, 128);
         const long long t0 = tile * p.kc, t1 = (tile + 1) * p.kc - 1;
         const long long c_first = sk_owner(t0, G, p.total), c_last = sk_owner(t1, G, p.total);
         if (l128 == 0) {
-          const int contributors = (int)(c_last - c_first + 1);
-          const int old = atomicAdd(&p.counters[tile], 1);
+          // contributors: the CTAs in [c_first, c_last] whose chunk range is not
+          // empty (with fewer chunks than CTAs some ranges are)
+          int contributors = 0;
+          for (long long ctr = c_first; ctr <= c_last; ++ctr)
+            contributors += (ctr * p.total / G) < ((ctr + 1) * p.total / G) ? 1 : 0;
+          const int old = atomic_add_acq_rel_gpu(&p.counters[tile], 1);
           const int last = (old == contributors - 1);
           if (last) p.counters[tile] = 0;
           *bcast = last;
         }
         named_bar_sync(1, 128);
         if (*bcast) {
-          __threadfence();
 #pragma unroll 1
           for (int c0 = 0; c0 < BN; c0 += 32) {
             float v[32];
@@ -537,6 +579,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int j = 0; j < 32; ++j) v[j] = 0.0f;
             for (long long ctr = c_first; ctr <= c_last; ++ctr) {
               const long long st = ctr * p.total / G;
+              if (st == (ctr + 1) * p.total / G) continue;   // empty range: no partial
               const long long sstart = st > t0 ? st : t0;
               const int sl = (sstart == st) ? 0 : 1;
               const float* src = p.ws + ((ctr * 2 + sl) * (long long)BN) * 128;

@@ -7,6 +7,7 @@
 
 #include "attention.cuh"
 #include "gemm.cuh"
+#include "step_kernel.cuh"
 
 namespace dllm {
 
@@ -49,6 +50,9 @@ inline cudaError_t launch_gemm(int kind, int bn, const CUtensorMap& a, const CUt
     default: return cudaErrorInvalidValue;
   }
 }
+
+cudaError_t launch_step_hd64(int bn, const StepArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_step_hd128(int bn, const StepArgs& a, int grid, cudaStream_t st);
 
 cudaError_t launch_attention(int hd, int wq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                              dim3 grid, cudaStream_t st, bool pdl);

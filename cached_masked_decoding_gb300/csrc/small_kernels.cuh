@@ -19,7 +19,7 @@ struct EmbedParams {
   int d, R, row0, T;
 };
 
-__global__ void __launch_bounds__(1024) embed_kernel(const EmbedParams p) {
+static __global__ void __launch_bounds__(1024) embed_kernel(const EmbedParams p) {
   griddep_launch_dependents();
   griddep_wait();
   const int r = blockIdx.x;
@@ -61,14 +61,16 @@ struct SelectRule {
 };
 
 // Select among the B positions of one sequence's block and commit.  Runs on
-// the whole CTA (any blockDim multiple of 32); conf_s / arg_s / flags in smem.
-// Writes x and returns the count through *count_out (thread 0).
-__device__ __forceinline__ void select_commit_cta(const float* conf_s, const int* arg_s, int* rank_s, float* eps_s,
-                                                  int B, int32_t* xblk, int mask_id, const SelectRule rule,
-                                                  int32_t* count_out, int* shared_best) {
-  const int tid = threadIdx.x;
+// a group of nthr threads (tid 0..nthr-1) that synchronise with sync();
+// conf_s / arg_s / rank_s / eps_s in shared memory.  Writes x and the count
+// (*count_out, by tid 0).
+template <typename Sync>
+__device__ __forceinline__ void select_commit_group(const float* conf_s, const int* arg_s, int* rank_s, float* eps_s,
+                                                    int B, int32_t* xblk, int mask_id, const SelectRule rule,
+                                                    int32_t* count_out, int* shared_best, int tid, int nthr,
+                                                    Sync sync) {
   // eligibility and confidence rank (descending confidence, ties by position)
-  for (int i = tid; i < B; i += blockDim.x) {
+  for (int i = tid; i < B; i += nthr) {
     const bool e = xblk[i] == mask_id;
     int rank = -1;
     if (e) {
@@ -83,16 +85,16 @@ __device__ __forceinline__ void select_commit_cta(const float* conf_s, const int
     rank_s[i] = rank;
   }
   if (tid == 0) *shared_best = 0;
-  __syncthreads();
+  sync();
   int n_sel = 0;  // select ranks < n_sel
   if (rule.policy == 0) {
     // threshold: count qualifying positions
-    for (int i = tid; i < B; i += blockDim.x)
+    for (int i = tid; i < B; i += nthr)
       if (rank_s[i] >= 0 && conf_s[i] >= rule.tau) atomicAdd(shared_best, 1);
-    __syncthreads();
+    sync();
     const int nq = *shared_best;
-    __syncthreads();
-    for (int i = tid; i < B; i += blockDim.x) {
+    sync();
+    for (int i = tid; i < B; i += nthr) {
       const int rk = rank_s[i];
       bool sel = false;
       if (rk >= 0) sel = (nq > 0) ? (conf_s[i] >= rule.tau) : (rk == 0);
@@ -103,20 +105,20 @@ __device__ __forceinline__ void select_commit_cta(const float* conf_s, const int
       n_sel = rule.k;
     } else if (rule.policy == 2) {
       // factor: largest n with (n+1)(1 - c_(n)) < f, c_(n) = confidence of rank n-1
-      for (int i = tid; i < B; i += blockDim.x) {
+      for (int i = tid; i < B; i += nthr) {
         const int rk = rank_s[i];
         if (rk >= 0) {
           const float lhs = __fmul_rn((float)(rk + 2), __fsub_rn(1.0f, conf_s[i]));
           if (lhs < rule.factor) atomicMax(shared_best, rk + 1);
         }
       }
-      __syncthreads();
+      sync();
       n_sel = max(*shared_best, 1);
     } else {
       // eq. 9 budget: sequential float32 prefix sum in rank order
-      for (int i = tid; i < B; i += blockDim.x)
+      for (int i = tid; i < B; i += nthr)
         if (rank_s[i] >= 0) eps_s[rank_s[i]] = __fsub_rn(1.0f, conf_s[i]);
-      __syncthreads();
+      sync();
       if (tid == 0) {
         int m = 0;
         for (int i = 0; i < B; ++i) m += rank_s[i] >= 0 ? 1 : 0;
@@ -129,26 +131,33 @@ __device__ __forceinline__ void select_commit_cta(const float* conf_s, const int
         }
         *shared_best = best;
       }
-      __syncthreads();
+      sync();
       n_sel = max(*shared_best, 1);
     }
-    __syncthreads();
-    for (int i = tid; i < B; i += blockDim.x) {
+    sync();
+    for (int i = tid; i < B; i += nthr) {
       const int rk = rank_s[i];
       eps_s[i] = (rk >= 0 && rk < n_sel) ? 1.0f : 0.0f;
     }
   }
-  __syncthreads();
+  sync();
   if (tid == 0) *shared_best = 0;
-  __syncthreads();
-  for (int i = tid; i < B; i += blockDim.x) {
+  sync();
+  for (int i = tid; i < B; i += nthr) {
     if (eps_s[i] != 0.0f) {
       xblk[i] = arg_s[i];
       atomicAdd(shared_best, 1);
     }
   }
-  __syncthreads();
+  sync();
   if (tid == 0) *count_out = *shared_best;
+}
+
+__device__ __forceinline__ void select_commit_cta(const float* conf_s, const int* arg_s, int* rank_s, float* eps_s,
+                                                  int B, int32_t* xblk, int mask_id, const SelectRule rule,
+                                                  int32_t* count_out, int* shared_best) {
+  select_commit_group(conf_s, arg_s, rank_s, eps_s, B, xblk, mask_id, rule, count_out, shared_best, threadIdx.x,
+                      blockDim.x, [] { __syncthreads(); });
 }
 
 // LM-head tile statistics -> (conf, arg) per block row, then select/commit.
@@ -189,7 +198,7 @@ __device__ __forceinline__ MaxSumArg msa_merge(MaxSumArg x, MaxSumArg y) {
   return r;
 }
 
-__global__ void __launch_bounds__(256) merge_select_kernel(const MergeParams p) {
+static __global__ void __launch_bounds__(256) merge_select_kernel(const MergeParams p) {
   __shared__ MaxSumArg part[8];
   __shared__ float conf_s[kMaxBlock];
   __shared__ int arg_s[kMaxBlock];
@@ -247,7 +256,7 @@ struct SelectParams {
   SelectRule rule;
 };
 
-__global__ void __launch_bounds__(256) select_kernel(const SelectParams p) {
+static __global__ void __launch_bounds__(256) select_kernel(const SelectParams p) {
   __shared__ float conf_s[kMaxBlock];
   __shared__ int arg_s[kMaxBlock];
   __shared__ int rank_s[kMaxBlock];

@@ -1,0 +1,41 @@
+// Instantiations of the persistent DualCache step kernel for head_dim 128.
+#include "launch.h"
+#include "step_kernel.cuh"
+
+namespace dllm {
+
+template <int BN>
+static cudaError_t go_step_128(const StepArgs& a, int grid, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(step_kernel<BN, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         StepCfg<BN, 128>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(step_kernel<BN, 128>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = StepCfg<BN, 128>::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_kernel<BN, 128>, a);
+}
+
+cudaError_t launch_step_hd128(int bn, const StepArgs& a, int grid, cudaStream_t st) {
+  switch (bn) {
+    case 32: return go_step_128<32>(a, grid, st);
+    case 64: return go_step_128<64>(a, grid, st);
+    case 128: return go_step_128<128>(a, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dllm

@@ -212,6 +212,26 @@ dllm_status dllm_read_kv(const dllm_state* s, int32_t layer, float* k, float* v)
 typedef enum dllm_precision { DLLM_PREC_SPLIT = 0, DLLM_PREC_BF16 = 1 } dllm_precision;
 dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode);
 
+/* DualCache steps with at most 128 activation rows (b * block <= 128, block
+ * <= 32) run by default as one persistent cooperative launch: one CTA per SM
+ * walks through every phase of the step (embedding, each layer's projections
+ * and attention, LM head, merge and selection) with grid barriers between
+ * them, and streams the next phase's weights while a phase finishes.
+ * enable 0 selects one launch per kernel instead (same arithmetic except the
+ * attention key split; tracing always uses it). */
+dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable);
+
+/* Diagnostics of the persistent step: with enable 1 the next persistent steps
+ * record, per CTA and phase, {time the CTA's workers finished the phase, time
+ * its TMA producer passed the barrier into the phase, time its MMA issuer
+ * finished the phase, time the producer issued the phase's last weight tile,
+ * time the workers started the phase, time the workers got the phase's first
+ * accumulator} in %globaltimer nanoseconds (uint64 [ctas][phases][6]; entry
+ * [cta][0][1] is the kernel start).  dllm_read_step_timeline copies the last step's record. */
+dllm_status dllm_state_set_step_timeline(dllm_state* s, int32_t enable);
+dllm_status dllm_read_step_timeline(const dllm_state* s, uint64_t* out, int64_t capacity, int32_t* ctas,
+                                    int32_t* phases);
+
 /* Record the residual stream after the embedding and after every layer on the
  * next steps (1) or stop (0).  dllm_read_trace copies the last step's record,
  * host float32 [n_layers+1][rows][d_model], rows = b * rows_per_seq as
@@ -225,8 +245,8 @@ dllm_status dllm_read_trace(const dllm_state* s, float* out, int64_t capacity_fl
  * milliseconds, launch counts and algorithmic bytes (weights, K/V and
  * activations each counted once).  Classes of a denoise step: 0 embed,
  * 1 qkv_gemm, 2 attention, 3 o_gemm, 4 gateup_gemm, 5 down_gemm,
- * 6 lm_head_gemm, 7 merge_select; a refresh's launches use 8 + the same index.
- * 16 classes in all.  The events serialise the kernels: not for the headline
+ * 6 lm_head_gemm, 7 merge_select; a refresh's launches use 8 + the same index;
+ * 14 is the persistent step kernel.  16 classes in all.  The events serialise the kernels: not for the headline
  * time. */
 dllm_status dllm_state_set_kernel_timing(dllm_state* s, int32_t enable);
 dllm_status dllm_kernel_times(const dllm_state* s, double* ms, int64_t* launches,

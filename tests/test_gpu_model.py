@@ -114,6 +114,41 @@ def test_other_rules_dual(gmodel, omodel, rule):
     st.free()
 
 
+@pytest.mark.parametrize("b,P,B", [(1, 32, 16), (2, 45, 16), (4, 32, 32)])
+def test_persistent_step_matches_per_kernel_launches(gmodel, b, P, B):
+    """The cooperative single-launch DualCache step computes what the chain of
+    per-kernel launches computes (the attention key split differs, so values
+    agree to float32 rounding, not bit for bit)."""
+    gen = 2 * B
+    pr = synth.prompts(CFG, 5, b, P)
+    outs = []
+    for persistent in (False, True):
+        st = binding.State(gmodel, pr, b, P, gen, B)
+        st.set_persistent(persistent)
+        st.refresh()
+        st.step(0, 0.9, "dual")
+        t, c, a = st.read()
+        outs.append((t, c, a, st.hidden()))
+        st.free()
+    (t0, c0, a0, h0), (t1, c1, a1, h1) = outs
+    assert np.abs(c0 - c1).max() <= 1e-4
+    np.testing.assert_array_equal(a0, a1)
+    np.testing.assert_array_equal(t0, t1)
+    rel = np.linalg.norm(h0 - h1, axis=-1) / np.linalg.norm(h0, axis=-1)
+    assert rel.max() <= 1e-4
+
+
+def test_persistent_whole_run_matches_oracle_8_blocks(gmodel, omodel):
+    """A longer DualCache run through the persistent step (8 blocks, 2 sequences)."""
+    P, gen, B, b = 24, 128, 16, 2
+    pr = synth.prompts(CFG, 6, b, P)
+    st = binding.State(gmodel, pr, b, P, gen, B)
+    dec = OS.Decoder(omodel, pr, gen, B, "dual")
+    rep = run_synced(st, dec, OS.Rule(OS.THRESHOLD, 0.9), "dual")
+    assert rep.steps >= gen // B
+    st.free()
+
+
 def test_bf16_activation_mode(gmodel, omodel):
     """DLLM_PREC_BF16 rounds every GEMM input to bf16: the tiny model's steep
     LM head (logit sigma 10) turns those roundings into max-prob errors of up
