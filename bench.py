@@ -30,10 +30,42 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from cached_masked_decoding_gb300 import configs, roofline, synth  # noqa: E402
+from cached_masked_decoding_gb300 import configs, replicas, roofline, synth  # noqa: E402
 
 METRIC = "committed tokens/s per GB300 (8B dLLM, blk32, DualCache, τ=0.9); % HBM roofline"
 UNIT = "tokens/s"
+
+
+# DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernel, keyed by (kernel class, workload), with the SHA-256 prefix of
+# the device sources it was measured on and how the figure was obtained.  A
+# figure whose sources have changed since is reported as null.
+STEP_SOURCES = ("attention.cuh", "gemm.cuh", "ptx.cuh", "small_kernels.cuh", "step_kernel.cuh",
+                "step_hd64.cu", "step_hd128.cu")
+MEASURED_TRAFFIC = {
+    ("persistent_step", "1b"): (1.830795e9, "6cc72654ab5228be", "ncu --set full capture of one launch"),
+    # the 8B launch is too large for a multi-pass capture: the 1B capture's
+    # traffic / algorithmic ratio (1.0169) times the 8B launch's algorithmic bytes
+    ("persistent_step", "8b"): (1.0169 * 15397289984.0, "6cc72654ab5228be",
+                                "scaled from the 1B capture by algorithmic bytes"),
+}
+
+
+def sources_sha() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in STEP_SOURCES:
+        with open(os.path.join(ROOT, "cached_masked_decoding_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    rec = MEASURED_TRAFFIC.get((kernel, workload))
+    if rec is None or rec[1] != sources_sha():
+        return None, None
+    return rec[0], rec[2]
 
 
 def load_peaks() -> dict:
@@ -183,8 +215,9 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     model = binding.Model.from_synth(cfg, seed=wl.seed)
     stream = torch.cuda.current_stream()
     b, P, gen, B = wl.batch, wl.prompt_len, wl.gen_len, wl.block
+    sh = replicas.shard(rank, world, b)
     prompts_dev = torch.empty(b * max(P, 1), dtype=torch.int32, device="cuda")
-    synth.device_fill_prompts(prompts_dev.data_ptr(), cfg, wl.seed, b, P, first_seq=rank * b,
+    synth.device_fill_prompts(prompts_dev.data_ptr(), cfg, wl.seed, b, P, first_seq=sh.first_seq,
                               stream=stream.cuda_stream)
     state = binding.State(model, None, b, P, gen, B, stream=stream.cuda_stream)
     state.set_precision(args.precision)
@@ -215,11 +248,8 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
         torch.distributed.barrier()
     clk = clocks.stop()
     elapsed_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    tokens = sum(s["committed"] for s in stats) * world
+    elapsed_ms, tokens = replicas.reduce_timing(elapsed_ms, sum(s["committed"] for s in stats),
+                                                device=torch.device("cuda", local_rank))
     value = tokens / (elapsed_ms / 1e3)
     launches = sum(s["kernel_launches"] for s in stats) + args.steps   # + one canvas reset each
     steps = sum(s["steps"] for s in stats)
@@ -250,10 +280,12 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     n_refresh_timed = max(kt["refresh_qkv_gemm"]["launches"] // cfg.n_layers, 1)
 
     # ---------------------------------------------------------------- end to end (host buffers)
-    host_prompts = synth.prompts(cfg, wl.seed, b, P, first_seq=rank * b)
+    host_prompts = synth.prompts(cfg, wl.seed, b, P, first_seq=sh.first_seq)
     toks = np.zeros((b, wl.T), dtype=np.int32)
     e2e_state = state
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     e2e_tokens = 0
     e2e_steps = 0
@@ -263,10 +295,13 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
         toks[:] = e2e_state.tokens()                    # D2H: canvas b*T int32
         e2e_tokens += st["committed"]
         e2e_steps += st["steps"]
-    e2e_s = time.perf_counter() - t0
+    e2e_ms, e2e_tokens = replicas.reduce_timing((time.perf_counter() - t0) * 1e3, e2e_tokens,
+                                                device=torch.device("cuda", local_rank))
+    e2e_s = e2e_ms / 1e3
     h2d = b * wl.T * 4
     d2h = b * wl.T * 4 + (e2e_steps // max(args.steps, 1)) * (b + 1) * 4
 
+    traffic, traffic_src = measured_traffic(dom, wl.name) if mode == "dual" and b == wl.batch else (None, None)
     step_bytes = roofline.dual_step_bytes(cfg.weight_bytes_step(), cfg.kv_bytes(wl.T, b))
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -276,19 +311,19 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
             "workload": f"{wl.name}: {cfg.name}-shaped random-init dLLM, batch {b}, prompt {P}, gen {gen}, "
                         f"block {B}, tau {wl.tau}, {mode} cache",
             "model": f"{cfg.n_layers}L d{cfg.d_model} H{cfg.n_heads} F{cfg.d_ffn} V{cfg.vocab} (random init)",
-            "global_batch": b * world, "seq_len": wl.T, "block": B, "tau": wl.tau, "cache_mode": mode,
+            "global_batch": sh.global_batch, "seq_len": wl.T, "block": B, "tau": wl.tau, "cache_mode": mode,
             "precision": f"{args.precision} activations, bf16 weights and K/V, f32 accumulate",
             "step_launch": "persistent (one cooperative launch per denoise step)" if args.persistent
             else "one launch per kernel",
             "l2": "inputs larger than L2 (every step streams all weights)",
             "parallelism": f"replicas x{world} (no data-path collective)",
         },
-        "e2e": {"value": e2e_tokens * world / e2e_s if args.e2e else None, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_tokens / e2e_s if args.e2e else None, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "api": "dllm_state_reset(host prompts) + dllm_run + dllm_read_state(host tokens)"},
         "roofline": {
             "bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "traffic_source": traffic_src,
             "peak_source": f"{peaks['source']} HBM copy bandwidth",
             "timing": "per-launch CUDA events around each kernel, one extra generation after the timed region",
             "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
