@@ -91,6 +91,7 @@ SIGNATURES = {
     "dllm_read_step_timeline": (_I32, [_P, _P, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "dllm_op_gemm_trace": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _P, ctypes.POINTER(_I32), _P]),
     "dllm_op_attention": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
+    "dllm_op_attention_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
     "dllm_op_select_commit": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(Select), _P, _P]),
     "dllm_last_error": (ctypes.c_char_p, []),
     "dllm_status_string": (ctypes.c_char_p, [_I32]),
@@ -342,6 +343,12 @@ def op_attention(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, b: int, H: int,
                  stream: int = 0):
     check(lib().dllm_op_attention(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                                   ctypes.c_void_p(o_ptr), b, H, hd, R, T, ctypes.c_void_p(stream)))
+
+
+def op_attention_noalloc(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, b: int, H: int, hd: int, R: int,
+                         T: int, stream: int = 0):
+    check(lib().dllm_op_attention_noalloc(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                                          ctypes.c_void_p(o_ptr), b, H, hd, R, T, ctypes.c_void_p(stream)))
 
 
 def op_select_commit(conf_ptr: int, arg_ptr: int, x_ptr: int, b: int, T: int, blk_start: int, B: int,

@@ -1813,6 +1813,99 @@ extern "C" dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_ca
   return DLLM_OK;
 }
 
+// ---------------------------------------------------------------- attention without allocation
+// Scratch of dllm_op_attention_noalloc, in static storage of this library's
+// module: the key-split partials (o, m, l) and the per-work merge counters.
+// Module load zero-fills it; each work's last-arriving split puts its counter
+// back to 0, so the counters are zero again after every completed launch.
+constexpr size_t kNoAllocAttnFloats = size_t(1) << 20;   // 4 MiB of split partials
+constexpr int kNoAllocAttnWorks = 4096;                   // merge counters (b * H * query tiles)
+static __device__ __align__(256) float g_noalloc_attn_ws[kNoAllocAttnFloats];
+static __device__ __align__(256) int g_noalloc_attn_cnt[kNoAllocAttnWorks];
+static __device__ __align__(256) int g_noalloc_attn_err[64];
+
+namespace {
+
+struct NoAllocScratch {
+  float* ws;
+  int* cnt;
+  int* err;
+};
+constexpr int kNoAllocDevices = 64;
+std::mutex g_noalloc_mu;
+NoAllocScratch g_noalloc[kNoAllocDevices] = {};
+
+// Device addresses of the static scratch for the current device, looked up
+// once per device (cudaGetSymbolAddress with that device current).
+dllm_status noalloc_scratch(NoAllocScratch* out) {
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocDevices) {
+    set_error("device %d outside the %d devices the no-alloc scratch table holds", dev, kNoAllocDevices);
+    return DLLM_EINVAL;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  NoAllocScratch& s = g_noalloc[dev];
+  if (!s.ws) {
+    NoAllocScratch t = {};
+    CK(cudaGetSymbolAddress(reinterpret_cast<void**>(&t.ws), g_noalloc_attn_ws));
+    CK(cudaGetSymbolAddress(reinterpret_cast<void**>(&t.cnt), g_noalloc_attn_cnt));
+    CK(cudaGetSymbolAddress(reinterpret_cast<void**>(&t.err), g_noalloc_attn_err));
+    s = t;
+  }
+  *out = s;
+  return DLLM_OK;
+}
+
+}  // namespace
+
+extern "C" dllm_status dllm_op_attention_noalloc(const uint16_t* q, const uint16_t* k_cache,
+                                                 const uint16_t* v_cache, uint16_t* out, int32_t b, int32_t H,
+                                                 int32_t hd, int32_t R, int32_t T, void* stream) {
+  if (!q || !k_cache || !v_cache || !out || b < 1 || H < 1 || (hd != 64 && hd != 128) || R < 1 || T < 1 ||
+      !aligned16(k_cache) || !aligned16(v_cache)) {
+    set_error("bad attention arguments: b=%d H=%d hd=%d R=%d T=%d", b, H, hd, R, T);
+    return DLLM_EINVAL;
+  }
+  NoAllocScratch sc;
+  CKS(noalloc_scratch(&sc));
+  // the same plan as dllm_op_attention, so that both give identical outputs
+  const AttnPlan a = plan_attention(b, H, R, T, device_sms());
+  const int QT = 16 * a.wq;
+  const size_t works = (size_t)b * H * a.q_tiles;
+  const size_t floats = a.splits > 1 ? works * a.splits * QT * (hd + 2) : 0;
+  if (floats > kNoAllocAttnFloats || (a.splits > 1 && works > (size_t)kNoAllocAttnWorks)) {
+    set_error("attention b=%d H=%d hd=%d R=%d T=%d needs %zu scratch floats and %zu counters; the no-alloc "
+              "variant holds %zu floats and %d counters (use dllm_op_attention)",
+              b, H, hd, R, T, floats, works, kNoAllocAttnFloats, kNoAllocAttnWorks);
+    return DLLM_EINVAL;
+  }
+  CUtensorMap tk, tv;
+  CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H));
+  CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H));
+  AttnParams p = {};
+  p.q = q;
+  p.o = out;
+  p.o_lo = nullptr;
+  p.R = R;
+  p.b = b;
+  p.H = H;
+  p.T = T;
+  p.z_k0 = 0;
+  p.z_v0 = 0;
+  p.q_tiles = a.q_tiles;
+  p.splits = a.splits;
+  p.kps = a.kps;
+  p.scale_log2 = kLog2e / std::sqrt((float)hd);
+  p.ws_o = sc.ws;
+  p.ws_ml = sc.ws + works * a.splits * QT * hd;
+  p.counters = sc.cnt;
+  p.err = sc.err;
+  CK(launch_attention(hd, a.wq, tk, tv, p, dim3(a.splits, a.q_tiles * H, b), static_cast<cudaStream_t>(stream),
+                      false));
+  return DLLM_OK;
+}
+
 extern "C" dllm_status dllm_op_select_commit(const float* conf, const int32_t* arg, int32_t* x, int32_t b, int32_t T,
                                              int32_t blk_start, int32_t B, int32_t mask_id, const dllm_select* sel,
                                              int32_t* count, void* stream) {

@@ -279,6 +279,41 @@ dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_cache, const 
                               uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R,
                               int32_t T, void* cuda_stream);
 
+/* dllm_op_attention with no allocation of any kind.  The pages have no
+ * counterpart: the operation is the same non-causal attention (eq. 3 of the
+ * Fast-dLLM reading notes, section 2), same arguments, layouts and output,
+ * bit-identical to dllm_op_attention for every shape it accepts.  What
+ * differs is where the scratch lives.  dllm_op_attention grows a
+ * library-owned workspace with cudaMalloc + cudaMemset the first time a shape
+ * needs more; this variant uses a fixed scratch in static device storage of
+ * the library (key-split partials: 1 Mi floats = 4 MiB; merge counters: 4096)
+ * and never calls cudaMalloc, cudaFree or an allocating library.  It serves
+ * callers that must not allocate device memory at call time: a caller whose
+ * device memory is fully reserved up front (weights and K/V pools sized to
+ * the card), or one that issues work where an allocation, or the device-wide
+ * synchronisation a cudaMalloc/cudaMemset may imply, is not allowed.
+ *  - Set-up: the first call on each device looks up the scratch's device
+ *    address (cudaGetSymbolAddress with that device current) and the driver's
+ *    tensor-map entry point; make that first call before any stream capture.
+ *  - Limit: b*H*ceil(R/QT) merge works and, when the keys are split,
+ *    works*splits*QT*(hd+2) floats (QT = 32 for R <= 32, else 64; splits as
+ *    dllm_op_attention plans them for this GPU).  A call over the limit
+ *    returns DLLM_EINVAL, launches nothing and names the limit in
+ *    dllm_last_error(); use dllm_op_attention for it.  The 8B DualCache block
+ *    (b=1, H=32, hd=128, R=32, T=768) fits.
+ *  - Zero state: the merge counters must be zero when a launch starts.  They
+ *    are zero at library load and every completed launch leaves them zero; a
+ *    launch that ended in a bounded-wait timeout leaves them undefined.
+ *  - Concurrency: all calls on a device share the one scratch.  Calls ordered
+ *    on one stream are safe; calls that may overlap (different streams, or
+ *    different host threads without ordering) race on the scratch and give
+ *    wrong results.
+ *  - Asynchronous like dllm_op_attention: returns after the launch. */
+dllm_status dllm_op_attention_noalloc(const uint16_t* q, const uint16_t* k_cache,
+                                      const uint16_t* v_cache, uint16_t* out, int32_t b,
+                                      int32_t H, int32_t hd, int32_t R, int32_t T,
+                                      void* cuda_stream);
+
 /* The selection/commit kernel alone: given conf [b][B] float32 and arg [b][B]
  * int32 (device), select on the MASK positions x[s][blk_start .. +B) of the
  * canvas x [b][T] (device int32), write the chosen arg ids into x and the
