@@ -44,10 +44,8 @@ STEP_SOURCES = ("attention.cuh", "gemm.cuh", "ptx.cuh", "small_kernels.cuh", "st
                 "step_hd64.cu", "step_hd128.cu")
 MEASURED_TRAFFIC = {
     ("persistent_step", "1b"): (1.830795e9, "6cc72654ab5228be", "ncu --set full capture of one launch"),
-    # the 8B launch is too large for a multi-pass capture: the 1B capture's
-    # traffic / algorithmic ratio (1.0169) times the 8B launch's algorithmic bytes
-    ("persistent_step", "8b"): (1.0169 * 15397289984.0, "6cc72654ab5228be",
-                                "scaled from the 1B capture by algorithmic bytes"),
+    ("persistent_step", "8b"): (15.50e9 + 105.65e6, "6cc72654ab5228be",
+                                "ncu one-pass capture of dram__bytes_read.sum + dram__bytes_write.sum, one launch"),
 }
 
 
