@@ -300,7 +300,9 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     d2h = b * wl.T * 4 + (e2e_steps // max(args.steps, 1)) * (b + 1) * 4
 
     traffic, traffic_src = measured_traffic(dom, wl.name) if mode == "dual" and b == wl.batch else (None, None)
-    step_bytes = roofline.dual_step_bytes(cfg.weight_bytes_step(), cfg.kv_bytes(wl.T, b))
+    # split precision keeps the K/V cache as hi/lo bf16 pairs: twice the K/V bytes
+    kv_parts = 2 if args.precision == "split" else 1
+    step_bytes = roofline.dual_step_bytes(cfg.weight_bytes_step(), kv_parts * cfg.kv_bytes(wl.T, b))
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,

@@ -122,8 +122,12 @@ dllm_status map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
   return DLLM_OK;
 }
 
-// 3-D bf16 map over [planes][T][hd] (K or V planes of the cache), box [1][64][64].
-dllm_status map_kv(CUtensorMap* m, const void* base, uint64_t hd, uint64_t T, uint64_t planes) {
+// Keys per shared-memory tile of the state's attention (32: room for the low
+// halves of K and V next to them).
+constexpr int kStateAttnKT = 32;
+
+// 3-D bf16 map over [planes][T][hd] (K or V planes of the cache), box [1][keys][64].
+dllm_status map_kv(CUtensorMap* m, const void* base, uint64_t hd, uint64_t T, uint64_t planes, uint32_t keys) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -131,7 +135,7 @@ dllm_status map_kv(CUtensorMap* m, const void* base, uint64_t hd, uint64_t T, ui
   }
   cuuint64_t dims[3] = {hd, T, planes};
   cuuint64_t strides[2] = {hd * 2, T * hd * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {64, keys, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -475,6 +479,7 @@ struct dllm_state {
   uint16_t* xn_lo = nullptr;
   float* ss = nullptr;
   uint16_t* q = nullptr;
+  uint16_t* q_lo = nullptr;
   uint16_t* ao = nullptr;
   uint16_t* ao_lo = nullptr;
   uint16_t* act = nullptr;
@@ -629,11 +634,11 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
   auto al = [](size_t bytes) { return (bytes + 1023) / 1024 * 1024; };
   size_t total = 0;
   const size_t o_x = total; total += al(n_max * 4);
-  const size_t o_kv = total; total += al(L * 2 * b * H * T * hd * 2);
+  const size_t o_kv = total; total += al(L * 4 * b * H * T * hd * 2);
   const size_t o_h = total; total += al(n_max * d * 4);
   const size_t o_xn = total; total += al(2 * n_max * d * 2);
   const size_t o_ss = total; total += al(n_max * d_tiles * 4);
-  const size_t o_q = total; total += al(n_max * d * 2);
+  const size_t o_q = total; total += al(2 * n_max * d * 2);
   const size_t o_ao = total; total += al(2 * n_max * d * 2);
   const size_t o_act = total; total += al(2 * n_max * F * 2);
   const size_t o_xf = total; total += al(2 * n_lm * d * 2);
@@ -669,6 +674,7 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
   s->xn_lo = s->xn + n_max * d;
   s->ss = reinterpret_cast<float*>(a + o_ss);
   s->q = reinterpret_cast<uint16_t*>(a + o_q);
+  s->q_lo = s->q + n_max * d;
   s->ao = reinterpret_cast<uint16_t*>(a + o_ao);
   s->ao_lo = s->ao + n_max * d;
   s->act = reinterpret_cast<uint16_t*>(a + o_act);
@@ -734,7 +740,7 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
       return fail(DLLM_ECUDA);
     }
   }
-  if ((st = map_kv(&s->tm_kv, s->kv, hd, T, L * 2 * b * H)) != DLLM_OK) return fail(st);
+  if ((st = map_kv(&s->tm_kv, s->kv, hd, T, L * 4 * b * H, kStateAttnKT)) != DLLM_OK) return fail(st);
   if ((st = upload_canvas(s)) != DLLM_OK) return fail(st);
   *out = s;
   return DLLM_OK;
@@ -757,7 +763,7 @@ extern "C" dllm_status dllm_state_reset(dllm_state* s, const int32_t* prompts) {
     std::memcpy(s->prompts.data(), prompts, sizeof(int32_t) * s->b * s->P);
   }
   reset_counters(s);
-  CK(cudaMemsetAsync(s->kv, 0, (size_t)s->m->cfg.n_layers * 2 * s->b * s->m->cfg.d_model * s->T * 2, s->st));
+  CK(cudaMemsetAsync(s->kv, 0, (size_t)s->m->cfg.n_layers * 4 * s->b * s->m->cfg.d_model * s->T * 2, s->st));
   return upload_canvas(s);
 }
 
@@ -897,14 +903,19 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
   const long long works = (long long)s->b * c.n_heads * a.q_tiles;
   AttnParams p = {};
   p.q = s->q;
+  p.q_lo = s->split ? s->q_lo : nullptr;
+  p.kv_lo = s->split ? 1 : 0;
   p.o = s->ao;
   p.o_lo = s->split ? s->ao_lo : nullptr;
   p.R = R;
   p.b = s->b;
   p.H = c.n_heads;
   p.T = s->T;
-  p.z_k0 = (layer * 2 + 0) * s->b * c.n_heads;
-  p.z_v0 = (layer * 2 + 1) * s->b * c.n_heads;
+  const int bh = s->b * c.n_heads;
+  p.z_k0 = ((layer * 2 + 0) * 2 + 0) * bh;
+  p.z_kl0 = ((layer * 2 + 0) * 2 + 1) * bh;
+  p.z_v0 = ((layer * 2 + 1) * 2 + 0) * bh;
+  p.z_vl0 = ((layer * 2 + 1) * 2 + 1) * bh;
   p.q_tiles = a.q_tiles;
   p.splits = a.splits;
   p.kps = a.kps;
@@ -915,8 +926,8 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
   p.err = s->count_err + s->b;
   if (s->timing) s->kt_bytes[cls] += bytes;
   Timed t(s, cls, bytes);
-  CK(launch_attention(c.head_dim, a.wq, s->tm_kv, s->tm_kv, p, dim3(a.splits, a.q_tiles * c.n_heads, s->b), s->st,
-                      true));
+  CK(launch_attention(c.head_dim, a.wq, kStateAttnKT, s->tm_kv, s->tm_kv, p,
+                      dim3(a.splits, a.q_tiles * c.n_heads, s->b), s->st, true));
   ++s->launches;
   return DLLM_OK;
 }
@@ -944,7 +955,7 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
     ++s->launches;
   }
   if (s->trace) CK(cudaMemcpyAsync(s->trace_buf, s->h, (size_t)n * d * 4, cudaMemcpyDeviceToDevice, s->st));
-  const double kv_bytes = (double)s->b * s->T * d * 2 * 2;
+  const double kv_bytes = (double)s->b * s->T * d * 2 * 2 * (s->split ? 2 : 1);
   for (int l = 0; l < L; ++l) {
     const LayerW& w = m->layers[l];
     const bool last = l == L - 1;
@@ -956,6 +967,7 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
     p.R = R;
     p.row0 = row0;
     p.q_out = s->q;
+    p.q_out_lo = s->split ? s->q_lo : nullptr;
     p.kv = s->kv;
     p.rope_cs = s->rope;
     p.d_model = d;
@@ -1111,6 +1123,7 @@ dllm_status build_step(dllm_state* s) {
       q.g.R = s->B;
       q.g.row0 = blk;
       q.g.q_out = s->q;
+      q.g.q_out_lo = s->split ? s->q_lo : nullptr;
       q.g.kv = s->kv;
       q.g.rope_cs = s->rope;
       q.g.d_model = d;
@@ -1244,6 +1257,8 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
   const int QT = 32;
   const long long works = (long long)s->b * c.n_heads * ap.q_tiles;
   a.attn.q = s->q;
+  a.attn.q_lo = s->split ? s->q_lo : nullptr;
+  a.attn.kv_lo = s->split ? 1 : 0;
   a.attn.o = s->ao;
   a.attn.o_lo = s->split ? s->ao_lo : nullptr;
   a.attn.R = s->B;
@@ -1283,7 +1298,7 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
   CK(cudaMemsetAsync(s->d_bar, 0, 4, s->st));
   const double bytes = (double)s->m->cfg.n_layers * 2.0 *
                            (4.0 * d * d + 3.0 * (double)d * c.d_ffn) +
-                       2.0 * V * d + (double)s->b * s->T * d * 2 * 2 * c.n_layers;
+                       2.0 * V * d + (double)s->b * s->T * d * 2 * 2 * c.n_layers * (s->split ? 2 : 1);
   if (s->timing) s->kt_bytes[KC_PSTEP] += bytes;
   Timed t(s, KC_PSTEP, bytes);
   const int grid = s->m->sms;
@@ -1548,15 +1563,20 @@ extern "C" dllm_status dllm_read_kv(const dllm_state* s, int32_t layer, float* k
   }
   const dllm_config& c = s->m->cfg;
   const size_t plane = (size_t)s->b * c.n_heads * s->T * c.head_dim;
-  std::vector<uint16_t> buf(plane);
+  std::vector<uint16_t> hi(plane), lo(plane);
   CK(cudaStreamSynchronize(s->st));
   for (int kvi = 0; kvi < 2; ++kvi) {
     float* dst = kvi == 0 ? k : v;
     if (!dst) continue;
-    CK(cudaMemcpy(buf.data(), s->kv + ((size_t)layer * 2 + kvi) * plane, plane * 2, cudaMemcpyDeviceToHost));
+    const uint16_t* src = s->kv + ((size_t)layer * 2 + kvi) * 2 * plane;
+    CK(cudaMemcpy(hi.data(), src, plane * 2, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(lo.data(), src + plane, plane * 2, cudaMemcpyDeviceToHost));
     for (size_t i = 0; i < plane; ++i) {
-      uint32_t u = (uint32_t)buf[i] << 16;
-      std::memcpy(&dst[i], &u, 4);
+      const uint32_t uh = (uint32_t)hi[i] << 16, ul = (uint32_t)lo[i] << 16;
+      float fh, fl;
+      std::memcpy(&fh, &uh, 4);
+      std::memcpy(&fl, &ul, 4);
+      dst[i] = s->split ? fh + fl : fh;
     }
   }
   return DLLM_OK;
@@ -1788,8 +1808,8 @@ extern "C" dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_ca
   OpWorkspace* w = nullptr;
   CKS(op_workspace(&w, 1, works * a.splits * QT * (hd + 2), works));
   CUtensorMap tk, tv;
-  CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H));
-  CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H));
+  CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H, 64));
+  CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H, 64));
   AttnParams p = {};
   p.q = q;
   p.o = out;
@@ -1808,7 +1828,7 @@ extern "C" dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_ca
   p.ws_ml = w->attn + works * a.splits * QT * hd;
   p.counters = w->attn_cnt;
   p.err = w->err;
-  CK(launch_attention(hd, a.wq, tk, tv, p, dim3(a.splits, a.q_tiles * H, b), static_cast<cudaStream_t>(stream),
+  CK(launch_attention(hd, a.wq, 64, tk, tv, p, dim3(a.splits, a.q_tiles * H, b), static_cast<cudaStream_t>(stream),
                       false));
   return DLLM_OK;
 }
@@ -1881,8 +1901,8 @@ extern "C" dllm_status dllm_op_attention_noalloc(const uint16_t* q, const uint16
     return DLLM_EINVAL;
   }
   CUtensorMap tk, tv;
-  CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H));
-  CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H));
+  CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H, 64));
+  CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H, 64));
   AttnParams p = {};
   p.q = q;
   p.o = out;
@@ -1901,7 +1921,7 @@ extern "C" dllm_status dllm_op_attention_noalloc(const uint16_t* q, const uint16
   p.ws_ml = sc.ws + works * a.splits * QT * hd;
   p.counters = sc.cnt;
   p.err = sc.err;
-  CK(launch_attention(hd, a.wq, tk, tv, p, dim3(a.splits, a.q_tiles * H, b), static_cast<cudaStream_t>(stream),
+  CK(launch_attention(hd, a.wq, 64, tk, tv, p, dim3(a.splits, a.q_tiles * H, b), static_cast<cudaStream_t>(stream),
                       false));
   return DLLM_OK;
 }

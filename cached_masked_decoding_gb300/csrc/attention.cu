@@ -1,32 +1,38 @@
-// Instantiations of the block-attention kernel (head_dim 64/128, 2 or 4 query warps).
+// Instantiations of the block-attention kernel (head_dim 64/128, 2 or 4 query
+// warps, 64-key tiles in bf16 or 32-key tiles that also carry the low halves).
 #include "launch.h"
 
 namespace dllm {
 
-template <int HD, int WQ>
+template <int HD, int WQ, int KT>
 static cudaError_t go_attn(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
                            cudaStream_t st, bool pdl) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, WQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         AttnCfg<HD>::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, WQ, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AttnCfg<HD, KT>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     // every kernel of the step asks for the same L1/shared split, so an SM
     // never has to drain and reconfigure between them
-    e = cudaFuncSetAttribute(attn_kernel<HD, WQ>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(attn_kernel<HD, WQ, KT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(attn_kernel<HD, WQ>, grid, dim3(128), AttnCfg<HD>::SMEM_BYTES, st, pdl, tk, tv, p);
+  return launch_ex(attn_kernel<HD, WQ, KT>, grid, dim3(128), AttnCfg<HD, KT>::SMEM_BYTES, st, pdl, tk, tv, p);
 }
 
-cudaError_t launch_attention(int hd, int wq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                             dim3 grid, cudaStream_t st, bool pdl) {
-  if (hd == 64 && wq == 2) return go_attn<64, 2>(tk, tv, p, grid, st, pdl);
-  if (hd == 64 && wq == 4) return go_attn<64, 4>(tk, tv, p, grid, st, pdl);
-  if (hd == 128 && wq == 2) return go_attn<128, 2>(tk, tv, p, grid, st, pdl);
-  if (hd == 128 && wq == 4) return go_attn<128, 4>(tk, tv, p, grid, st, pdl);
+cudaError_t launch_attention(int hd, int wq, int kt, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const AttnParams& p, dim3 grid, cudaStream_t st, bool pdl) {
+  if (kt == 64 && p.kv_lo) return cudaErrorInvalidValue;   // 64-key tiles have no room for the low halves
+  if (hd == 64 && wq == 2) return kt == 32 ? go_attn<64, 2, 32>(tk, tv, p, grid, st, pdl)
+                                           : go_attn<64, 2, 64>(tk, tv, p, grid, st, pdl);
+  if (hd == 64 && wq == 4) return kt == 32 ? go_attn<64, 4, 32>(tk, tv, p, grid, st, pdl)
+                                           : go_attn<64, 4, 64>(tk, tv, p, grid, st, pdl);
+  if (hd == 128 && wq == 2) return kt == 32 ? go_attn<128, 2, 32>(tk, tv, p, grid, st, pdl)
+                                            : go_attn<128, 2, 64>(tk, tv, p, grid, st, pdl);
+  if (hd == 128 && wq == 4) return kt == 32 ? go_attn<128, 4, 32>(tk, tv, p, grid, st, pdl)
+                                            : go_attn<128, 4, 64>(tk, tv, p, grid, st, pdl);
   return cudaErrorInvalidValue;
 }
 

@@ -11,6 +11,12 @@
 // exponentials), merges the warps' key halves through shared memory and the
 // key splits through a workspace: the last split to finish combines all
 // partials in split order.
+//
+// Split precision (kv_lo = 1): q, K and V each come as a bf16 pair x = hi + lo
+// (lo = bf16(x - hi), about 16 significant bits together), and so does P in
+// registers; S = Qh Kh + Ql Kh + Qh Kl and O = Ph Vh + Pl Vh + Ph Vl (the lo*lo
+// terms are below 2^-16 relative).  With bf16 alone the rounding of the
+// cached K/V moves final hidden states by a few 1e-3 relative.
 #pragma once
 
 #include "ptx.cuh"
@@ -19,10 +25,13 @@ namespace dllm {
 
 struct AttnParams {
   const uint16_t* q;   // [b*R][H][HD]
+  const uint16_t* q_lo;  // low halves of q (kv_lo = 1), else unused
   uint16_t* o;         // [b*R][H*HD]
   uint16_t* o_lo;      // low halves (o - bf16(o)), or null
   int R, b, H, T;      // query rows per sequence, sequences, heads, valid keys
   int z_k0, z_v0;      // plane of (seq 0, head 0) in the K and V maps; plane = z0 + seq*H + head
+  int z_kl0, z_vl0;    // the same for the low halves of K and V (kv_lo = 1)
+  int kv_lo;           // 1: split-precision q, K, V and P
   int q_tiles, splits, kps;  // query tiles per (seq, head), key splits, keys per split (multiple of 64)
   float scale_log2;    // log2(e) / sqrt(HD)
   float* ws_o;         // [works][splits][QT][HD]
@@ -31,12 +40,12 @@ struct AttnParams {
   int* err;
 };
 
-template <int HD>
+template <int HD, int KT>
 struct AttnCfg {
-  static constexpr int KT = 64;                      // keys per smem tile
-  static constexpr int TILE_BYTES = KT * HD * 2;     // one of K or V
+  static constexpr int TILE_BYTES = KT * HD * 2;     // one of K, V, K lo, V lo
   static constexpr int STAGES = 2;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * TILE_BYTES + 32 * HD * 4 + 32 * 2 * 4 + 64;
+  static constexpr int PARTS = KT == 32 ? 2 : 1;     // 32-key tiles leave room for the low halves
+  static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * PARTS * TILE_BYTES + 32 * HD * 4 + 32 * 2 * 4 + 64;
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -60,6 +69,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// The bf16 residuals of a pair against its packed bf16 values hv.
+__device__ __forceinline__ uint32_t pack_lo(float a, float b, uint32_t hv) {
+  return pack_bf16(a - __uint_as_float(hv << 16), b - __uint_as_float(hv & 0xffff0000u));
+}
 
 // Store a pair of outputs as bf16 and, when o_lo is set, their bf16 residuals.
 __device__ __forceinline__ void store_pair(uint16_t* o, uint16_t* o_lo, long long idx, float a, float b) {
@@ -72,22 +85,23 @@ __device__ __forceinline__ void store_pair(uint16_t* o, uint16_t* o_lo, long lon
 }
 
 // Byte offset of the 16-byte chunk `ch` (8 bf16 along the head dim) of key row
-// `r` in a TMA 128B-swizzled tile stored as HD/64 boxes of [64 keys][128 B].
+// `r` in a TMA 128B-swizzled tile stored as HD/64 boxes of [KT keys][128 B].
+template <int KT>
 __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
-  return (uint32_t)((ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+  return (uint32_t)((ch >> 3) * (KT * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
 // One work item (key split, query tile, head, sequence) of block attention,
 // run by a group of 128 threads (tid 0..127, named barrier 2).  sK/sV hold ST
-// stages of [64 keys][HD] tiles (1024-byte aligned), xo at least 32*HD floats,
-// full[ST] mbarriers initialised to count 1.  tcount counts the tiles this
-// group has loaded through `full` so far (phase parity across items); it is
-// advanced by the item's tile count.
-template <int HD, int WQ, int ST>
+// stages of [KT keys][HD] tiles (1024-byte aligned), each stage followed by its
+// low-half tile when p.kv_lo is set; xo at least 32*HD floats, full[ST]
+// mbarriers initialised to count 1.  tcount counts the tiles this group has
+// loaded through `full` so far (phase parity across items); it is advanced by
+// the item's tile count.
+template <int HD, int WQ, int ST, int KT>
 __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
                                           int split, int qt, int head, int seq, uint8_t* sK, uint8_t* sV, float* xo,
                                           uint64_t* full, int* bcast, uint32_t& tcount, int tid) {
-  constexpr int KT = 64;
   constexpr int TILE_BYTES = KT * HD * 2;
   constexpr int WK = 4 / WQ;
   constexpr int QT = 16 * WQ;
@@ -104,15 +118,22 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
   const int k_end = min(p.T, k_beg + p.kps);
   const int ntiles = (k_end - k_beg + KT - 1) / KT;
   const int zk = p.z_k0 + seq * p.H + head, zv = p.z_v0 + seq * p.H + head;
+  const int zkl = p.z_kl0 + seq * p.H + head, zvl = p.z_vl0 + seq * p.H + head;
+  const bool lo = KT == 32 && p.kv_lo != 0;   // 64-key tiles are bf16 only (no room for the low halves)
+  const int stage_bytes = (lo ? 2 : 1) * TILE_BYTES;   // per stage of sK (and of sV): hi tile, then lo tile
 
   const uint64_t pol = policy_evict_first();
   auto issue = [&](int t, int s) {
     const int key0 = k_beg + t * KT;
-    mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES);
+    mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * stage_bytes));
 #pragma unroll
     for (int bx = 0; bx < HD / 64; ++bx) {
-      tma_load_3d(sK + s * TILE_BYTES + bx * 8192, tmK, &full[s], bx * 64, key0, zk, pol);
-      tma_load_3d(sV + s * TILE_BYTES + bx * 8192, tmV, &full[s], bx * 64, key0, zv, pol);
+      tma_load_3d(sK + s * stage_bytes + bx * (KT * 128), tmK, &full[s], bx * 64, key0, zk, pol);
+      tma_load_3d(sV + s * stage_bytes + bx * (KT * 128), tmV, &full[s], bx * 64, key0, zv, pol);
+      if (lo) {
+        tma_load_3d(sK + s * stage_bytes + TILE_BYTES + bx * (KT * 128), tmK, &full[s], bx * 64, key0, zkl, pol);
+        tma_load_3d(sV + s * stage_bytes + TILE_BYTES + bx * (KT * 128), tmV, &full[s], bx * 64, key0, zvl, pol);
+      }
     }
   };
   const uint32_t tc0 = tcount;
@@ -121,12 +142,13 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
 
   // Q fragments of this warp's 16 query rows
   const int qrow0 = qt * QT + wq * 16;
-  uint32_t qa[KS][4];
+  uint32_t qa[KS][4], ql[KS][4];
   {
     const long long base_lo = (((long long)seq * p.R + qrow0 + g) * p.H + head) * HD;
     const long long base_hi = base_lo + 8LL * p.H * HD;
     const bool lo_ok = qrow0 + g < p.R, hi_ok = qrow0 + g + 8 < p.R;
     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+    const uint32_t* ql32 = reinterpret_cast<const uint32_t*>(lo ? p.q_lo : p.q);
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
       const int c0 = kk * 16 + 2 * t4;
@@ -135,6 +157,10 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
       qa[kk][1] = hi_ok ? __ldcg(&q32[(base_hi + c0) >> 1]) : 0u;
       qa[kk][2] = lo_ok ? __ldcg(&q32[(base_lo + c0 + 8) >> 1]) : 0u;
       qa[kk][3] = hi_ok ? __ldcg(&q32[(base_hi + c0 + 8) >> 1]) : 0u;
+      ql[kk][0] = lo && lo_ok ? __ldcg(&ql32[(base_lo + c0) >> 1]) : 0u;
+      ql[kk][1] = lo && hi_ok ? __ldcg(&ql32[(base_hi + c0) >> 1]) : 0u;
+      ql[kk][2] = lo && lo_ok ? __ldcg(&ql32[(base_lo + c0 + 8) >> 1]) : 0u;
+      ql[kk][3] = lo && hi_ok ? __ldcg(&ql32[(base_hi + c0 + 8) >> 1]) : 0u;
     }
   }
 
@@ -150,8 +176,8 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
     if (!failed && !mbar_wait(&full[s], (tg / ST) & 1u, nullptr, p.err, ERR_ATTN_FULL))
       failed = true;
     if (!failed) {
-      const uint32_t kb = smem_u32(sK + s * TILE_BYTES);
-      const uint32_t vb = smem_u32(sV + s * TILE_BYTES);
+      const uint32_t kb = smem_u32(sK + s * stage_bytes);
+      const uint32_t vb = smem_u32(sV + s * stage_bytes);
       const int key_w = wk * KW;       // first key of this warp inside the tile
       // S = Q K^T
       float sacc[NT][4];
@@ -163,9 +189,16 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
         for (int kk = 0; kk < KS; kk += 2) {
           const int ch = 2 * kk + (lane >> 3);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb + swz_off(r, ch), b0, b1, b2, b3);
+          ldsm_x4(kb + swz_off<KT>(r, ch), b0, b1, b2, b3);
           mma16816(sacc[nt], qa[kk], b0, b1);
           mma16816(sacc[nt], qa[kk + 1], b2, b3);
+          if (lo) {
+            mma16816(sacc[nt], ql[kk], b0, b1);
+            mma16816(sacc[nt], ql[kk + 1], b2, b3);
+            ldsm_x4(kb + TILE_BYTES + swz_off<KT>(r, ch), b0, b1, b2, b3);
+            mma16816(sacc[nt], qa[kk], b0, b1);
+            mma16816(sacc[nt], qa[kk + 1], b2, b3);
+          }
         }
       }
       // online softmax (base 2)
@@ -219,20 +252,33 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
       // O += P V
 #pragma unroll
       for (int j = 0; j < KW / 16; ++j) {
-        uint32_t pa[4];
+        uint32_t pa[4], pl[4];
         pa[0] = pack_bf16(sacc[2 * j][0], sacc[2 * j][1]);
         pa[1] = pack_bf16(sacc[2 * j][2], sacc[2 * j][3]);
         pa[2] = pack_bf16(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
         pa[3] = pack_bf16(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
+        if (lo) {
+          pl[0] = pack_lo(sacc[2 * j][0], sacc[2 * j][1], pa[0]);
+          pl[1] = pack_lo(sacc[2 * j][2], sacc[2 * j][3], pa[1]);
+          pl[2] = pack_lo(sacc[2 * j + 1][0], sacc[2 * j + 1][1], pa[2]);
+          pl[3] = pack_lo(sacc[2 * j + 1][2], sacc[2 * j + 1][3], pa[3]);
+        }
         const int mi = lane >> 3;
         const int r = key_w + j * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
         for (int ot = 0; ot < OT; ot += 2) {
           const int ch = ot + (mi >> 1);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vb + swz_off(r, ch), b0, b1, b2, b3);
+          ldsm_x4_t(vb + swz_off<KT>(r, ch), b0, b1, b2, b3);
           mma16816(oacc[ot], pa, b0, b1);
           mma16816(oacc[ot + 1], pa, b2, b3);
+          if (lo) {
+            mma16816(oacc[ot], pl, b0, b1);
+            mma16816(oacc[ot + 1], pl, b2, b3);
+            ldsm_x4_t(vb + TILE_BYTES + swz_off<KT>(r, ch), b0, b1, b2, b3);
+            mma16816(oacc[ot], pa, b0, b1);
+            mma16816(oacc[ot + 1], pa, b2, b3);
+          }
         }
       }
     }
@@ -369,16 +415,17 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
   }
 }
 
-// Standalone launch: one work item per CTA.
-template <int HD, int WQ>
+// Standalone launch: one work item per CTA.  KT = 32 also takes the low
+// halves (kv_lo); KT = 64 is bf16 only.
+template <int HD, int WQ, int KT>
 __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUtensorMap tmK,
                                                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using C = AttnCfg<HD>;
+  using C = AttnCfg<HD, KT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
-  uint8_t* sV = smem + C::STAGES * C::TILE_BYTES;
-  float* xo = reinterpret_cast<float*>(sV + C::STAGES * C::TILE_BYTES);   // [32][HD] + [32][2]
+  uint8_t* sV = smem + C::STAGES * C::PARTS * C::TILE_BYTES;
+  float* xo = reinterpret_cast<float*>(sV + C::STAGES * C::PARTS * C::TILE_BYTES);   // [32][HD] + [32][2]
   uint64_t* full = reinterpret_cast<uint64_t*>(xo + 32 * HD + 64);
   int* bcast = reinterpret_cast<int*>(full + C::STAGES);
   if (threadIdx.x == 0) {
@@ -391,7 +438,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUten
   griddep_launch_dependents();
   griddep_wait();
   uint32_t tcount = 0;
-  attn_item<HD, WQ, C::STAGES>(&tmK, &tmV, p, blockIdx.x, blockIdx.y % p.q_tiles, blockIdx.y / p.q_tiles,
+  attn_item<HD, WQ, C::STAGES, KT>(&tmK, &tmV, p, blockIdx.x, blockIdx.y % p.q_tiles, blockIdx.y / p.q_tiles,
                                blockIdx.z, sK, sV, xo, full, bcast, tcount, threadIdx.x);
 }
 

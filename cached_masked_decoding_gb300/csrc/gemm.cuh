@@ -46,7 +46,8 @@ struct GemmParams {
   int R, row0;
   // GEMM_QKV
   uint16_t* q_out;        // [N][d]
-  uint16_t* kv;           // cache [L][2][b][H][T_pad][hd]
+  uint16_t* q_out_lo;     // low halves of q, or null (then K/V low halves are not written either)
+  uint16_t* kv;           // cache [L][K|V][hi|lo][b][H][T_pad][hd]
   const float2* rope_cs;  // [T_pad][hd/2] (cos, sin)
   int d_model, head_dim, n_heads, T_pad, b_seqs, layer;
   // GEMM_RESID
@@ -151,6 +152,7 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
     const int R = p.R, row0 = p.row0, T = p.T_pad, H = p.n_heads, layer = p.layer, b = p.b_seqs;
     const float2* __restrict__ rope = p.rope_cs;
     uint16_t* __restrict__ q_out = p.q_out;
+    uint16_t* __restrict__ q_lo = p.q_out_lo;
     uint16_t* __restrict__ kv = p.kv;
     const int sec = (m_idx * 128) / d;          // uniform over the tile: 0 q, 1 k, 2 v
     const int mr = m - sec * d;
@@ -185,11 +187,14 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
       const int r = r0 + c;
       if (r < N) {
         const uint16_t bits = f32_to_bf16_bits(v[c]);
+        const uint16_t lbits = f32_to_bf16_bits(v[c] - bf16_bits_to_f32(bits));
         if (sec == 0) {
           q_out[(long long)r * d + mr] = bits;
+          if (q_lo) q_lo[(long long)r * d + mr] = lbits;
         } else {
-          const long long plane = (((long long)layer * 2 + (sec - 1)) * b + seq) * H + head;
+          const long long plane = ((((long long)layer * 2 + (sec - 1)) * 2) * b + seq) * H + head;
           kv[(plane * T + row0 + i) * hd + j] = bits;
+          if (q_lo) kv[((plane + (long long)b * H) * T + row0 + i) * hd + j] = lbits;
         }
       }
       if (++i == R) {

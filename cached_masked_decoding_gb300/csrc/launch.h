@@ -54,8 +54,10 @@ inline cudaError_t launch_gemm(int kind, int bn, const CUtensorMap& a, const CUt
 cudaError_t launch_step_hd64(int bn, const StepArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_step_hd128(int bn, const StepArgs& a, int grid, cudaStream_t st);
 
-cudaError_t launch_attention(int hd, int wq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                             dim3 grid, cudaStream_t st, bool pdl);
+// kt: keys per shared-memory tile, 64 (bf16 K/V) or 32 (also with low halves,
+// p.kv_lo); the tensor maps' key box must match.
+cudaError_t launch_attention(int hd, int wq, int kt, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const AttnParams& p, dim3 grid, cudaStream_t st, bool pdl);
 
 }  // namespace dllm
 

@@ -55,18 +55,20 @@ struct StepCfg {
   static constexpr int A_BYTES = 128 * 64 * 2;           // one weight tile (128 rows x 64 k)
   static constexpr int B_BYTES = B_ROWS * 64 * 2;        // one activation tile (hi and lo rows)
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int ATT_TILE = 64 * HD * 2;
+  static constexpr int ATT_KT = 32;                      // keys per attention tile
+  static constexpr int ATT_TILE = ATT_KT * HD * 2;        // one of K, K lo, V, V lo
   static constexpr int XCH_BYTES = 128 * 33 * 4;         // epilogue exchange; also attention xo, merge arrays
   static constexpr int FIXED = 1024 + XCH_BYTES + 512 + 512 + 512;   // + row factors, params, barriers
   static constexpr int MAX_SMEM = 232448;
   static constexpr int ST_FIT = (MAX_SMEM - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = ST_FIT > 12 ? 12 : ST_FIT;
-  // attention K/V tiles borrow the activation half of the ring (idle in ATTN phases)
-  static constexpr int AST = (STAGES * B_BYTES) / (2 * ATT_TILE) >= 2 ? 2 : 1;
+  // attention K/V tiles (with their low halves) borrow the activation half of
+  // the ring, idle in ATTN phases
+  static constexpr int AST = (STAGES * B_BYTES) / (4 * ATT_TILE) >= 2 ? 2 : 1;
   static constexpr int TMEM_COLS = 2 * B_ROWS;
   static constexpr int SMEM_BYTES = FIXED + STAGES * STAGE_BYTES;
   static_assert(STAGES >= 4, "ring too shallow");
-  static_assert(AST * 2 * ATT_TILE <= STAGES * B_BYTES, "attention tiles fit the activation half of the ring");
+  static_assert(AST * 4 * ATT_TILE <= STAGES * B_BYTES, "attention tiles fit the activation half of the ring");
   static_assert(32 * HD * 4 + 64 * 4 <= XCH_BYTES, "attention scratch");
   static_assert(sizeof(GemmParams) <= 512, "phase parameter copy");
   static_assert(BN <= 128, "persistent step: at most 128 activation rows per tile");
@@ -367,18 +369,21 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
         embed_rows(a.emb, a.merge.n_rows, (int)cta, (int)G, l128);
       } else if (P.kind == PH_ATTN) {
         AttnParams ap = a.attn;
-        ap.z_k0 = (P.layer * 2 + 0) * ap.b * ap.H;
-        ap.z_v0 = (P.layer * 2 + 1) * ap.b * ap.H;
+        ap.z_k0 = ((P.layer * 2 + 0) * 2 + 0) * ap.b * ap.H;
+        ap.z_kl0 = ((P.layer * 2 + 0) * 2 + 1) * ap.b * ap.H;
+        ap.z_v0 = ((P.layer * 2 + 1) * 2 + 0) * ap.b * ap.H;
+        ap.z_vl0 = ((P.layer * 2 + 1) * 2 + 1) * ap.b * ap.H;
         const CUtensorMap* tkv = a.maps + a.attn_map;
         uint8_t* sK = sB;                                    // the activation half of the ring is idle now
-        uint8_t* sV = sB + C::AST * C::ATT_TILE;
+        uint8_t* sV = sB + C::AST * 2 * C::ATT_TILE;
         for (int item = (int)cta; item < a.attn_items; item += (int)G) {
           const int split = item % ap.splits;
           const int rest = item / ap.splits;
           const int qt = rest % ap.q_tiles;
           const int head = (rest / ap.q_tiles) % ap.H;
           const int sq = rest / (ap.q_tiles * ap.H);
-          attn_item<HD, 2, C::AST>(tkv, tkv, ap, split, qt, head, sq, sK, sV, xch, afull, abcast, att_tc, l128);
+          attn_item<HD, 2, C::AST, C::ATT_KT>(tkv, tkv, ap, split, qt, head, sq, sK, sV, xch, afull, abcast, att_tc,
+                                              l128);
           named_bar_sync(2, 128);
         }
       } else if (P.kind == PH_MERGE) {

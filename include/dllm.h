@@ -200,15 +200,19 @@ dllm_status dllm_read_state(const dllm_state* s, int32_t* tokens, float* conf, i
  * rows, host float32 [b][block][d_model]. */
 dllm_status dllm_read_hidden(const dllm_state* s, float* h);
 
-/* Copy the cached K and V of one layer as float32, host [b][n_heads][T][head_dim] each. */
+/* Copy the cached K and V of one layer as float32, host [b][n_heads][T][head_dim] each
+ * (hi + lo in split precision). */
 dllm_status dllm_read_kv(const dllm_state* s, int32_t layer, float* k, float* v);
 
 /* Precision of the activations fed to the tensor cores.  DLLM_PREC_SPLIT
  * (default) carries every GEMM input as a pair of bf16 arrays hi + lo with
  * lo = bf16(x - hi) (about 16 mantissa bits; the weights are read once, the
  * MMA is twice as wide).  DLLM_PREC_BF16 rounds activations to bf16 (half the
- * tensor work: for the compute-bound batch regime).  K/V cache, q and the
- * attention probabilities are bf16 in both modes; accumulation is float32. */
+ * tensor work: for the compute-bound batch regime).  In split precision the
+ * K/V cache, q and the attention probabilities are hi/lo pairs as well (the
+ * cache holds both halves: twice the K/V bytes); in bf16 precision they are
+ * bf16.  Accumulation is float32 in both.  Change the precision only before a
+ * refresh: the cache's low halves are written only in split precision. */
 typedef enum dllm_precision { DLLM_PREC_SPLIT = 0, DLLM_PREC_BF16 = 1 } dllm_precision;
 dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode);
 

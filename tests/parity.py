@@ -19,13 +19,12 @@ from oracle import sampler as OS
 
 TOL = 2e-3
 
-# Max-prob tolerance per model.  2e-3 is the stated bar (tiny at x8, 1B, 8B).
-# The tiny model at logit sigma 10 (lm_scale 31.25 on d = 256) is a variant
-# added to exercise the threshold path at tiny size; its bf16 K/V cache
-# (relative rounding ~2^-9) leaves relative hidden errors up to ~4e-3, i.e.
-# logit errors up to sigma * 4e-3 = 0.04 on each of two logits, and max-prob
-# errors up to max c(1-c) * 2 * 0.04 = 0.02: it is held to 2e-2.
-CONF_TOL = {"tiny_spread": 2e-2}
+# Max-prob tolerance per model: the stated 2e-3 for every model.  It holds
+# because the split-precision path keeps q, K, V and the attention
+# probabilities as hi/lo bf16 pairs; with the K/V cache in bf16 alone, final
+# hidden rows move by a few 1e-3 relative, which at logit sigma 10-12 moves
+# mid-range confidences by up to ~1e-2.
+CONF_TOL: dict = {}
 
 
 def conf_tol(cfg) -> float:
