@@ -29,6 +29,9 @@ KERNEL_CLASSES = ("embed", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "do
                   "refresh_gateup_gemm", "refresh_down_gemm", "persistent_step", "unused_15")
 
 
+TIMELINE_SLOTS = 10   # per (CTA, phase) entries of dllm_read_step_timeline
+
+
 class DllmError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"dllm status {status}: {msg}")
@@ -274,7 +277,7 @@ class State:
         c = ctypes.c_int32()
         ph = ctypes.c_int32()
         check(lib().dllm_read_step_timeline(self.h, None, 0, ctypes.byref(c), ctypes.byref(ph)))
-        out = np.zeros((c.value, ph.value, 6), dtype=np.uint64)
+        out = np.zeros((c.value, ph.value, TIMELINE_SLOTS), dtype=np.uint64)
         check(lib().dllm_read_step_timeline(self.h, _ptr(out), out.size, ctypes.byref(c), ctypes.byref(ph)))
         return out
 

@@ -529,7 +529,8 @@ struct dllm_state {
   int map_kv = 0;
   StepPhase* d_phases = nullptr;  // [n_blocks][n_phases]
   CUtensorMap* d_maps = nullptr;
-  unsigned int* d_bar = nullptr;
+  int* d_flags = nullptr;         // dataflow flags of the persistent step, zeroed per launch
+  int n_flags = 0;
   AttnPlan step_attn = {};
   int step_prefetch = 1 << 20;                // weight tiles loaded ahead of a phase barrier (ring depth cap)
   unsigned long long* d_timeline = nullptr;   // persistent-step phase timeline (diagnostics)
@@ -544,7 +545,7 @@ dllm_status state_free_device(dllm_state* s) {
   if (s->trace_buf) cudaFree(s->trace_buf);
   if (s->d_phases) cudaFree(s->d_phases);
   if (s->d_maps) cudaFree(s->d_maps);
-  if (s->d_bar) cudaFree(s->d_bar);
+  if (s->d_flags) cudaFree(s->d_flags);
   if (s->d_timeline) cudaFree(s->d_timeline);
   if (s->host_ce) cudaFreeHost(s->host_ce);
   for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
@@ -1213,13 +1214,110 @@ dllm_status build_step(dllm_state* s) {
     P[k] = StepPhase{};
     P[k++].kind = PH_MERGE;
   }
+  // Dataflow flags (one int block, zeroed per launch; the same layout for
+  // every block's phase list, whose order is embed, L x [QKV, ATTN, O, GU, D],
+  // LM, MERGE).  A GEMM phase owns m_tiles row-tile flags (each counts its
+  // finished n-tiles), a completion counter and m_tiles * n_tiles stream-K
+  // fix-up counters; an attention phase owns one flag per head (counting
+  // finished works) and a completion counter; the embedding one counter (one
+  // count per CTA).
+  const AttnPlan ap = plan_attention_persistent(s->b, c.n_heads, s->B, s->T, s->m->sms);
+  const int G = s->m->sms;
+  std::vector<int> cnt_of(n_phases, -1), unit_of(n_phases, -1), done_of(n_phases, -1);
+  int n_flags = 0;
+  for (int k = 0; k < n_phases; ++k) {
+    const StepPhase& q = ph[k];
+    if (q.kind == PH_EMBED) {
+      done_of[k] = n_flags++;
+    } else if (q.kind == PH_ATTN) {
+      unit_of[k] = n_flags;
+      n_flags += c.n_heads;
+      done_of[k] = n_flags++;
+    } else if (q.kind == PH_GEMM) {
+      if (q.g.total * (G + 1) >= (1LL << 31)) {   // the kernel's stream-K arithmetic is 32-bit
+        set_error("persistent step: %lld chunks in one phase is too many", (long long)q.g.total);
+        return DLLM_EINVAL;
+      }
+      unit_of[k] = n_flags;
+      n_flags += q.g.m_tiles;
+      done_of[k] = n_flags++;
+      cnt_of[k] = n_flags;
+      n_flags += q.g.m_tiles * q.g.n_tiles;
+    }
+  }
+  if (s->n_flags < n_flags) {
+    if (s->d_flags) cudaFree(s->d_flags);
+    s->d_flags = nullptr;
+    s->n_flags = 0;
+    CKS(dev_alloc((void**)&s->d_flags, (size_t)n_flags * 4));
+    s->n_flags = n_flags;
+  }
+  for (int j = 0; j < s->n_blocks; ++j) {
+    StepPhase* P = &ph[(size_t)j * n_phases];
+    int gemm_ord = 0;
+    for (int k = 0; k < n_phases; ++k) {
+      StepPhase& q = P[k];
+      q.unit0 = unit_of[k];
+      q.done = done_of[k];
+      q.rs_done = -1;
+      q.rs_need = 0;
+      q.dep0 = 0;
+      q.dep_shift = 31;
+      q.dep_need = 0;
+      q.dep_attn = 0;
+      q.qkv0 = 0;
+      q.qkv_need = 0;
+      q.src_done = 0;
+      q.src_need = 0;
+      if (q.kind == PH_MERGE) {           // every LM-head tile
+        const StepPhase& lm = P[k - 1];
+        q.rs_done = done_of[k - 1];
+        q.rs_need = lm.g.m_tiles * lm.g.n_tiles;
+        continue;
+      }
+      if (q.kind == PH_ATTN) {            // q, k, v row tiles of the QKV phase before
+        q.qkv0 = unit_of[k - 1];
+        q.qkv_need = P[k - 1].g.n_tiles;
+        continue;
+      }
+      if (q.kind != PH_GEMM) continue;
+      GemmParams& g = q.g;
+      g.counters = s->d_flags + cnt_of[k];
+      g.ws = s->gemm_ws + (size_t)(gemm_ord++ & 1) * G * 2 * BN * 128;
+      const StepPhase& prev = P[k - 1];
+      q.src_done = done_of[k - 1];
+      q.src_need = prev.kind == PH_EMBED  ? G
+                   : prev.kind == PH_ATTN ? s->b * ap.q_tiles * c.n_heads   // attention works (seq, head, query tile)
+                                          : prev.g.m_tiles * prev.g.n_tiles;
+      if (prev.kind == PH_EMBED) {        // QKV of layer 0: every CTA's embedding rows
+        q.dep0 = done_of[k - 1];
+        q.dep_shift = 31;                 // every chunk: unit 0, the embedding counter
+        q.dep_need = G;
+        q.rs_done = done_of[k - 1];
+        q.rs_need = G;
+      } else if (prev.kind == PH_ATTN) {  // O: this layer's attention heads
+        q.dep0 = unit_of[k - 1];
+        q.dep_shift = c.head_dim == 128 ? 1 : 0;   // a head spans head_dim columns
+        q.dep_need = s->b * ap.q_tiles;
+        q.dep_attn = 1;
+        q.layer = prev.layer;
+      } else {                            // QKV (l > 0), GU, D, LM: the GEMM before
+        q.dep0 = unit_of[k - 1];
+        q.dep_shift = prev.gemm_kind == GEMM_SWIGLU ? 0 : 1;   // a SwiGLU tile writes 64 columns, others 128
+        q.dep_need = prev.g.n_tiles;
+        if (g.ss_in) {                    // row factors from every tile of the RESID phase before
+          q.rs_done = done_of[k - 1];
+          q.rs_need = prev.g.m_tiles * prev.g.n_tiles;
+        }
+      }
+    }
+  }
   if (s->d_phases) cudaFree(s->d_phases);
   if (s->d_maps) cudaFree(s->d_maps);
   s->d_phases = nullptr;
   s->d_maps = nullptr;
   CKS(dev_alloc((void**)&s->d_phases, ph.size() * sizeof(StepPhase)));
   CKS(dev_alloc((void**)&s->d_maps, maps.size() * sizeof(CUtensorMap)));
-  if (!s->d_bar) CKS(dev_alloc((void**)&s->d_bar, 256));
   CK(cudaMemcpy(s->d_phases, ph.data(), ph.size() * sizeof(StepPhase), cudaMemcpyHostToDevice));
   CK(cudaMemcpy(s->d_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
   s->n_phases = n_phases;
@@ -1249,7 +1347,7 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
   a.phases = s->d_phases + (size_t)j * s->n_phases;
   a.n_phases = s->n_phases;
   a.maps = s->d_maps;
-  a.bar = s->d_bar;
+  a.flags = s->d_flags;
   a.err = s->count_err + s->b;
   a.emb = EmbedParams{s->x, m->embed, m->layers[0].attn_norm, s->h, s->xn, s->split ? s->xn_lo : nullptr, s->ss,
                       d, s->B, blk, s->T};
@@ -1292,10 +1390,12 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
   a.merge.rule = rule;
   a.prefetch = s->step_prefetch;
   if (s->timeline) {
-    if (!s->d_timeline) CKS(dev_alloc((void**)&s->d_timeline, (size_t)s->m->sms * s->n_phases * 6 * 8));
+    const size_t tl_bytes = (size_t)s->m->sms * s->n_phases * kTimelineSlots * 8;
+    if (!s->d_timeline) CKS(dev_alloc((void**)&s->d_timeline, tl_bytes));
+    CK(cudaMemsetAsync(s->d_timeline, 0, tl_bytes, s->st));
     a.timeline = s->d_timeline;
   }
-  CK(cudaMemsetAsync(s->d_bar, 0, 4, s->st));
+  CK(cudaMemsetAsync(s->d_flags, 0, (size_t)s->n_flags * 4, s->st));
   const double bytes = (double)s->m->cfg.n_layers * 2.0 *
                            (4.0 * d * d + 3.0 * (double)d * c.d_ffn) +
                        2.0 * V * d + (double)s->b * s->T * d * 2 * 2 * c.n_layers * (s->split ? 2 : 1);
@@ -1615,7 +1715,7 @@ extern "C" dllm_status dllm_read_step_timeline(const dllm_state* s, uint64_t* ou
     set_error("no persistent-step timeline was recorded");
     return DLLM_ESTATE;
   }
-  const size_t n = (size_t)s->m->sms * s->n_phases * 6;
+  const size_t n = (size_t)s->m->sms * s->n_phases * kTimelineSlots;
   if (ctas) *ctas = s->m->sms;
   if (phases) *phases = s->n_phases;
   if (!out) return DLLM_OK;

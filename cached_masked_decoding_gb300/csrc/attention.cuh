@@ -97,9 +97,11 @@ __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
 // low-half tile when p.kv_lo is set; xo at least 32*HD floats, full[ST]
 // mbarriers initialised to count 1.  tcount counts the tiles this group has
 // loaded through `full` so far (phase parity across items); it is advanced by
-// the item's tile count.
+// the item's tile count.  Returns true when this call wrote the final output
+// rows of its (sequence, head, query tile): the only split, or the last split
+// to finish, which merges all of them.
 template <int HD, int WQ, int ST, int KT>
-__device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
+__device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
                                           int split, int qt, int head, int seq, uint8_t* sK, uint8_t* sV, float* xo,
                                           uint64_t* full, int* bcast, uint32_t& tcount, int tid) {
   constexpr int TILE_BYTES = KT * HD * 2;
@@ -346,7 +348,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
                      oacc[i][3] * ih);
       }
     }
-    return;
+    return true;
   }
 
   const long long work = ((long long)seq * p.H + head) * p.q_tiles + qt;
@@ -376,7 +378,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
     *bcast = last;
   }
   named_bar_sync(2, 128);
-  if (!*bcast) return;
+  if (!*bcast) return false;
   // combine the splits: per row, weights exp2(m_s - M) / L computed once, then
   // every output element is an independent weighted sum over the splits
   const float* base_o = p.ws_o + work * p.splits * QT * HD;
@@ -413,6 +415,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap* tmK, const CUtensor
     store_pair(p.o, p.o_lo, oi, acc.x, acc.y);
     store_pair(p.o, p.o_lo, oi + 2, acc.z, acc.w);
   }
+  return true;
 }
 
 // Standalone launch: one work item per CTA.  KT = 32 also takes the low

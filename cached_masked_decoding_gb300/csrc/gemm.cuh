@@ -124,6 +124,27 @@ __device__ __forceinline__ void warp_transpose_argmax(float (&v)[32], int (&id)[
   }
 }
 
+// Row stride (floats) of the [32 rows][128 features] staging of an epilogue
+// tile in the exchange buffer: 16-byte aligned rows, 128 * 33 floats in all.
+constexpr int kStageLd = 132;
+
+// Eight consecutive floats as bf16 pairs: hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+  const float4 a = *reinterpret_cast<const float4*>(x);
+  const float4 b = *reinterpret_cast<const float4*>(x + 4);
+  const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint16_t b0 = f32_to_bf16_bits(f[2 * t]), b1 = f32_to_bf16_bits(f[2 * t + 1]);
+    h[t] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+    l[t] = (uint32_t)f32_to_bf16_bits(f[2 * t] - bf16_bits_to_f32(b0)) |
+           ((uint32_t)f32_to_bf16_bits(f[2 * t + 1] - bf16_bits_to_f32(b1)) << 16);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 // Epilogue of 32 consecutive activation rows (columns of the accumulator) for
 // the thread's weight row m = m_idx*128 + l128.  v holds raw sums.  Every
 // epilogue thread of the CTA calls this with the same (m_idx, r0).
@@ -151,16 +172,13 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
     const int d = p.d_model, hd = p.head_dim, half = hd >> 1;
     const int R = p.R, row0 = p.row0, T = p.T_pad, H = p.n_heads, layer = p.layer, b = p.b_seqs;
     const float2* __restrict__ rope = p.rope_cs;
-    uint16_t* __restrict__ q_out = p.q_out;
-    uint16_t* __restrict__ q_lo = p.q_out_lo;
-    uint16_t* __restrict__ kv = p.kv;
     const int sec = (m_idx * 128) / d;          // uniform over the tile: 0 q, 1 k, 2 v
     const int mr = m - sec * d;
-    const int head = mr / hd, j = mr - head * hd;
+    const int j = mr % hd;
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] *= rs[c];
-    const int seq0 = r0 / R, i0 = r0 - seq0 * R;   // rows r0.. walk (seq, i) without dividing
     if (sec < 2) {
+      const int seq0 = r0 / R, i0 = r0 - seq0 * R;   // rows r0.. walk (seq, i) without dividing
       const int jj = j & (half - 1);
       float2 cs[32];
       int i = i0;
@@ -181,84 +199,102 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
 #pragma unroll
       for (int c = 0; c < 32; ++c) v[c] = v[c] * cs[c].x + sgn * pv[c] * cs[c].y;
     }
-    int seq = seq0, i = i0;
+    // Store through shared memory: the tile is staged as [32 rows][128
+    // features] and written 8 features (16 bytes) per thread and store, not
+    // one 2-byte element per thread and row.
+    named_bar_sync(1, 128);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int r = r0 + c;
-      if (r < N) {
-        const uint16_t bits = f32_to_bf16_bits(v[c]);
-        const uint16_t lbits = f32_to_bf16_bits(v[c] - bf16_bits_to_f32(bits));
-        if (sec == 0) {
-          q_out[(long long)r * d + mr] = bits;
-          if (q_lo) q_lo[(long long)r * d + mr] = lbits;
-        } else {
-          const long long plane = ((((long long)layer * 2 + (sec - 1)) * 2) * b + seq) * H + head;
-          kv[(plane * T + row0 + i) * hd + j] = bits;
-          if (q_lo) kv[((plane + (long long)b * H) * T + row0 + i) * hd + j] = lbits;
-        }
-      }
-      if (++i == R) {
-        i = 0;
-        ++seq;
+    for (int c = 0; c < 32; ++c) xch[c * kStageLd + l128] = v[c];
+    named_bar_sync(1, 128);
+    uint16_t* __restrict__ q_out = p.q_out;
+    uint16_t* __restrict__ q_lo = p.q_out_lo;
+    uint16_t* __restrict__ kv = p.kv;
+    const int f0 = m_idx * 128 - sec * d;       // the tile's first feature within its section
+#pragma unroll
+    for (int e = l128; e < 32 * 16; e += 128) {
+      const int row = e >> 4, f8 = (e & 15) * 8;
+      const int r = r0 + row;
+      if (r >= N) continue;
+      uint4 hi, lo;
+      split8(xch + row * kStageLd + f8, hi, lo);
+      const int fm = f0 + f8;
+      if (sec == 0) {
+        *reinterpret_cast<uint4*>(&q_out[(long long)r * d + fm]) = hi;
+        if (q_lo) *reinterpret_cast<uint4*>(&q_lo[(long long)r * d + fm]) = lo;
+      } else {
+        const int seq = r / R, i = r - seq * R;
+        const int head = fm / hd, jj = fm - head * hd;
+        const long long plane = ((((long long)layer * 2 + (sec - 1)) * 2) * b + seq) * H + head;
+        *reinterpret_cast<uint4*>(&kv[(plane * T + row0 + i) * hd + jj]) = hi;
+        if (q_lo) *reinterpret_cast<uint4*>(&kv[((plane + (long long)b * H) * T + row0 + i) * hd + jj]) = lo;
       }
     }
   } else if constexpr (KIND == GEMM_RESID) {
+    // Staged through shared memory as [32 rows][128 features]: warp q then
+    // handles rows q, q+4, ..., lane handles features 4*lane .. 4*lane+3, so
+    // every global access is a 16-byte (h) or 8-byte (bf16) vector and the
+    // row's sum of squares is one warp reduction.
     const int d = p.d_model, R = p.R, row0 = p.row0, blk0 = p.blk_start, blen = p.blk_len;
     const bool remap = p.remap != 0;
     float* __restrict__ h = p.h;
     uint16_t* __restrict__ xo = p.xn_out;
     uint16_t* __restrict__ xl = p.xn_out_lo;
     float* __restrict__ sso = p.ss_out;
-    const float g = bf16_bits_to_f32(__ldg(&p.g_next[m]));
-    float hv[32];
+    const int fb = m_idx * 128 + lane * 4;
+    const uint2 graw = __ldg(reinterpret_cast<const uint2*>(p.g_next + fb));
+    float hv[8][4];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int r = r0 + c;
-      hv[c] = r < N ? __ldcg(&h[(long long)r * d + m]) : 0.0f;
+    for (int k = 0; k < 8; ++k) {
+      const int r = r0 + q + 4 * k;
+      const float4 x = r < N ? __ldcg(reinterpret_cast<const float4*>(&h[(long long)r * d + fb]))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      hv[k][0] = x.x;
+      hv[k][1] = x.y;
+      hv[k][2] = x.z;
+      hv[k][3] = x.w;
     }
-    float sq[32];
-    int seq = r0 / R, i = r0 - (r0 / R) * R;      // rows r0.. walk (seq, i) without dividing
+    named_bar_sync(1, 128);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int r = r0 + c;
-      hv[c] += v[c];
+    for (int c = 0; c < 32; ++c) xch[c * kStageLd + l128] = v[c];
+    named_bar_sync(1, 128);
+    const float g4[4] = {__uint_as_float(graw.x << 16), __uint_as_float(graw.x & 0xffff0000u),
+                         __uint_as_float(graw.y << 16), __uint_as_float(graw.y & 0xffff0000u)};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int row = q + 4 * k;
+      const int r = r0 + row;
+      const float4 add = *reinterpret_cast<const float4*>(xch + row * kStageLd + lane * 4);
+      hv[k][0] += add.x;
+      hv[k][1] += add.y;
+      hv[k][2] += add.z;
+      hv[k][3] += add.w;
       int ro = r;
       if (remap) {
-        const int bi = row0 + i - blk0;
+        const int seq = r / R, pos = row0 + r % R;
+        const int bi = pos - blk0;
         ro = (bi >= 0 && bi < blen) ? seq * blen + bi : -1;
       }
-      if (++i == R) {
-        i = 0;
-        ++seq;
-      }
-      sq[c] = 0.0f;
+      float sq = 0.0f;
       if (r < N) {
-        h[(long long)r * d + m] = hv[c];
+        *reinterpret_cast<float4*>(&h[(long long)r * d + fb]) = make_float4(hv[k][0], hv[k][1], hv[k][2], hv[k][3]);
         if (ro >= 0) {
-          const float xv = hv[c] * g;
-          const uint16_t hb = f32_to_bf16_bits(xv);
-          xo[(long long)ro * d + m] = hb;
-          if (xl) xl[(long long)ro * d + m] = f32_to_bf16_bits(xv - bf16_bits_to_f32(hb));
-          sq[c] = hv[c] * hv[c];
+          uint32_t hb[2], lb[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const float x0 = hv[k][2 * t] * g4[2 * t], x1 = hv[k][2 * t + 1] * g4[2 * t + 1];
+            const uint16_t b0 = f32_to_bf16_bits(x0), b1 = f32_to_bf16_bits(x1);
+            hb[t] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+            lb[t] = (uint32_t)f32_to_bf16_bits(x0 - bf16_bits_to_f32(b0)) |
+                    ((uint32_t)f32_to_bf16_bits(x1 - bf16_bits_to_f32(b1)) << 16);
+          }
+          *reinterpret_cast<uint2*>(&xo[(long long)ro * d + fb]) = make_uint2(hb[0], hb[1]);
+          if (xl) *reinterpret_cast<uint2*>(&xl[(long long)ro * d + fb]) = make_uint2(lb[0], lb[1]);
+          sq = (hv[k][0] * hv[k][0] + hv[k][1] * hv[k][1]) + (hv[k][2] * hv[k][2] + hv[k][3] * hv[k][3]);
         }
       }
-    }
-    warp_transpose_sum(sq, lane);
-    named_bar_sync(1, 128);
-    red[q * 32 + lane] = sq[0];
-    named_bar_sync(1, 128);
-    if (l128 < 32) {
-      const int r = r0 + l128;
-      if (r < N) {
-        int ro = r;
-        if (remap) {
-          const int seq = r / R, pos = row0 + r % R;
-          const int bi = pos - blk0;
-          ro = (bi >= 0 && bi < blen) ? seq * blen + bi : -1;
-        }
-        if (ro >= 0)
-          sso[(long long)ro * (d >> 7) + m_idx] = ((red[l128] + red[32 + l128]) + red[64 + l128]) + red[96 + l128];
-      }
+#pragma unroll
+      for (int s = 16; s >= 1; s >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, s);
+      if (lane == 0 && r < N && ro >= 0) sso[(long long)ro * (d >> 7) + m_idx] = sq;
     }
   } else if constexpr (KIND == GEMM_SWIGLU) {
     uint16_t* __restrict__ act = p.act;
@@ -270,21 +306,31 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
 #pragma unroll
     for (int c = 0; c < 32; ++c) xch[l128 * 33 + c] = v[c];
     named_bar_sync(1, 128);
+    float a[32];
     if (l128 < 64) {
-      const int f = m_idx * 64 + l128;
-      float up[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) up[c] = xch[(l128 + 64) * 33 + c];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const int r = r0 + c;
-        if (r >= N) continue;
-        const float gt = v[c];
-        const float a = gt / (1.0f + __expf(-gt)) * up[c];
-        const uint16_t hb = f32_to_bf16_bits(a);
-        act[(long long)r * ld + f] = hb;
-        if (act_lo) act_lo[(long long)r * ld + f] = f32_to_bf16_bits(a - bf16_bits_to_f32(hb));
+        const float gt = v[c], up = xch[(l128 + 64) * 33 + c];
+        a[c] = gt / (1.0f + __expf(-gt)) * up;
       }
+    }
+    // staged as [32 rows][64 features], stored 8 features per thread and store
+    named_bar_sync(1, 128);
+    if (l128 < 64) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) xch[c * kStageLd + l128] = a[c];
+    }
+    named_bar_sync(1, 128);
+#pragma unroll
+    for (int e = l128; e < 32 * 8; e += 128) {
+      const int row = e >> 3, f8 = (e & 7) * 8;
+      const int r = r0 + row;
+      if (r >= N) continue;
+      uint4 hi, lo;
+      split8(xch + row * kStageLd + f8, hi, lo);
+      const long long o = (long long)r * ld + m_idx * 64 + f8;
+      *reinterpret_cast<uint4*>(&act[o]) = hi;
+      if (act_lo) *reinterpret_cast<uint4*>(&act_lo[o]) = lo;
     }
   } else if constexpr (KIND == GEMM_LMHEAD) {
     const int M = p.M;

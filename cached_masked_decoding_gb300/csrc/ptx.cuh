@@ -22,6 +22,8 @@ enum ErrSite : int {
   ERR_GEMM_DRAIN = 105,
   ERR_ATTN_FULL = 201,
   ERR_GRID_BARRIER = 301,
+  ERR_STEP_FLAG = 302,
+  ERR_STEP_LOCAL = 303,
   ERR_PROBE = 901,
 };
 

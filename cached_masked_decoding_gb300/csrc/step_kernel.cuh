@@ -1,8 +1,10 @@
 // Persistent DualCache denoise step: one cooperative launch, one CTA per SM,
 // runs every phase of a step - embedding, per layer [QKV+RoPE+K/V write,
 // block attention, O-proj+residual+norm, gate/up+SwiGLU, down+residual+norm],
-// LM head + softmax statistics, statistic merge + select/commit - separated by
-// grid barriers (a global arrival counter, waits bounded in time).
+// LM head + softmax statistics, statistic merge + select/commit - ordered by
+// dataflow flags instead of grid barriers: every finished unit of a phase (a
+// GEMM row tile, an attention head) raises a counter, and a consumer waits
+// only for the units it reads (waits bounded in time).
 //
 // Why: a DualCache step streams ~15 GB of weights through 160 GEMM phases of
 // 5-30 us each.  As separate launches every phase pays a pipeline fill (the
@@ -10,7 +12,18 @@
 // the TMA producer walks straight from one GEMM phase into the next: it keeps
 // loading the next phase's weight tiles into the shared-memory ring (weights
 // depend on nothing) while the other CTAs finish the current phase's
-// epilogues, and only the activation tiles wait for the barrier.
+// epilogues, and each activation tile waits only for the row tile or head
+// that writes its 64 columns - so a phase starts on the columns that are
+// ready while the previous phase's last tiles are still being reduced.
+//
+// Ordering.  A unit's finisher writes its outputs, passes a barrier of the
+// four epilogue warps, and one thread raises the unit's flag with a release
+// (after a proxy fence, as the readers are TMA loads); readers acquire it.
+// Buffers reused across phases stay safe without barriers because every
+// GEMM reads all of its input columns: a unit of phase p+2 can only start
+// after all of phase p+1's units finished, hence after all of phase p's
+// readers.  The stream-K partial workspace alternates between two halves by
+// GEMM phase for the same reason.
 //
 // Roles per CTA (192 threads): warp 0 TMA producer, warp 1 tcgen05.mma issuer,
 // warps 2-5 "workers": GEMM epilogues, and the embedding, attention and merge
@@ -26,11 +39,33 @@ namespace dllm {
 
 enum PhaseKind : int { PH_EMBED = 0, PH_GEMM = 1, PH_ATTN = 2, PH_MERGE = 3 };
 
+// Diagnostic timeline slots per (CTA, phase), %globaltimer ns:
+// 0 workers finished the phase, 1 producer issued the phase's first
+// activation tile (phase 0: kernel start), 2 MMA issuer finished the phase,
+// 3 producer issued the phase's last tile, 4 workers started the phase,
+// 5 workers got the phase's first accumulator, 6 workers were through their
+// first segment, 7 workers started their last fix-up as the last
+// contributor, 8 it had summed the partials, 9 workers published their last
+// unit of the phase.
+constexpr int kTimelineSlots = 10;
+
 struct StepPhase {
   int kind;
   int gemm_kind;
   int map_a, map_b, map_blo;   // indices into StepArgs::maps
   int layer;                   // attention: cache layer
+  // dataflow (indices into StepArgs::flags)
+  int unit0;     // first flag of this phase's units: GEMM row tiles (count n-tiles) or attention heads (count works)
+  int done;      // counter of this phase's finished units (GEMM tiles, attention works, CTAs for the embedding)
+  int dep0;      // first flag of the units that write this phase's activation columns
+  int dep_shift; // activation k-chunk (64 columns) k is written by unit k >> dep_shift
+  int dep_need;  // value such a unit's flag reaches when it is complete
+  int dep_attn;  // 1: the activations are the attention output of this layer (attention uses the ring's B half)
+  int rs_done;   // counter that must reach rs_need before the row factors / the merge may read (-1: none)
+  int rs_need;
+  int src_done, src_need;   // completion counter of the phase producing the activations, and its final value
+  int qkv0;      // attention: first row-tile flag of this layer's QKV phase
+  int qkv_need;  // value a QKV row-tile flag reaches when complete
   GemmParams g;
 };
 
@@ -38,14 +73,14 @@ struct StepArgs {
   const StepPhase* phases;
   int n_phases;
   const CUtensorMap* maps;     // global memory, 64-byte aligned, written before the launch
-  unsigned int* bar;           // grid arrival counter, zero at launch
+  int* flags;                  // dataflow flags and counters, zero at launch
   int* err;
   EmbedParams emb;
   AttnParams attn;             // z_k0 / z_v0 set per phase from its layer
   int attn_map;                // the K/V cache map
   int attn_items;              // b * H * q_tiles * splits
   MergeParams merge;
-  unsigned long long* timeline;  // optional [grid][n_phases][6] (diagnostics), or null
+  unsigned long long* timeline;  // optional [grid][n_phases][kTimelineSlots] (diagnostics), or null
   int prefetch;                  // weight tiles loaded ahead of a phase's barrier (<= ring depth)
 };
 
@@ -74,31 +109,70 @@ struct StepCfg {
   static_assert(BN <= 128, "persistent step: at most 128 activation rows per tile");
 };
 
-// ---------------------------------------------------------------- grid barrier
-// Called by one thread after a CTA barrier over the workers.
-__device__ __forceinline__ void grid_arrive(unsigned int* bar) {
-  asm volatile("fence.proxy.async.global;" ::: "memory");   // our generic writes before others' TMA reads
-  red_add_release_gpu(bar, 1u);
+// ---------------------------------------------------------------- dataflow flags
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// Wait until `target` arrivals are counted; bounded by kWaitLimitNs.
-__device__ __forceinline__ bool grid_wait(const unsigned int* bar, unsigned int target, volatile int* abort,
-                                          int* err) {
-  const unsigned long long t0 = globaltimer();
-  for (;;) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
-    if (v >= target) break;
-    if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      record_error(err, ERR_GRID_BARRIER);
-      return false;
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until *f >= need (acquire), then order later TMA reads after it.
+// Bounded by kWaitLimitNs; gives up early once this CTA raised *abort or any
+// CTA recorded an error.
+__device__ __forceinline__ bool flag_wait(const int* f, int need, volatile int* abort, int* err) {
+  if (ld_acquire_gpu(f) < need) {
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+      __nanosleep(32);
+      if (ld_acquire_gpu(f) >= need) break;
+      if (*abort || ld_relaxed_gpu(err) != 0) {
+        *abort = 1;
+        return false;
+      }
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        record_error(err, ERR_STEP_FLAG);
+        return false;
+      }
     }
-    __nanosleep(256);   // ~300 pollers on one word: keep its L2 slice free for real traffic
   }
-  asm volatile("fence.proxy.async.global;" ::: "memory");   // later TMA reads see what the barrier published
+  asm volatile("fence.proxy.async.global;" ::: "memory");
   return true;
+}
+
+// Wait until *f0 >= need0 and *f1 >= need1 (f1 may be null).  The first
+// look reads both with relaxed loads issued together (one round trip) and
+// turns them into an acquire with a fence; only a flag not yet raised is
+// then polled.
+__device__ __forceinline__ bool flags_wait2(const int* f0, int need0, const int* f1, int need1,
+                                            volatile int* abort, int* err) {
+  const int v0 = ld_relaxed_gpu(f0);
+  const int v1 = f1 ? ld_relaxed_gpu(f1) : need1;
+  if (v0 >= need0 && v1 >= need1) {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+  }
+  if (v0 < need0 && !flag_wait(f0, need0, abort, err)) return false;
+  if (f1 && v1 < need1 && !flag_wait(f1, need1, abort, err)) return false;
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");   // also covers the flag seen by the relaxed load
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+// Raise two counters by one with release semantics.  Called by one thread
+// after a barrier over the threads whose writes it publishes; the proxy fence
+// makes those writes visible to other CTAs' TMA reads.
+__device__ __forceinline__ void flag_publish(int* a, int* b) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a) : "memory");
+  if (b) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(b) : "memory");
 }
 
 // ---------------------------------------------------------------- worker phases
@@ -182,6 +256,51 @@ __device__ __forceinline__ void merge_row(const MergeParams& p, int row, int tid
   named_bar_sync(1, 128);
 }
 
+// ---------------------------------------------------------------- chunk positions
+// Stream-K bookkeeping in 32-bit integers (a phase has at most a few 1e5
+// chunks, times the grid stays below 2^31) and without divisions in the
+// per-chunk loops: 64-bit integer division is a long software sequence,
+// and several of them per chunk would cap the TMA issue rate.
+__device__ __forceinline__ uint32_t sk_begin(uint32_t cta, uint32_t G, uint32_t total) { return cta * total / G; }
+
+// The CTA whose stream-K range holds chunk i.
+__device__ __forceinline__ uint32_t sk_owner32(uint32_t i, uint32_t G, uint32_t total) {
+  return ((i + 1) * G + total - 1) / total - 1;
+}
+
+// (k-chunk, n-tile, m-tile) of a chunk; chunks run k fastest, then n-tiles,
+// then m-tiles.
+struct ChunkPos {
+  int k, n, m;
+  __device__ __forceinline__ void init(uint32_t g, int kc, int n_tiles) {
+    const uint32_t tile = g / (uint32_t)kc;
+    k = (int)(g - tile * (uint32_t)kc);
+    m = (int)(tile / (uint32_t)n_tiles);
+    n = (int)(tile - (uint32_t)m * (uint32_t)n_tiles);
+  }
+  __device__ __forceinline__ void next(int kc, int n_tiles) {
+    if (++k == kc) {
+      k = 0;
+      if (++n == n_tiles) {
+        n = 0;
+        ++m;
+      }
+    }
+  }
+};
+
+// Slot and phase parity of a position in the shared-memory ring.
+struct RingPos {
+  int s;
+  uint32_t par;
+  __device__ __forceinline__ void next(int stages) {
+    if (++s == stages) {
+      s = 0;
+      par ^= 1u;
+    }
+  }
+};
+
 // ---------------------------------------------------------------- the kernel
 template <int BN, int HD>
 __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
@@ -204,10 +323,11 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bcast = reinterpret_cast<int*>(tmem_slot + 2);
   int* abcast = reinterpret_cast<int*>(tmem_slot + 3);
+  volatile int* att_done = reinterpret_cast<volatile int*>(tmem_slot + 4);   // layers whose attention items this CTA finished
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x, cta = blockIdx.x;
-  unsigned long long* tl = a.timeline ? a.timeline + cta * a.n_phases * 6 : nullptr;
+  unsigned long long* tl = a.timeline ? a.timeline + cta * a.n_phases * kTimelineSlots : nullptr;
   if (tl && threadIdx.x == 0) tl[1] = globaltimer();
 
   if (threadIdx.x == 0) {
@@ -221,6 +341,7 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
     }
     for (int s = 0; s < C::AST; ++s) mbar_init(&afull[s], 1);
     *abort_flag = 0;
+    *att_done = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -238,90 +359,134 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
       // Walks this CTA's chunks of every GEMM phase in order through one ring.
       // At a phase's start it first loads the weight tiles of up to STAGES
       // chunks (they depend on nothing: the ring slots free up as the MMA
-      // finishes the previous phase), then waits until every CTA finished the
-      // previous phase and loads the matching activation tiles.
+      // finishes the previous phase), then loads each chunk's activation tile
+      // once the unit writing those 64 columns has finished.
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      long long ring = 0;   // chunks issued so far, over all phases
+      RingPos rw{0, 0u};   // ring position of the next weight load, over all phases
       for (int ph = 0; ph < a.n_phases && !*abort_flag; ++ph) {
         const StepPhase& P = a.phases[ph];
         if (P.kind != PH_GEMM) continue;
-        const long long total = P.g.total;
+        const uint32_t total = (uint32_t)P.g.total;
         const int kc = P.g.kc, n_tiles = P.g.n_tiles;
         const bool split = BN <= 128 && P.g.split != 0;
         const uint32_t tx = (uint32_t)(C::A_BYTES + (split ? 2 : 1) * BN * 128);
         const CUtensorMap* tA = a.maps + P.map_a;
         const CUtensorMap* tB = a.maps + P.map_b;
         const CUtensorMap* tBl = a.maps + P.map_blo;
-        const long long start = cta * total / G, end = (cta + 1) * total / G;
-        const long long n = end - start;
-        const long long depth = a.prefetch < STAGES ? a.prefetch : STAGES;
-        const long long pre = n < depth ? n : depth;
+        const int* dep = a.flags + P.dep0;
+        const int dep_shift = P.dep_shift, dep_need = P.dep_need;
+        const uint32_t start = sk_begin((uint32_t)cta, (uint32_t)G, total);
+        const int n = (int)(sk_begin((uint32_t)cta + 1, (uint32_t)G, total) - start);
+        const int depth = a.prefetch < STAGES ? a.prefetch : STAGES;
+        const int pre = n < depth ? n : depth;
+        ChunkPos cw;
+        cw.init(start, kc, n_tiles);
+        const ChunkPos c_first = cw;
+        const RingPos r_first = rw;
         bool ok = true;
-        for (long long i = 0; i < pre && ok; ++i) {
-          const long long c = ring + i;
-          const int s = (int)(c % STAGES);
-          if (!mbar_wait(&empty[s], (uint32_t)(((c / STAGES) & 1) ^ 1), abort_flag, a.err, ERR_GEMM_EMPTY)) {
+        for (int i = 0; i < pre; ++i) {
+          if (!mbar_wait(&empty[rw.s], rw.par ^ 1u, abort_flag, a.err, ERR_GEMM_EMPTY)) {
             ok = false;
             break;
           }
-          const long long gch = start + i;
-          const long long tile = gch / kc;
-          mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_2d(sA + s * C::A_BYTES, tA, &full[s], (int)(gch - tile * kc) * 64, (int)(tile / n_tiles) * 128,
-                      pol_w);
+          mbar_arrive_expect_tx(&full[rw.s], tx);
+          tma_load_2d(sA + rw.s * C::A_BYTES, tA, &full[rw.s], cw.k * 64, cw.m * 128, pol_w);
+          cw.next(kc, n_tiles);
+          rw.next(STAGES);
         }
         if (!ok) break;
-        if (!grid_wait(a.bar, (unsigned int)(G * ph), abort_flag, a.err)) break;
-        if (tl) tl[ph * 6 + 1] = globaltimer();
-        for (long long i = 0; i < pre; ++i) {
-          const long long c = ring + i;
-          const int s = (int)(c % STAGES);
-          const long long gch = start + i;
-          const long long tile = gch / kc;
-          const int k = (int)(gch - tile * kc), n_idx = (int)(tile % n_tiles);
-          tma_load_2d(sB + s * C::B_BYTES, tB, &full[s], k * 64, n_idx * BN, pol_x);
-          if (split) tma_load_2d(sB + s * C::B_BYTES + BN * 128, tBl, &full[s], k * 64, n_idx * BN, pol_x);
+        if (P.dep_attn) {
+          // the activation half of the ring holds this CTA's attention tiles
+          // until its workers are through this layer's attention items
+          const unsigned long long t0 = globaltimer();
+          while (*att_done < P.layer + 1) {
+            if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
+              if (!*abort_flag) record_error(a.err, ERR_STEP_LOCAL);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (!ok) break;
         }
-        for (long long i = pre; i < n; ++i) {
-          const long long c = ring + i;
-          const int s = (int)(c % STAGES);
-          if (!mbar_wait(&empty[s], (uint32_t)(((c / STAGES) & 1) ^ 1), abort_flag, a.err, ERR_GEMM_EMPTY)) {
+        // activation columns [64k, 64k+64) come from unit k >> dep_shift; the
+        // last unit found complete is remembered within a run of chunks, and
+        // once the whole producing phase is seen complete nothing is polled
+        int ready_unit = -1;
+        bool all_ready = false;
+        const int* src_done = a.flags + P.src_done;
+        const int src_need = P.src_need;
+        auto dep_ready = [&](int k) -> bool {
+          if (all_ready) return true;
+          const int unit = k >> dep_shift;
+          if (unit == ready_unit) return true;
+          const int vd = ld_relaxed_gpu(src_done);
+          const int vu = ld_relaxed_gpu(dep + unit);
+          if (vd >= src_need) {
+            all_ready = true;
+          } else if (vu < dep_need) {
+            if (!flag_wait(dep + unit, dep_need, abort_flag, a.err)) return false;
+            ready_unit = unit;
+            return true;
+          }
+          ready_unit = unit;
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          return true;
+        };
+        ChunkPos cx = c_first;
+        RingPos rx = r_first;
+        for (int i = 0; i < pre; ++i) {
+          if (!dep_ready(cx.k)) {
             ok = false;
             break;
           }
-          const long long gch = start + i;
-          const long long tile = gch / kc;
-          const int k = (int)(gch - tile * kc), n_idx = (int)(tile % n_tiles), m_idx = (int)(tile / n_tiles);
-          mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_2d(sA + s * C::A_BYTES, tA, &full[s], k * 64, m_idx * 128, pol_w);
-          tma_load_2d(sB + s * C::B_BYTES, tB, &full[s], k * 64, n_idx * BN, pol_x);
-          if (split) tma_load_2d(sB + s * C::B_BYTES + BN * 128, tBl, &full[s], k * 64, n_idx * BN, pol_x);
+          if (tl && i == 0) tl[ph * kTimelineSlots + 1] = globaltimer();
+          tma_load_2d(sB + rx.s * C::B_BYTES, tB, &full[rx.s], cx.k * 64, cx.n * BN, pol_x);
+          if (split) tma_load_2d(sB + rx.s * C::B_BYTES + BN * 128, tBl, &full[rx.s], cx.k * 64, cx.n * BN, pol_x);
+          cx.next(kc, n_tiles);
+          rx.next(STAGES);
+        }
+        for (int i = pre; i < n && ok; ++i) {
+          if (!mbar_wait(&empty[rw.s], rw.par ^ 1u, abort_flag, a.err, ERR_GEMM_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[rw.s], tx);
+          tma_load_2d(sA + rw.s * C::A_BYTES, tA, &full[rw.s], cw.k * 64, cw.m * 128, pol_w);
+          if (!dep_ready(cw.k)) {
+            ok = false;
+            break;
+          }
+          tma_load_2d(sB + rw.s * C::B_BYTES, tB, &full[rw.s], cw.k * 64, cw.n * BN, pol_x);
+          if (split) tma_load_2d(sB + rw.s * C::B_BYTES + BN * 128, tBl, &full[rw.s], cw.k * 64, cw.n * BN, pol_x);
+          cw.next(kc, n_tiles);
+          rw.next(STAGES);
         }
         if (!ok) break;
-        if (tl) tl[ph * 6 + 3] = globaltimer();
-        ring += n;
+        if (tl) tl[ph * kTimelineSlots + 3] = globaltimer();
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      long long ring = 0;
+      RingPos rm{0, 0u};
       int seg = 0;
       bool ok = true;
       for (int ph = 0; ph < a.n_phases && ok; ++ph) {
         const StepPhase& P = a.phases[ph];
         if (P.kind != PH_GEMM) continue;
-        const long long total = P.g.total;
-        const int kc = P.g.kc;
+        const uint32_t total = (uint32_t)P.g.total;
+        const uint32_t kc = (uint32_t)P.g.kc;
         const bool split = BN <= 128 && P.g.split != 0;
         const uint32_t idesc = idesc_bf16_f32(128, split ? 2 * BN : BN);
-        const long long start = cta * total / G, end = (cta + 1) * total / G;
-        long long g = start;
+        uint32_t g = sk_begin((uint32_t)cta, (uint32_t)G, total);
+        const uint32_t end = sk_begin((uint32_t)cta + 1, (uint32_t)G, total);
+        uint32_t k = g % kc;
         while (g < end) {
-          const long long tile = g / kc;
-          const long long seg_first = g;
-          const long long seg_end = ((tile + 1) * kc < end) ? (tile + 1) * kc : end;
+          const uint32_t len = (kc - k < end - g) ? kc - k : end - g;   // this segment: the rest of a tile
           const int buf = seg & 1;
           const uint32_t use = (uint32_t)(seg >> 1);
           if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, a.err, ERR_GEMM_TEMPTY)) {
@@ -330,26 +495,27 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
           }
           tc_fence_after();
           const uint32_t d = tmem + (uint32_t)(buf * C::B_ROWS);
-          for (; g < seg_end; ++g, ++ring) {
-            const int s = (int)(ring % STAGES);
-            if (!mbar_wait(&full[s], (uint32_t)((ring / STAGES) & 1), abort_flag, a.err, ERR_GEMM_FULL)) {
+          for (uint32_t i = 0; i < len; ++i) {
+            if (!mbar_wait(&full[rm.s], rm.par, abort_flag, a.err, ERR_GEMM_FULL)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
-            const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
+            const uint32_t a0 = smem_u32(sA + rm.s * C::A_BYTES);
+            const uint32_t b0 = smem_u32(sB + rm.s * C::B_BYTES);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
-                          (g > seg_first || kk > 0) ? 1u : 0u);
-            mma_commit(&empty[s]);
+              mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&empty[rm.s]);
+            rm.next(STAGES);
           }
           if (!ok) break;
           mma_commit(&tfull[buf]);
           ++seg;
+          g += len;
+          k = 0;
         }
-        if (tl) tl[ph * 6 + 2] = globaltimer();
+        if (tl) tl[ph * kTimelineSlots + 2] = globaltimer();
       }
     }
   } else {
@@ -359,14 +525,16 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
     int seg = 0;
     uint32_t att_tc = 0;
     for (int ph = 0; ph < a.n_phases; ++ph) {
-      if (ph > 0) {
-        if (l128 == 0) grid_wait(a.bar, (unsigned int)(G * ph), abort_flag, a.err);
-        if (named_bar_or(1, 128, *abort_flag != 0)) break;
-      }
-      if (tl && l128 == 0) tl[ph * 6 + 4] = globaltimer();
       const StepPhase& P = a.phases[ph];
+      if (tl && l128 == 0) tl[ph * kTimelineSlots + 4] = globaltimer();
+      // a phase that reads row statistics (or, for the merge, every LM-head
+      // tile) waits until all units of the phase producing them finished
+      if (P.rs_done >= 0 && l128 == 0) flag_wait(a.flags + P.rs_done, P.rs_need, abort_flag, a.err);
+      if (named_bar_or(1, 128, *abort_flag != 0)) break;
       if (P.kind == PH_EMBED) {
         embed_rows(a.emb, a.merge.n_rows, (int)cta, (int)G, l128);
+        named_bar_sync(1, 128);
+        if (l128 == 0) flag_publish(a.flags + P.done, nullptr);
       } else if (P.kind == PH_ATTN) {
         AttnParams ap = a.attn;
         ap.z_k0 = ((P.layer * 2 + 0) * 2 + 0) * ap.b * ap.H;
@@ -376,16 +544,31 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
         const CUtensorMap* tkv = a.maps + a.attn_map;
         uint8_t* sK = sB;                                    // the activation half of the ring is idle now
         uint8_t* sV = sB + C::AST * 2 * C::ATT_TILE;
+        bool stop = false;
         for (int item = (int)cta; item < a.attn_items; item += (int)G) {
           const int split = item % ap.splits;
           const int rest = item / ap.splits;
           const int qt = rest % ap.q_tiles;
           const int head = (rest / ap.q_tiles) % ap.H;
           const int sq = rest / (ap.q_tiles * ap.H);
-          attn_item<HD, 2, C::AST, C::ATT_KT>(tkv, tkv, ap, split, qt, head, sq, sK, sV, xch, afull, abcast, att_tc,
-                                              l128);
+          if (l128 == 0) {
+            // q, k and v of this head: the QKV row tiles holding its columns
+            const int d = ap.H * HD, c0 = head * HD;
+            if (flags_wait2(a.flags + P.qkv0 + c0 / 128, P.qkv_need, a.flags + P.qkv0 + (d + c0) / 128, P.qkv_need,
+                            abort_flag, a.err))
+              flags_wait2(a.flags + P.qkv0 + (2 * d + c0) / 128, P.qkv_need, nullptr, 0, abort_flag, a.err);
+          }
+          if (named_bar_or(1, 128, *abort_flag != 0)) {
+            stop = true;
+            break;
+          }
+          const bool fin = attn_item<HD, 2, C::AST, C::ATT_KT>(tkv, tkv, ap, split, qt, head, sq, sK, sV, xch, afull,
+                                                               abcast, att_tc, l128);
           named_bar_sync(2, 128);
+          if (fin && l128 == 0) flag_publish(a.flags + P.unit0 + head, a.flags + P.done);
         }
+        if (stop) break;
+        if (l128 == 0) *att_done = P.layer + 1;
       } else if (P.kind == PH_MERGE) {
         for (int row = (int)cta; row < a.merge.n_rows; row += (int)G)
           merge_row(a.merge, row, l128, reinterpret_cast<uint8_t*>(xch), bcast);
@@ -396,20 +579,23 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
           reinterpret_cast<int*>(ps)[w] = reinterpret_cast<const int*>(&P.g)[w];
         named_bar_sync(1, 128);
         const GemmParams& p = *ps;
-        const long long total = p.total;
+        const uint32_t total = (uint32_t)p.total, uG = (uint32_t)G;
         const int kc = p.kc, n_tiles = p.n_tiles;
         const bool split = BN <= 128 && p.split != 0;
-        const long long start = cta * total / G, end = (cta + 1) * total / G;
-        long long g = start;
+        const uint32_t start = sk_begin((uint32_t)cta, uG, total), end = sk_begin((uint32_t)cta + 1, uG, total);
+        uint32_t g = start;
+        ChunkPos cp;
+        cp.init(start, kc, n_tiles);
         bool stop = false;
         int rs_tile = -1;
         while (g < end && !stop) {
-          const long long tile = g / kc;
-          const long long seg_first = g;
-          const long long seg_end = ((tile + 1) * kc < end) ? (tile + 1) * kc : end;
-          const bool full_tile = (seg_first == tile * kc) && (seg_end == (tile + 1) * kc);
-          const int m_idx = (int)(tile / n_tiles);
-          const int n_idx = (int)(tile % n_tiles);
+          const uint32_t len = ((uint32_t)(kc - cp.k) < end - g) ? (uint32_t)(kc - cp.k) : end - g;
+          const uint32_t seg_end = g + len;
+          const uint32_t t0 = g - (uint32_t)cp.k;            // first chunk of this tile
+          const bool full_tile = (cp.k == 0) && (len == (uint32_t)kc);
+          const int m_idx = cp.m;
+          const int n_idx = cp.n;
+          const int tile = m_idx * n_tiles + n_idx;
           const int buf = seg & 1;
           const uint32_t use = (uint32_t)(seg >> 1);
           if (n_idx != rs_tile) {
@@ -445,7 +631,7 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
             stop = true;
             break;
           }
-          if (tl && l128 == 0 && g == start) tl[ph * 6 + 5] = globaltimer();
+          if (tl && l128 == 0 && g == start) tl[ph * kTimelineSlots + 5] = globaltimer();
           tc_fence_after();
           const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::B_ROWS);
           if (full_tile) {
@@ -466,8 +652,14 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
                 default: epi_chunk<GEMM_LMHEAD>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
               }
             }
+            named_bar_sync(1, 128);
+            if (l128 == 0) flag_publish(a.flags + P.unit0 + m_idx, a.flags + P.done);
+            if (tl && l128 == 0) {
+              if (g == start) tl[ph * kTimelineSlots + 6] = globaltimer();
+              tl[ph * kTimelineSlots + 9] = globaltimer();
+            }
           } else {
-            const int slot = (seg_first == start) ? 0 : 1;
+            const int slot = (g == start) ? 0 : 1;
             float* wsp = p.ws + ((cta * 2 + slot) * (long long)BN) * 128;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -481,18 +673,26 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
             named_bar_sync(1, 128);
-            const long long t0 = tile * kc, t1 = (tile + 1) * kc - 1;
-            const long long c_first = sk_owner(t0, G, total), c_last = sk_owner(t1, G, total);
+            const uint32_t t1 = t0 + (uint32_t)kc - 1;
+            const uint32_t c_first = sk_owner32(t0, uG, total), c_last = sk_owner32(t1, uG, total);
             if (l128 == 0) {
-              // contributors: the CTAs in [c_first, c_last] whose chunk range is not
-          // empty (with fewer chunks than CTAs some ranges are)
-          int contributors = 0;
-          for (long long ctr = c_first; ctr <= c_last; ++ctr)
-            contributors += (ctr * total / G) < ((ctr + 1) * total / G) ? 1 : 0;
+              // contributors: the CTAs in [c_first, c_last] whose chunk range is
+              // not empty (with fewer chunks than CTAs some ranges are)
+              int contributors = 0;
+              uint32_t st = sk_begin(c_first, uG, total);
+              for (uint32_t ctr = c_first; ctr <= c_last; ++ctr) {
+                const uint32_t en = sk_begin(ctr + 1, uG, total);
+                contributors += st < en ? 1 : 0;
+                st = en;
+              }
               const int old = atomic_add_acq_rel_gpu(&p.counters[tile], 1);
               const int last = (old == contributors - 1);
               if (last) p.counters[tile] = 0;
               *bcast = last;
+              if (tl) {
+                if (g == start) tl[ph * kTimelineSlots + 6] = globaltimer();
+                if (last) tl[ph * kTimelineSlots + 7] = globaltimer();
+              }
             }
             named_bar_sync(1, 128);
             if (*bcast) {
@@ -501,15 +701,40 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                for (long long ctr = c_first; ctr <= c_last; ++ctr) {
-                  const long long st = ctr * total / G;
-                  if (st == (ctr + 1) * total / G) continue;   // empty range: no partial
-                  const long long sstart = st > t0 ? st : t0;
-                  const int sl = (sstart == st) ? 0 : 1;
-                  const float* src = p.ws + ((ctr * 2 + sl) * (long long)BN) * 128;
+                // partials in contributor order, two at a time so that both
+                // sets of loads are in flight together: ((v + p0) + p1) + ...
+                uint32_t ctr = c_first;
+                uint32_t st = sk_begin(c_first, uG, total);
+                while (ctr <= c_last) {
+                  const float* src0 = nullptr;
+                  const float* src1 = nullptr;
+                  int ns = 0;
+                  for (; ctr <= c_last && ns < 2; ++ctr) {
+                    const uint32_t en = sk_begin(ctr + 1, uG, total);
+                    const uint32_t cst = st;
+                    st = en;
+                    if (cst == en) continue;                     // empty range: no partial
+                    const int sl = (cst >= t0) ? 0 : 1;          // its first segment starts in this tile?
+                    const float* sp = p.ws + (((long long)ctr * 2 + sl) * BN) * 128 + (long long)c0 * 128 + l128;
+                    if (ns == 0) src0 = sp;
+                    else src1 = sp;
+                    ++ns;
+                  }
+                  if (ns == 2) {
+                    float x0[32], x1[32];
 #pragma unroll
-                  for (int j = 0; j < 32; ++j) v[j] += __ldcg(&src[(long long)(c0 + j) * 128 + l128]);
+                    for (int j = 0; j < 32; ++j) {
+                      x0[j] = __ldcg(src0 + j * 128);
+                      x1[j] = __ldcg(src1 + j * 128);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = (v[j] + x0[j]) + x1[j];
+                  } else if (ns == 1) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] += __ldcg(src0 + j * 128);
+                  }
                 }
+                if (tl && l128 == 0 && c0 == 0) tl[ph * kTimelineSlots + 8] = globaltimer();
                 switch (P.gemm_kind) {
                   case GEMM_QKV: epi_chunk<GEMM_QKV>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
                   case GEMM_RESID: epi_chunk<GEMM_RESID>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
@@ -517,19 +742,22 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
                   default: epi_chunk<GEMM_LMHEAD>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
                 }
               }
+              named_bar_sync(1, 128);
+              if (l128 == 0) flag_publish(a.flags + P.unit0 + m_idx, a.flags + P.done);
+              if (tl && l128 == 0) tl[ph * kTimelineSlots + 9] = globaltimer();
             }
           }
           g = seg_end;
+          cp.k = 0;                                            // the next segment starts a tile
+          if (++cp.n == n_tiles) {
+            cp.n = 0;
+            ++cp.m;
+          }
           ++seg;
         }
         if (stop) break;
       }
-      // publish this CTA's part of the phase
-      named_bar_sync(1, 128);
-      if (l128 == 0) {
-        if (tl) tl[ph * 6] = globaltimer();
-        grid_arrive(a.bar);
-      }
+      if (tl && l128 == 0) tl[ph * kTimelineSlots] = globaltimer();
     }
   }
   tc_fence_before();

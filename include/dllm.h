@@ -226,12 +226,16 @@ dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode);
 dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable);
 
 /* Diagnostics of the persistent step: with enable 1 the next persistent steps
- * record, per CTA and phase, {time the CTA's workers finished the phase, time
- * its TMA producer passed the barrier into the phase, time its MMA issuer
- * finished the phase, time the producer issued the phase's last weight tile,
- * time the workers started the phase, time the workers got the phase's first
- * accumulator} in %globaltimer nanoseconds (uint64 [ctas][phases][6]; entry
- * [cta][0][1] is the kernel start).  dllm_read_step_timeline copies the last step's record. */
+ * record, per CTA and phase, 10 %globaltimer nanosecond stamps (uint64
+ * [ctas][phases][10]): 0 the CTA's workers finished the phase, 1 its TMA
+ * producer issued the phase's first activation tile (entry [cta][0][1] is the
+ * kernel start), 2 its MMA issuer finished the phase, 3 the producer issued
+ * the phase's last tile, 4 the workers started the phase, 5 they got its
+ * first accumulator, 6 they were through their first segment, 7 they started
+ * their last stream-K fix-up as the last contributor, 8 they had summed its
+ * partials, 9 they published their last unit (row tile) of the phase; 0 where
+ * an event did not occur.  dllm_read_step_timeline copies the last step's
+ * record. */
 dllm_status dllm_state_set_step_timeline(dllm_state* s, int32_t enable);
 dllm_status dllm_read_step_timeline(const dllm_state* s, uint64_t* out, int64_t capacity, int32_t* ctas,
                                     int32_t* phases);
