@@ -97,13 +97,15 @@ __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
 // low-half tile when p.kv_lo is set; xo at least 32*HD floats, full[ST]
 // mbarriers initialised to count 1.  tcount counts the tiles this group has
 // loaded through `full` so far (phase parity across items); it is advanced by
-// the item's tile count.  Returns true when this call wrote the final output
+// the item's tile count.  stamps (optional, thread 0): [0] keys done, [1]
+// split partial stored and counted.  Returns true when this call wrote the final output
 // rows of its (sequence, head, query tile): the only split, or the last split
 // to finish, which merges all of them.
 template <int HD, int WQ, int ST, int KT>
 __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
                                           int split, int qt, int head, int seq, uint8_t* sK, uint8_t* sV, float* xo,
-                                          uint64_t* full, int* bcast, uint32_t& tcount, int tid) {
+                                          uint64_t* full, int* bcast, uint32_t& tcount, int tid,
+                                          unsigned long long* stamps = nullptr) {
   constexpr int TILE_BYTES = KT * HD * 2;
   constexpr int WK = 4 / WQ;
   constexpr int QT = 16 * WQ;
@@ -181,27 +183,35 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
       const uint32_t kb = smem_u32(sK + s * stage_bytes);
       const uint32_t vb = smem_u32(sV + s * stage_bytes);
       const int key_w = wk * KW;       // first key of this warp inside the tile
-      // S = Q K^T
+      // S = Q K^T.  Six independent accumulators per n8 tile (the hi*hi,
+      // lo*hi and hi*lo products, each split over even and odd k16 steps)
+      // keep the dependent MMA chains short; they are summed in a fixed order.
       float sacc[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+        float acc[6][4];
+#pragma unroll
+        for (int u = 0; u < 6; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.0f;
         const int r = key_w + nt * 8 + (lane & 7);
 #pragma unroll
         for (int kk = 0; kk < KS; kk += 2) {
           const int ch = 2 * kk + (lane >> 3);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + swz_off<KT>(r, ch), b0, b1, b2, b3);
-          mma16816(sacc[nt], qa[kk], b0, b1);
-          mma16816(sacc[nt], qa[kk + 1], b2, b3);
+          mma16816(acc[0], qa[kk], b0, b1);
+          mma16816(acc[1], qa[kk + 1], b2, b3);
           if (lo) {
-            mma16816(sacc[nt], ql[kk], b0, b1);
-            mma16816(sacc[nt], ql[kk + 1], b2, b3);
+            mma16816(acc[2], ql[kk], b0, b1);
+            mma16816(acc[3], ql[kk + 1], b2, b3);
             ldsm_x4(kb + TILE_BYTES + swz_off<KT>(r, ch), b0, b1, b2, b3);
-            mma16816(sacc[nt], qa[kk], b0, b1);
-            mma16816(sacc[nt], qa[kk + 1], b2, b3);
+            mma16816(acc[4], qa[kk], b0, b1);
+            mma16816(acc[5], qa[kk + 1], b2, b3);
           }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sacc[nt][e] = lo ? ((acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e])) + (acc[4][e] + acc[5][e])
+                           : acc[0][e] + acc[1][e];
       }
       // online softmax (base 2)
       const int key_base = k_beg + t * KT + key_w;
@@ -288,6 +298,7 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
     if (tid == 0 && !failed && t + ST < ntiles) issue(t + ST, s);
   }
   tcount = tc0 + ntiles;
+  if (stamps && tid == 0) stamps[0] = globaltimer();   // keys done
 
   // combine the key groups of a CTA (WK == 2): group 1 hands its state to group 0
   if constexpr (WK == 2) {
@@ -376,6 +387,7 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
     const int last = (old == p.splits - 1);
     if (last) p.counters[work] = 0;
     *bcast = last;
+    if (stamps) stamps[1] = globaltimer();               // partial stored and counted
   }
   named_bar_sync(2, 128);
   if (!*bcast) return false;
@@ -384,36 +396,86 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
   const float* base_o = p.ws_o + work * p.splits * QT * HD;
   const float* base_ml = p.ws_ml + work * p.splits * QT * 2;
   float* wn = xo;   // [QT][splits] normalised split weights (the key-group buffer is free now)
+  const int S = p.splits;
+  // The partials were written by other CTAs: every load is an L2 round trip,
+  // so they are issued in unrolled, predicated batches rather than one
+  // dependent load per split.
   for (int rl = tid; rl < QT; rl += 128) {
     float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(&base_ml[(s * QT + rl) * 2]));
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float mv[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mv[t] = s0 + t < S ? __ldcg(&base_ml[((s0 + t) * QT + rl) * 2]) : -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) M = fmaxf(M, mv[t]);
+    }
     const float u = (M == -INFINITY) ? 0.0f : M;
     float L = 0.0f;
-    for (int s = 0; s < p.splits; ++s) {
-      const float a = exp2f(__ldcg(&base_ml[(s * QT + rl) * 2]) - u);
-      wn[rl * p.splits + s] = a;
-      L += __ldcg(&base_ml[(s * QT + rl) * 2 + 1]) * a;
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float2 ml[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        ml[t] = s0 + t < S ? __ldcg(reinterpret_cast<const float2*>(&base_ml[((s0 + t) * QT + rl) * 2]))
+                           : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (s0 + t < S) {
+          const float a = exp2f(ml[t].x - u);
+          wn[rl * S + s0 + t] = a;
+          L += ml[t].y * a;
+        }
+      }
     }
     const float il = L > 0.0f ? 1.0f / L : 0.0f;
-    for (int s = 0; s < p.splits; ++s) wn[rl * p.splits + s] *= il;
+    for (int s = 0; s < S; ++s) wn[rl * S + s] *= il;
   }
   named_bar_sync(2, 128);
-  for (int e4 = tid; e4 < QT * HD / 4; e4 += 128) {
-    const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
-    const int row = qt * QT + rl;
-    if (row >= p.R) continue;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < p.splits; ++s) {
-      const float w = wn[rl * p.splits + s];
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(&base_o[(s * QT + rl) * HD + col]));
-      acc.x += v.x * w;
-      acc.y += v.y * w;
-      acc.z += v.z * w;
-      acc.w += v.w * w;
+  // four output vectors per thread and pass, four splits per batch: sixteen
+  // loads in flight; the sum over splits keeps split order
+  for (int e0 = tid; e0 < QT * HD / 4; e0 += 4 * 128) {
+    float4 acc[4];
+#pragma unroll
+    for (int u4 = 0; u4 < 4; ++u4) acc[u4] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 4) {
+      float4 v[4][4];
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const int e4 = e0 + u4 * 128;
+        const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          v[u4][t] = (e4 < QT * HD / 4 && s0 + t < S)
+                         ? __ldcg(reinterpret_cast<const float4*>(&base_o[((s0 + t) * QT + rl) * HD + col]))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const int e4 = e0 + u4 * 128;
+        const int rl = (e4 * 4) / HD;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (e4 < QT * HD / 4 && s0 + t < S) {
+            const float w = wn[rl * S + s0 + t];
+            acc[u4].x += v[u4][t].x * w;
+            acc[u4].y += v[u4][t].y * w;
+            acc[u4].z += v[u4][t].z * w;
+            acc[u4].w += v[u4][t].w * w;
+          }
+        }
+      }
     }
-    const long long oi = ((long long)seq * p.R + row) * p.H * HD + head * HD + col;
-    store_pair(p.o, p.o_lo, oi, acc.x, acc.y);
-    store_pair(p.o, p.o_lo, oi + 2, acc.z, acc.w);
+#pragma unroll
+    for (int u4 = 0; u4 < 4; ++u4) {
+      const int e4 = e0 + u4 * 128;
+      if (e4 >= QT * HD / 4) continue;
+      const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
+      const int row = qt * QT + rl;
+      if (row >= p.R) continue;
+      const float4 a4 = acc[u4];
+      const long long oi = ((long long)seq * p.R + row) * p.H * HD + head * HD + col;
+      store_pair(p.o, p.o_lo, oi, a4.x, a4.y);
+      store_pair(p.o, p.o_lo, oi + 2, a4.z, a4.w);
+    }
   }
   return true;
 }

@@ -46,7 +46,9 @@ enum PhaseKind : int { PH_EMBED = 0, PH_GEMM = 1, PH_ATTN = 2, PH_MERGE = 3 };
 // 5 workers got the phase's first accumulator, 6 workers were through their
 // first segment, 7 workers started their last fix-up as the last
 // contributor, 8 it had summed the partials, 9 workers published their last
-// unit of the phase.
+// unit of the phase.  Attention phases: 5 first item's inputs ready, 6 first
+// item done, 7 its keys done, 8 its split partial stored and counted, 9 last
+// head published by this CTA.
 constexpr int kTimelineSlots = 10;
 
 struct StepPhase {
@@ -562,10 +564,17 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
             stop = true;
             break;
           }
+          const bool first = item == (int)cta;
+          if (tl && l128 == 0 && first) tl[ph * kTimelineSlots + 5] = globaltimer();
           const bool fin = attn_item<HD, 2, C::AST, C::ATT_KT>(tkv, tkv, ap, split, qt, head, sq, sK, sV, xch, afull,
-                                                               abcast, att_tc, l128);
+                                                               abcast, att_tc, l128,
+                                                               tl && first ? tl + ph * kTimelineSlots + 7 : nullptr);
           named_bar_sync(2, 128);
           if (fin && l128 == 0) flag_publish(a.flags + P.unit0 + head, a.flags + P.done);
+          if (tl && l128 == 0) {
+            if (first) tl[ph * kTimelineSlots + 6] = globaltimer();
+            if (fin) tl[ph * kTimelineSlots + 9] = globaltimer();
+          }
         }
         if (stop) break;
         if (l128 == 0) *att_done = P.layer + 1;

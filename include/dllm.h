@@ -233,8 +233,10 @@ dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable);
  * the phase's last tile, 4 the workers started the phase, 5 they got its
  * first accumulator, 6 they were through their first segment, 7 they started
  * their last stream-K fix-up as the last contributor, 8 they had summed its
- * partials, 9 they published their last unit (row tile) of the phase; 0 where
- * an event did not occur.  dllm_read_step_timeline copies the last step's
+ * partials, 9 they published their last unit (row tile) of the phase; for
+ * attention phases 5-9 are: first item's inputs ready, first item done, its
+ * keys done, its split partial stored and counted, last head published; 0
+ * where an event did not occur.  dllm_read_step_timeline copies the last step's
  * record. */
 dllm_status dllm_state_set_step_timeline(dllm_state* s, int32_t enable);
 dllm_status dllm_read_step_timeline(const dllm_state* s, uint64_t* out, int64_t capacity, int32_t* ctas,
