@@ -890,6 +890,10 @@ dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int
   }
   gemm_shape(s, p, M, K, N, BN);
   const int grid = (int)std::min<long long>(s->m->sms, p.total);
+  if (p.total * (grid + 1) >= (1LL << 31)) {   // the kernel's stream-K arithmetic is 32-bit
+    set_error("GEMM of %lld chunks is too large", (long long)p.total);
+    return DLLM_EINVAL;
+  }
   if (s->timing) s->kt_bytes[cls] += bytes;
   Timed t(s, cls, bytes);
   CK(launch_gemm(kind, BN, tmA, *tmB, *tmBlo, p, grid, s->st, true));
@@ -1887,6 +1891,10 @@ extern "C" dllm_status dllm_op_gemm_trace(const uint16_t* W, const uint16_t* X, 
   tbl = tb;
   if (X_lo) CKS(map_2d(&tbl, X_lo, K, N, BN));
   const int grid = (int)std::min<long long>(device_sms(), p.total);
+  if (p.total * (grid + 1) >= (1LL << 31)) {   // the kernel's stream-K arithmetic is 32-bit
+    set_error("GEMM of %lld chunks is too large", (long long)p.total);
+    return DLLM_EINVAL;
+  }
   if (grid_out) *grid_out = grid;
   CK(launch_gemm(GEMM_PLAIN, BN, ta, tb, tbl, p, grid, static_cast<cudaStream_t>(stream), false));
   return DLLM_OK;

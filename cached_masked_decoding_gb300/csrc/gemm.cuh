@@ -85,9 +85,51 @@ struct GemmCfg {
                                     (2 * STAGES + 4) * 8 + 64;
 };
 
-__device__ __forceinline__ long long sk_owner(long long i, long long G, long long total) {
+// ---------------------------------------------------------------- chunk positions
+// Stream-K bookkeeping in 32-bit integers (a phase has at most a few 1e5
+// chunks, times the grid stays below 2^31) and without divisions in the
+// per-chunk loops: 64-bit integer division is a long software sequence,
+// and several of them per chunk would cap the TMA issue rate.
+__device__ __forceinline__ uint32_t sk_begin(uint32_t cta, uint32_t G, uint32_t total) { return cta * total / G; }
+
+// The CTA whose stream-K range holds chunk i.
+__device__ __forceinline__ uint32_t sk_owner32(uint32_t i, uint32_t G, uint32_t total) {
   return ((i + 1) * G + total - 1) / total - 1;
 }
+
+// (k-chunk, n-tile, m-tile) of a chunk; chunks run k fastest, then n-tiles,
+// then m-tiles.
+struct ChunkPos {
+  int k, n, m;
+  __device__ __forceinline__ void init(uint32_t g, int kc, int n_tiles) {
+    const uint32_t tile = g / (uint32_t)kc;
+    k = (int)(g - tile * (uint32_t)kc);
+    m = (int)(tile / (uint32_t)n_tiles);
+    n = (int)(tile - (uint32_t)m * (uint32_t)n_tiles);
+  }
+  __device__ __forceinline__ void next(int kc, int n_tiles) {
+    if (++k == kc) {
+      k = 0;
+      if (++n == n_tiles) {
+        n = 0;
+        ++m;
+      }
+    }
+  }
+};
+
+// Slot and phase parity of a position in the shared-memory ring.
+struct RingPos {
+  int s;
+  uint32_t par;
+  __device__ __forceinline__ void next(int stages) {
+    if (++s == stages) {
+      s = 0;
+      par ^= 1u;
+    }
+  }
+};
+
 
 // Sum over the 32 lanes of a warp of 32 per-lane columns: afterwards v[0] on
 // lane c holds the total of column c.  Fixed pairing order (deterministic).
@@ -416,9 +458,11 @@ __global__ void __launch_bounds__(192, 1)
   int* bcast = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long G = gridDim.x, cta = blockIdx.x;
-  const long long start = cta * p.total / G;
-  const long long end = (cta + 1) * p.total / G;
+  const uint32_t G = gridDim.x, cta = blockIdx.x;
+  const uint32_t total = (uint32_t)p.total;
+  const uint32_t start = sk_begin(cta, G, total);
+  const uint32_t end = sk_begin(cta + 1, G, total);
+  const int kc = p.kc, n_tiles = p.n_tiles;
   const bool split = BN <= 128 && p.split != 0;
   const int n_rows = split ? 2 * BN : BN;                      // MMA width
   const uint32_t stage_tx = (uint32_t)(C::A_BYTES + n_rows * 128);
@@ -459,47 +503,41 @@ __global__ void __launch_bounds__(192, 1)
       // ------------------------------------------------ TMA producer
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const long long n = end - start;
-      const int pre = (int)(n < STAGES ? n : STAGES);
+      const int n = (int)(end - start);
+      const int pre = n < STAGES ? n : STAGES;
       // weights do not depend on the previous kernel: start streaming them
       // before waiting for its activations
+      ChunkPos cw;
+      cw.init(start, kc, n_tiles);
       for (int i = 0; i < pre; ++i) {
-        const long long gch = start + i;
-        const long long tile = gch / p.kc;
-        const int k = (int)(gch - tile * p.kc);
-        const int m_idx = (int)(tile / p.n_tiles);
         mbar_arrive_expect_tx(&full[i], stage_tx);
-        tma_load_2d(sA + i * C::A_BYTES, &tmA, &full[i], k * 64, m_idx * 128, pol_w);
+        tma_load_2d(sA + i * C::A_BYTES, &tmA, &full[i], cw.k * 64, cw.m * 128, pol_w);
+        cw.next(kc, n_tiles);
       }
       griddep_wait();
+      ChunkPos cx;
+      cx.init(start, kc, n_tiles);
       for (int i = 0; i < pre; ++i) {
-        const long long gch = start + i;
-        const long long tile = gch / p.kc;
-        const int k = (int)(gch - tile * p.kc);
-        const int n_idx = (int)(tile % p.n_tiles);
-        tma_load_2d(sB + i * C::B_BYTES, &tmB, &full[i], k * 64, n_idx * BN, pol_x);
-        if (split) tma_load_2d(sB + i * C::B_BYTES + BN * 128, &tmBlo, &full[i], k * 64, n_idx * BN, pol_x);
+        tma_load_2d(sB + i * C::B_BYTES, &tmB, &full[i], cx.k * 64, cx.n * BN, pol_x);
+        if (split) tma_load_2d(sB + i * C::B_BYTES + BN * 128, &tmBlo, &full[i], cx.k * 64, cx.n * BN, pol_x);
+        cx.next(kc, n_tiles);
       }
-      long long issued = pre;
-      for (long long i = pre; i < n; ++i) {
-        const int s = (int)(i % STAGES);
-        const uint32_t ph = (uint32_t)((i / STAGES) & 1);
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, ERR_GEMM_EMPTY)) break;
-        const long long gch = start + i;
-        const long long tile = gch / p.kc;
-        const int k = (int)(gch - tile * p.kc);
-        const int m_idx = (int)(tile / p.n_tiles);
-        const int n_idx = (int)(tile % p.n_tiles);
-        mbar_arrive_expect_tx(&full[s], stage_tx);
-        tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], k * 64, m_idx * 128, pol_w);
-        tma_load_2d(sB + s * C::B_BYTES, &tmB, &full[s], k * 64, n_idx * BN, pol_x);
-        if (split) tma_load_2d(sB + s * C::B_BYTES + BN * 128, &tmBlo, &full[s], k * 64, n_idx * BN, pol_x);
+      RingPos rw{pre % STAGES, (uint32_t)((pre / STAGES) & 1)};
+      int issued = pre;
+      for (int i = pre; i < n; ++i) {
+        if (!mbar_wait(&empty[rw.s], rw.par ^ 1u, abort_flag, p.err, ERR_GEMM_EMPTY)) break;
+        mbar_arrive_expect_tx(&full[rw.s], stage_tx);
+        tma_load_2d(sA + rw.s * C::A_BYTES, &tmA, &full[rw.s], cw.k * 64, cw.m * 128, pol_w);
+        tma_load_2d(sB + rw.s * C::B_BYTES, &tmB, &full[rw.s], cw.k * 64, cw.n * BN, pol_x);
+        if (split) tma_load_2d(sB + rw.s * C::B_BYTES + BN * 128, &tmBlo, &full[rw.s], cw.k * 64, cw.n * BN, pol_x);
+        cw.next(kc, n_tiles);
+        rw.next(STAGES);
         issued = i + 1;
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's smem goes away
-        const long long lo = issued > STAGES ? issued - STAGES : 0;
-        for (long long i = lo; i < issued; ++i)
+        const int lo = issued > STAGES ? issued - STAGES : 0;
+        for (int i = lo; i < issued; ++i)
           mbar_wait(&full[i % STAGES], (uint32_t)((i / STAGES) & 1), nullptr, p.err, ERR_GEMM_DRAIN);
       }
     }
@@ -507,37 +545,39 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       const uint32_t idesc = idesc_bf16_f32(128, n_rows);
-      long long g = start, i = 0;
+      uint32_t g = start, k = start % (uint32_t)kc;
+      RingPos rm{0, 0u};
+      bool first = true;
       int seg = 0;
       bool ok = true;
       while (ok && g < end) {
-        const long long tile = g / p.kc;
-        const long long seg_first = g;
-        const long long seg_end = ((tile + 1) * p.kc < end) ? (tile + 1) * p.kc : end;
+        const uint32_t len = ((uint32_t)kc - k < end - g) ? (uint32_t)kc - k : end - g;
         const int buf = seg & 1;
         const uint32_t use = (uint32_t)(seg >> 1);
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, ERR_GEMM_TEMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::B_ROWS);
-        for (; g < seg_end; ++g, ++i) {
-          const int s = (int)(i % STAGES);
-          if (!mbar_wait(&full[s], (uint32_t)((i / STAGES) & 1), abort_flag, p.err, ERR_GEMM_FULL)) {
+        for (uint32_t i = 0; i < len; ++i) {
+          if (!mbar_wait(&full[rm.s], rm.par, abort_flag, p.err, ERR_GEMM_FULL)) {
             ok = false;
             break;
           }
-          if (p.trace && i == 0) p.trace[cta * 8 + 2] = globaltimer();
+          if (p.trace && first) p.trace[cta * 8 + 2] = globaltimer();
+          first = false;
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
-          const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
+          const uint32_t a0 = smem_u32(sA + rm.s * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + rm.s * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
-                        (g > seg_first || kk > 0) ? 1u : 0u);
-          mma_commit(&empty[s]);
+            mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[rm.s]);
+          rm.next(STAGES);
         }
         if (!ok) break;
         mma_commit(&tfull[buf]);
         ++seg;
+        g += len;
+        k = 0;
       }
       if (p.trace) p.trace[cta * 8 + 3] = globaltimer();
     }
@@ -546,33 +586,50 @@ __global__ void __launch_bounds__(192, 1)
     griddep_wait();
     const int q = warp & 3;
     const int l128 = q * 32 + lane;
-    long long g = start;
+    uint32_t g = start;
+    ChunkPos cp;
+    cp.init(start, kc, n_tiles);
     int seg = 0;
+    int rs_tile = -1;
     while (g < end) {
-      const long long tile = g / p.kc;
-      const long long seg_first = g;
-      const long long seg_end = ((tile + 1) * p.kc < end) ? (tile + 1) * p.kc : end;
-      const bool full_tile = (seg_first == tile * p.kc) && (seg_end == (tile + 1) * p.kc);
-      const int m_idx = (int)(tile / p.n_tiles);
-      const int n_idx = (int)(tile % p.n_tiles);
+      const uint32_t len = ((uint32_t)(kc - cp.k) < end - g) ? (uint32_t)(kc - cp.k) : end - g;
+      const uint32_t seg_end = g + len;
+      const uint32_t t0 = g - (uint32_t)cp.k;                  // first chunk of this tile
+      const bool full_tile = (cp.k == 0) && (len == (uint32_t)kc);
+      const int m_idx = cp.m;
+      const int n_idx = cp.n;
+      const int tile = m_idx * n_tiles + n_idx;
       const int buf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
 
-      named_bar_sync(1, 128);
-      for (int c = l128; c < BN; c += 128) {
-        const int r = n_idx * BN + c;
-        float f = 1.0f;
+      if (n_idx != rs_tile) {
+        // RMSNorm row factors of this activation tile: partial sums of squares
+        // staged in smem with parallel loads, then each row sums its partials
+        // in order
+        rs_tile = n_idx;
+        named_bar_sync(1, 128);
         if (p.ss_in) {
-          f = 0.0f;
-          if (r < p.N) {
-            float s = 0.0f;
-            for (int t = 0; t < p.ss_in_tiles; ++t) s += p.ss_in[(long long)r * p.ss_in_tiles + t];
-            f = rsqrtf(s * p.inv_d + p.eps);
+          const int tiles = p.ss_in_tiles;
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int e = l128; e < 32 * tiles; e += 128) {
+              const int c = e / tiles, t = e - c * tiles;
+              const int r = n_idx * BN + c0 + c;
+              xch[e] = r < p.N ? __ldcg(&p.ss_in[(long long)r * tiles + t]) : 0.0f;
+            }
+            named_bar_sync(1, 128);
+            if (l128 < 32) {
+              const int r = n_idx * BN + c0 + l128;
+              float sum = 0.0f;
+              for (int t = 0; t < tiles; ++t) sum += xch[l128 * tiles + t];
+              rs_s[c0 + l128] = r < p.N ? rsqrtf(sum * p.inv_d + p.eps) : 0.0f;
+            }
+            named_bar_sync(1, 128);
           }
+        } else {
+          for (int c = l128; c < BN; c += 128) rs_s[c] = 1.0f;
         }
-        rs_s[c] = f;
+        named_bar_sync(1, 128);
       }
-      named_bar_sync(1, 128);
 
       // every epilogue warp takes the same decision: a warp whose wait gave up
       // raised *abort_flag before this barrier
@@ -594,8 +651,8 @@ __global__ void __launch_bounds__(192, 1)
           epi_chunk<KIND>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red);
         }
       } else {
-        const int slot = (seg_first == start) ? 0 : 1;
-        float* wsp = p.ws + ((cta * 2 + slot) * (long long)BN) * 128;
+        const int slot = (g == start) ? 0 : 1;
+        float* wsp = p.ws + (((long long)cta * 2 + slot) * BN) * 128;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
@@ -608,14 +665,17 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
         named_bar_sync(1, 128);
-        const long long t0 = tile * p.kc, t1 = (tile + 1) * p.kc - 1;
-        const long long c_first = sk_owner(t0, G, p.total), c_last = sk_owner(t1, G, p.total);
+        const uint32_t c_first = sk_owner32(t0, G, total), c_last = sk_owner32(t0 + (uint32_t)kc - 1, G, total);
         if (l128 == 0) {
           // contributors: the CTAs in [c_first, c_last] whose chunk range is not
           // empty (with fewer chunks than CTAs some ranges are)
           int contributors = 0;
-          for (long long ctr = c_first; ctr <= c_last; ++ctr)
-            contributors += (ctr * p.total / G) < ((ctr + 1) * p.total / G) ? 1 : 0;
+          uint32_t st = sk_begin(c_first, G, total);
+          for (uint32_t ctr = c_first; ctr <= c_last; ++ctr) {
+            const uint32_t en = sk_begin(ctr + 1, G, total);
+            contributors += st < en ? 1 : 0;
+            st = en;
+          }
           const int old = atomic_add_acq_rel_gpu(&p.counters[tile], 1);
           const int last = (old == contributors - 1);
           if (last) p.counters[tile] = 0;
@@ -628,20 +688,49 @@ __global__ void __launch_bounds__(192, 1)
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-            for (long long ctr = c_first; ctr <= c_last; ++ctr) {
-              const long long st = ctr * p.total / G;
-              if (st == (ctr + 1) * p.total / G) continue;   // empty range: no partial
-              const long long sstart = st > t0 ? st : t0;
-              const int sl = (sstart == st) ? 0 : 1;
-              const float* src = p.ws + ((ctr * 2 + sl) * (long long)BN) * 128;
+            // partials in contributor order, two at a time so that both sets
+            // of loads are in flight together: ((v + p0) + p1) + ...
+            uint32_t ctr = c_first;
+            uint32_t st = sk_begin(c_first, G, total);
+            while (ctr <= c_last) {
+              const float* src0 = nullptr;
+              const float* src1 = nullptr;
+              int ns = 0;
+              for (; ctr <= c_last && ns < 2; ++ctr) {
+                const uint32_t en = sk_begin(ctr + 1, G, total);
+                const uint32_t cst = st;
+                st = en;
+                if (cst == en) continue;                     // empty range: no partial
+                const int sl = (cst >= t0) ? 0 : 1;          // its first segment starts in this tile?
+                const float* sp = p.ws + (((long long)ctr * 2 + sl) * BN) * 128 + (long long)c0 * 128 + l128;
+                if (ns == 0) src0 = sp;
+                else src1 = sp;
+                ++ns;
+              }
+              if (ns == 2) {
+                float x0[32], x1[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += __ldcg(&src[(long long)(c0 + j) * 128 + l128]);
+                for (int j = 0; j < 32; ++j) {
+                  x0[j] = __ldcg(src0 + j * 128);
+                  x1[j] = __ldcg(src1 + j * 128);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = (v[j] + x0[j]) + x1[j];
+              } else if (ns == 1) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += __ldcg(src0 + j * 128);
+              }
             }
             epi_chunk<KIND>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red);
           }
         }
       }
       g = seg_end;
+      cp.k = 0;                                                // the next segment starts a tile
+      if (++cp.n == n_tiles) {
+        cp.n = 0;
+        ++cp.m;
+      }
       ++seg;
     }
     if (p.trace && l128 == 0) p.trace[cta * 8 + 4] = globaltimer();

@@ -258,51 +258,6 @@ __device__ __forceinline__ void merge_row(const MergeParams& p, int row, int tid
   named_bar_sync(1, 128);
 }
 
-// ---------------------------------------------------------------- chunk positions
-// Stream-K bookkeeping in 32-bit integers (a phase has at most a few 1e5
-// chunks, times the grid stays below 2^31) and without divisions in the
-// per-chunk loops: 64-bit integer division is a long software sequence,
-// and several of them per chunk would cap the TMA issue rate.
-__device__ __forceinline__ uint32_t sk_begin(uint32_t cta, uint32_t G, uint32_t total) { return cta * total / G; }
-
-// The CTA whose stream-K range holds chunk i.
-__device__ __forceinline__ uint32_t sk_owner32(uint32_t i, uint32_t G, uint32_t total) {
-  return ((i + 1) * G + total - 1) / total - 1;
-}
-
-// (k-chunk, n-tile, m-tile) of a chunk; chunks run k fastest, then n-tiles,
-// then m-tiles.
-struct ChunkPos {
-  int k, n, m;
-  __device__ __forceinline__ void init(uint32_t g, int kc, int n_tiles) {
-    const uint32_t tile = g / (uint32_t)kc;
-    k = (int)(g - tile * (uint32_t)kc);
-    m = (int)(tile / (uint32_t)n_tiles);
-    n = (int)(tile - (uint32_t)m * (uint32_t)n_tiles);
-  }
-  __device__ __forceinline__ void next(int kc, int n_tiles) {
-    if (++k == kc) {
-      k = 0;
-      if (++n == n_tiles) {
-        n = 0;
-        ++m;
-      }
-    }
-  }
-};
-
-// Slot and phase parity of a position in the shared-memory ring.
-struct RingPos {
-  int s;
-  uint32_t par;
-  __device__ __forceinline__ void next(int stages) {
-    if (++s == stages) {
-      s = 0;
-      par ^= 1u;
-    }
-  }
-};
-
 // ---------------------------------------------------------------- the kernel
 template <int BN, int HD>
 __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
