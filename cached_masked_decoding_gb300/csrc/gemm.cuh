@@ -16,11 +16,15 @@
 // yields W.hi and W.lo side by side in TMEM, summed in the epilogue.  The
 // weights are read once either way; while the GEMM is bound by HBM the extra
 // MMA width is free.
-// Work split ("stream-K"): the m_tiles*n_tiles*kc chunks of 64 reduction
-// elements are cut into gridDim.x equal contiguous ranges, so every SM streams
-// the same number of weight bytes.  A tile cut between CTAs is finished by the
-// last contributor to arrive, which sums every contributor's partial in
-// contributor order: results do not depend on arrival order.
+// Work split: W = tiles / gridDim.x whole waves of tiles first - CTA c takes
+// tiles w*G + c, so CTAs side by side work on tiles side by side, which share
+// their weight rows (tiles are numbered m-major): a weight tile comes from HBM
+// once per wave and from L2 for the other n-tiles.  The remaining tiles'
+// chunks of 64 reduction elements are cut into gridDim.x equal contiguous
+// ranges ("stream-K"), so every SM streams the same number of bytes.  A tile
+// cut between CTAs is finished by the last contributor to arrive, which sums
+// every contributor's partial in contributor order: results do not depend on
+// arrival order.
 #pragma once
 
 #include "ptx.cuh"
@@ -83,6 +87,68 @@ struct GemmCfg {
   static constexpr int RED_FLOATS = 4 * 32 * 3;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCH_FLOATS * 4 + 256 * 4 + RED_FLOATS * 4 +
                                     (2 * STAGES + 4) * 8 + 64;
+};
+
+// ---------------------------------------------------------------- standalone GEMM work list
+// One segment: kc-chunk run [k0, k0 + len) of one tile; `whole` when it is the
+// full reduction of the tile; rg0 is its first chunk in remainder-chunk space
+// (stream-K part only).
+struct GemmSeg {
+  int m, n, tile, k0, len;
+  bool whole;
+  uint32_t rg0;
+};
+
+// The segments of one CTA: its whole tiles, then its stream-K range of the
+// remainder (see the work split above).
+struct GemmWork {
+  uint32_t G, cta, kc, n_tiles, W, full, total_r, rs, re;
+  __device__ __forceinline__ void init(uint32_t G_, uint32_t cta_, uint32_t tiles, uint32_t kc_, uint32_t n_tiles_) {
+    G = G_;
+    cta = cta_;
+    kc = kc_;
+    n_tiles = n_tiles_;
+    W = tiles / G;
+    full = W * G;
+    total_r = (tiles - full) * kc;
+    rs = total_r ? cta * total_r / G : 0;
+    re = total_r ? (cta + 1) * total_r / G : 0;
+  }
+  __device__ __forceinline__ uint32_t chunks() const { return W * kc + (re - rs); }
+};
+
+struct GemmSegCursor {
+  uint32_t w, g;
+  __device__ __forceinline__ void init(const GemmWork& wk) {
+    w = 0;
+    g = wk.rs;
+  }
+  __device__ __forceinline__ bool next(const GemmWork& wk, GemmSeg& o) {
+    uint32_t tile;
+    if (w < wk.W) {
+      tile = w * wk.G + wk.cta;
+      ++w;
+      o.k0 = 0;
+      o.len = (int)wk.kc;
+      o.whole = true;
+      o.rg0 = 0;
+    } else if (g < wk.re) {
+      const uint32_t rt = g / wk.kc, k = g - rt * wk.kc;
+      const uint32_t len = (wk.kc - k < wk.re - g) ? wk.kc - k : wk.re - g;
+      tile = wk.full + rt;
+      o.k0 = (int)k;
+      o.len = (int)len;
+      o.whole = (k == 0) && (len == wk.kc);
+      o.rg0 = g;
+      g += len;
+    } else {
+      return false;
+    }
+    o.tile = (int)tile;
+    o.m = (int)(tile / wk.n_tiles);
+    o.n = (int)(tile - (uint32_t)o.m * wk.n_tiles);
+    return true;
+  }
 };
 
 // ---------------------------------------------------------------- chunk positions
@@ -459,10 +525,9 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t G = gridDim.x, cta = blockIdx.x;
-  const uint32_t total = (uint32_t)p.total;
-  const uint32_t start = sk_begin(cta, G, total);
-  const uint32_t end = sk_begin(cta + 1, G, total);
   const int kc = p.kc, n_tiles = p.n_tiles;
+  GemmWork wk;
+  wk.init(G, cta, (uint32_t)(p.m_tiles * n_tiles), (uint32_t)kc, (uint32_t)n_tiles);
   const bool split = BN <= 128 && p.split != 0;
   const int n_rows = split ? 2 * BN : BN;                      // MMA width
   const uint32_t stage_tx = (uint32_t)(C::A_BYTES + n_rows * 128);
@@ -503,36 +568,54 @@ __global__ void __launch_bounds__(192, 1)
       // ------------------------------------------------ TMA producer
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const int n = (int)(end - start);
+      const int n = (int)wk.chunks();
       const int pre = n < STAGES ? n : STAGES;
       // weights do not depend on the previous kernel: start streaming them
       // before waiting for its activations
-      ChunkPos cw;
-      cw.init(start, kc, n_tiles);
+      GemmSegCursor sw;
+      sw.init(wk);
+      GemmSeg a;
+      bool live = sw.next(wk, a);
+      int ka = 0;
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], stage_tx);
-        tma_load_2d(sA + i * C::A_BYTES, &tmA, &full[i], cw.k * 64, cw.m * 128, pol_w);
-        cw.next(kc, n_tiles);
+        tma_load_2d(sA + i * C::A_BYTES, &tmA, &full[i], (a.k0 + ka) * 64, a.m * 128, pol_w);
+        if (++ka == a.len) {
+          live = sw.next(wk, a);
+          ka = 0;
+        }
       }
       griddep_wait();
-      ChunkPos cx;
-      cx.init(start, kc, n_tiles);
-      for (int i = 0; i < pre; ++i) {
-        tma_load_2d(sB + i * C::B_BYTES, &tmB, &full[i], cx.k * 64, cx.n * BN, pol_x);
-        if (split) tma_load_2d(sB + i * C::B_BYTES + BN * 128, &tmBlo, &full[i], cx.k * 64, cx.n * BN, pol_x);
-        cx.next(kc, n_tiles);
+      {
+        GemmSegCursor sx;
+        sx.init(wk);
+        GemmSeg x;
+        sx.next(wk, x);
+        int kx = 0;
+        for (int i = 0; i < pre; ++i) {
+          tma_load_2d(sB + i * C::B_BYTES, &tmB, &full[i], (x.k0 + kx) * 64, x.n * BN, pol_x);
+          if (split) tma_load_2d(sB + i * C::B_BYTES + BN * 128, &tmBlo, &full[i], (x.k0 + kx) * 64, x.n * BN, pol_x);
+          if (++kx == x.len) {
+            sx.next(wk, x);
+            kx = 0;
+          }
+        }
       }
       RingPos rw{pre % STAGES, (uint32_t)((pre / STAGES) & 1)};
       int issued = pre;
-      for (int i = pre; i < n; ++i) {
+      for (int i = pre; i < n && live; ++i) {
         if (!mbar_wait(&empty[rw.s], rw.par ^ 1u, abort_flag, p.err, ERR_GEMM_EMPTY)) break;
+        const int k = a.k0 + ka;
         mbar_arrive_expect_tx(&full[rw.s], stage_tx);
-        tma_load_2d(sA + rw.s * C::A_BYTES, &tmA, &full[rw.s], cw.k * 64, cw.m * 128, pol_w);
-        tma_load_2d(sB + rw.s * C::B_BYTES, &tmB, &full[rw.s], cw.k * 64, cw.n * BN, pol_x);
-        if (split) tma_load_2d(sB + rw.s * C::B_BYTES + BN * 128, &tmBlo, &full[rw.s], cw.k * 64, cw.n * BN, pol_x);
-        cw.next(kc, n_tiles);
+        tma_load_2d(sA + rw.s * C::A_BYTES, &tmA, &full[rw.s], k * 64, a.m * 128, pol_w);
+        tma_load_2d(sB + rw.s * C::B_BYTES, &tmB, &full[rw.s], k * 64, a.n * BN, pol_x);
+        if (split) tma_load_2d(sB + rw.s * C::B_BYTES + BN * 128, &tmBlo, &full[rw.s], k * 64, a.n * BN, pol_x);
         rw.next(STAGES);
         issued = i + 1;
+        if (++ka == a.len) {
+          live = sw.next(wk, a);
+          ka = 0;
+        }
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's smem goes away
@@ -545,19 +628,20 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       const uint32_t idesc = idesc_bf16_f32(128, n_rows);
-      uint32_t g = start, k = start % (uint32_t)kc;
       RingPos rm{0, 0u};
       bool first = true;
       int seg = 0;
       bool ok = true;
-      while (ok && g < end) {
-        const uint32_t len = ((uint32_t)kc - k < end - g) ? (uint32_t)kc - k : end - g;
+      GemmSegCursor sc;
+      sc.init(wk);
+      GemmSeg sg;
+      while (ok && sc.next(wk, sg)) {
         const int buf = seg & 1;
         const uint32_t use = (uint32_t)(seg >> 1);
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, ERR_GEMM_TEMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::B_ROWS);
-        for (uint32_t i = 0; i < len; ++i) {
+        for (int i = 0; i < sg.len; ++i) {
           if (!mbar_wait(&full[rm.s], rm.par, abort_flag, p.err, ERR_GEMM_FULL)) {
             ok = false;
             break;
@@ -576,8 +660,6 @@ __global__ void __launch_bounds__(192, 1)
         if (!ok) break;
         mma_commit(&tfull[buf]);
         ++seg;
-        g += len;
-        k = 0;
       }
       if (p.trace) p.trace[cta * 8 + 3] = globaltimer();
     }
@@ -586,19 +668,16 @@ __global__ void __launch_bounds__(192, 1)
     griddep_wait();
     const int q = warp & 3;
     const int l128 = q * 32 + lane;
-    uint32_t g = start;
-    ChunkPos cp;
-    cp.init(start, kc, n_tiles);
+    GemmSegCursor sc;
+    sc.init(wk);
+    GemmSeg sg;
     int seg = 0;
     int rs_tile = -1;
-    while (g < end) {
-      const uint32_t len = ((uint32_t)(kc - cp.k) < end - g) ? (uint32_t)(kc - cp.k) : end - g;
-      const uint32_t seg_end = g + len;
-      const uint32_t t0 = g - (uint32_t)cp.k;                  // first chunk of this tile
-      const bool full_tile = (cp.k == 0) && (len == (uint32_t)kc);
-      const int m_idx = cp.m;
-      const int n_idx = cp.n;
-      const int tile = m_idx * n_tiles + n_idx;
+    while (sc.next(wk, sg)) {
+      const bool full_tile = sg.whole;
+      const int m_idx = sg.m;
+      const int n_idx = sg.n;
+      const int tile = sg.tile;
       const int buf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
 
@@ -651,7 +730,7 @@ __global__ void __launch_bounds__(192, 1)
           epi_chunk<KIND>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red);
         }
       } else {
-        const int slot = (g == start) ? 0 : 1;
+        const int slot = (sg.rg0 == wk.rs) ? 0 : 1;                // first segment of this CTA's stream-K range?
         float* wsp = p.ws + (((long long)cta * 2 + slot) * BN) * 128;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -665,6 +744,8 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
         named_bar_sync(1, 128);
+        const uint32_t total = wk.total_r;                          // stream-K space: the remainder tiles
+        const uint32_t t0 = sg.rg0 - (uint32_t)sg.k0;               // the tile's first chunk
         const uint32_t c_first = sk_owner32(t0, G, total), c_last = sk_owner32(t0 + (uint32_t)kc - 1, G, total);
         if (l128 == 0) {
           // contributors: the CTAs in [c_first, c_last] whose chunk range is not
@@ -724,12 +805,6 @@ __global__ void __launch_bounds__(192, 1)
             epi_chunk<KIND>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red);
           }
         }
-      }
-      g = seg_end;
-      cp.k = 0;                                                // the next segment starts a tile
-      if (++cp.n == n_tiles) {
-        cp.n = 0;
-        ++cp.m;
       }
       ++seg;
     }

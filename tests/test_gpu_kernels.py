@@ -52,6 +52,8 @@ GEMM_SHAPES = [
     (1024, 300, 512),     # several activation tiles (BN = 256)
     (640, 96, 1024),      # BN = 128
     (2048, 2048, 256),    # the compute-bound batch shape
+    (12288, 768, 256),    # refresh-shaped: 576 tiles, three whole waves + a stream-K remainder
+    (2432, 1024, 128),    # exactly one whole wave of 152 tiles (split), no remainder
 ]
 
 
