@@ -623,52 +623,68 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
               tl[ph * kTimelineSlots + 9] = globaltimer();
             }
           } else {
-            const int slot = (g == start) ? 0 : 1;
-            float* wsp = p.ws + ((cta * 2 + slot) * (long long)BN) * 128;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-              float v[32];
-              tmem_ld32(taddr + (uint32_t)c0, v);
-              if (split) add_lo<BN>(taddr, c0, v);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) __stcg(&wsp[(long long)(c0 + j) * 128 + l128], v[j]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
-            named_bar_sync(1, 128);
+            // A tile cut between CTAs is owned by the CTA whose range holds
+            // its first chunk.  The other contributors store their partial
+            // and count in; the owner keeps its own sums in tensor memory,
+            // waits until the others have counted in, adds their partials in
+            // contributor order and runs the epilogue.  A CTA owns at most the
+            // one tile that starts in its range, so no CTA runs two
+            // reductions back to back, and the owner's own partial never
+            // leaves the SM.
             const uint32_t t1 = t0 + (uint32_t)kc - 1;
             const uint32_t c_first = sk_owner32(t0, uG, total), c_last = sk_owner32(t1, uG, total);
-            if (l128 == 0) {
-              // contributors: the CTAs in [c_first, c_last] whose chunk range is
-              // not empty (with fewer chunks than CTAs some ranges are)
-              int contributors = 0;
-              uint32_t st = sk_begin(c_first, uG, total);
-              for (uint32_t ctr = c_first; ctr <= c_last; ++ctr) {
-                const uint32_t en = sk_begin(ctr + 1, uG, total);
-                contributors += st < en ? 1 : 0;
-                st = en;
-              }
-              const int old = atomic_add_acq_rel_gpu(&p.counters[tile], 1);
-              const int last = (old == contributors - 1);
-              if (last) p.counters[tile] = 0;
-              *bcast = last;
-              if (tl) {
-                if (g == start) tl[ph * kTimelineSlots + 6] = globaltimer();
-                if (last) tl[ph * kTimelineSlots + 7] = globaltimer();
-              }
-            }
-            named_bar_sync(1, 128);
-            if (*bcast) {
+            if (g != t0) {
+              // a contributor's segment in a tile it does not own is the first
+              // of its range: one partial slot per CTA
+              float* wsp = p.ws + ((cta * 2) * (long long)BN) * 128;
 #pragma unroll 1
               for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
+                tmem_ld32(taddr + (uint32_t)c0, v);
+                if (split) add_lo<BN>(taddr, c0, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                // partials in contributor order, two at a time so that both
-                // sets of loads are in flight together: ((v + p0) + p1) + ...
-                uint32_t ctr = c_first;
-                uint32_t st = sk_begin(c_first, uG, total);
+                for (int j = 0; j < 32; ++j) __stcg(&wsp[(long long)(c0 + j) * 128 + l128], v[j]);
+              }
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[buf]);
+              named_bar_sync(1, 128);
+              if (l128 == 0) {
+                flag_publish(&p.counters[tile], nullptr);
+                if (tl && g == start) tl[ph * kTimelineSlots + 6] = globaltimer();
+              }
+            } else {
+              if (l128 == 0) {
+                // the other contributors: CTAs in (c_first, c_last] whose chunk
+                // range is not empty (with fewer chunks than CTAs some are)
+                int others = 0;
+                uint32_t st = sk_begin(c_first + 1, uG, total);
+                for (uint32_t ctr = c_first + 1; ctr <= c_last; ++ctr) {
+                  const uint32_t en = sk_begin(ctr + 1, uG, total);
+                  others += st < en ? 1 : 0;
+                  st = en;
+                }
+                if (tl) tl[ph * kTimelineSlots + 7] = globaltimer();
+                flag_wait(&p.counters[tile], others, abort_flag, a.err);
+              }
+              if (named_bar_or(1, 128, *abort_flag != 0)) {
+                stop = true;
+                break;
+              }
+#pragma unroll 1
+              for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(taddr + (uint32_t)c0, v);
+                if (split) add_lo<BN>(taddr, c0, v);
+                if (c0 + 32 == BN) {
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(&tempty[buf]);
+                }
+                // the others' partials in contributor order, two at a time so
+                // that both sets of loads are in flight: ((own + p1) + p2) + ...
+                uint32_t ctr = c_first + 1;
+                uint32_t st = sk_begin(c_first + 1, uG, total);
                 while (ctr <= c_last) {
                   const float* src0 = nullptr;
                   const float* src1 = nullptr;
@@ -678,8 +694,7 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
                     const uint32_t cst = st;
                     st = en;
                     if (cst == en) continue;                     // empty range: no partial
-                    const int sl = (cst >= t0) ? 0 : 1;          // its first segment starts in this tile?
-                    const float* sp = p.ws + (((long long)ctr * 2 + sl) * BN) * 128 + (long long)c0 * 128 + l128;
+                    const float* sp = p.ws + (((long long)ctr * 2) * BN) * 128 + (long long)c0 * 128 + l128;
                     if (ns == 0) src0 = sp;
                     else src1 = sp;
                     ++ns;
