@@ -636,21 +636,34 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
             if (g != t0) {
               // a contributor's segment in a tile it does not own is the first
               // of its range: one partial slot per CTA
+              // stored through shared memory as [rows][128 features], 16 bytes
+              // per thread and store
               float* wsp = p.ws + ((cta * 2) * (long long)BN) * 128;
 #pragma unroll 1
               for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
                 tmem_ld32(taddr + (uint32_t)c0, v);
                 if (split) add_lo<BN>(taddr, c0, v);
+                if (c0 + 32 == BN) {
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(&tempty[buf]);
+                }
+                named_bar_sync(1, 128);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) __stcg(&wsp[(long long)(c0 + j) * 128 + l128], v[j]);
+                for (int c = 0; c < 32; ++c) xch[c * kStageLd + l128] = v[c];
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const int row = q + 4 * k;
+                  __stcg(reinterpret_cast<float4*>(&wsp[(long long)(c0 + row) * 128 + lane * 4]),
+                         *reinterpret_cast<const float4*>(xch + row * kStageLd + lane * 4));
+                }
               }
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&tempty[buf]);
               named_bar_sync(1, 128);
               if (l128 == 0) {
-                flag_publish(&p.counters[tile], nullptr);
+                // the owner reads the partial with generic loads: a release suffices
+                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(&p.counters[tile]) : "memory");
                 if (tl && g == start) tl[ph * kTimelineSlots + 6] = globaltimer();
               }
             } else {
