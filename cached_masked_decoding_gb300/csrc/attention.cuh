@@ -232,10 +232,15 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
       mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
       mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
       mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      // The reference max of a row only moves when a tile's max exceeds it by
+      // more than 8 (a factor 2^8 in probability); otherwise P = exp2(s - m)
+      // <= 256, and O and l keep their scale: the same sums, referred to a
+      // slightly smaller max, with the rescale of O skipped in most tiles.
+      const bool up_lo = mx_lo > m_lo + 8.0f, up_hi = mx_hi > m_hi + 8.0f;
+      const float mn_lo = up_lo ? mx_lo : m_lo, mn_hi = up_hi ? mx_hi : m_hi;
       const float use_lo = (mn_lo == -INFINITY) ? 0.0f : mn_lo;
       const float use_hi = (mn_hi == -INFINITY) ? 0.0f : mn_hi;
-      const float corr_lo = exp2f(m_lo - use_lo), corr_hi = exp2f(m_hi - use_hi);
+      const float corr_lo = up_lo ? exp2f(m_lo - use_lo) : 1.0f, corr_hi = up_hi ? exp2f(m_hi - use_hi) : 1.0f;
       m_lo = mn_lo;
       m_hi = mn_hi;
       float sum_lo = 0.0f, sum_hi = 0.0f;
@@ -254,12 +259,14 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
       sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 2);
       l_lo = l_lo * corr_lo + sum_lo;
       l_hi = l_hi * corr_hi + sum_hi;
+      if (up_lo || up_hi) {
 #pragma unroll
-      for (int i = 0; i < OT; ++i) {
-        oacc[i][0] *= corr_lo;
-        oacc[i][1] *= corr_lo;
-        oacc[i][2] *= corr_hi;
-        oacc[i][3] *= corr_hi;
+        for (int i = 0; i < OT; ++i) {
+          oacc[i][0] *= corr_lo;
+          oacc[i][1] *= corr_lo;
+          oacc[i][2] *= corr_hi;
+          oacc[i][3] *= corr_hi;
+        }
       }
       // O += P V
 #pragma unroll
