@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libdllm.so")
 OK, EINVAL, ENOMEM, ECUDA, EIO, ESTATE, ETIMEOUT = range(7)
 CACHE_NONE, CACHE_PREFIX, CACHE_DUAL = 0, 1, 2
 MODES = {"none": CACHE_NONE, "prefix": CACHE_PREFIX, "dual": CACHE_DUAL}
-SEL_THRESHOLD, SEL_FIXED_K, SEL_FACTOR, SEL_BUDGET = 0, 1, 2, 3
+SEL_THRESHOLD, SEL_FIXED_K, SEL_FACTOR, SEL_BUDGET, SEL_SCHEDULE = 0, 1, 2, 3, 4
 PREC_SPLIT, PREC_BF16 = 0, 1
 TENSOR_IDS = {"embed": 1, "attn_norm": 2, "wq": 3, "wk": 4, "wv": 5, "wo": 6, "ffn_norm": 7, "wg": 8, "wu": 9,
               "wd": 10, "final_norm": 11, "lm_head": 12}

@@ -1433,8 +1433,8 @@ dllm_status to_rule(const dllm_select* sel, SelectRule* r) {
   r->tau = sel->tau;
   r->k = sel->k;
   r->factor = sel->factor;
-  if (sel->policy < 0 || sel->policy > 3 || (sel->policy == 0 && std::isnan(sel->tau)) ||
-      (sel->policy == 1 && sel->k < 1) || (sel->policy == 2 && !(sel->factor > 0))) {
+  if (sel->policy < 0 || sel->policy > 4 || (sel->policy == 0 && std::isnan(sel->tau)) ||
+      ((sel->policy == 1 || sel->policy == 4) && sel->k < 1) || (sel->policy == 2 && !(sel->factor > 0))) {
     set_error("bad selection rule: policy=%d tau=%f k=%d factor=%f", sel->policy, sel->tau, sel->k, sel->factor);
     return DLLM_EINVAL;
   }
@@ -1486,7 +1486,9 @@ dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int3
   for (int i = 0; i < s->b; ++i) {
     const int cnt = s->host_ce[i];
     int& rem = s->remaining[(size_t)i * s->n_blocks + j];
-    if (cnt > rem || (rem > 0 && cnt == 0)) {
+    // every rule commits at least one MASK of the block per step, except the
+    // scheduled one, which may commit none while more steps are left
+    if (cnt > rem || (rem > 0 && cnt == 0 && !(rule.policy == 4 && rule.k > 1))) {
       set_error("sequence %d committed %d with %d MASK left in block %d", i, cnt, rem, j);
       return DLLM_ESTATE;
     }
@@ -1575,7 +1577,9 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
       if (!any) break;
       if (cached && refresh_interval > 0 && spb > 0 && spb % refresh_interval == 0) CKS(timed_refresh());
       int total = 0;
-      CKS(do_step(s, j, r, cache_mode, cnt.data(), &total, s->ev_a, s->ev_b));
+      SelectRule rs = r;
+      if (r.policy == 4) rs.k = std::max(1, r.k - spb);   // steps left in this block
+      CKS(do_step(s, j, rs, cache_mode, cnt.data(), &total, s->ev_a, s->ev_b));
       float ms = 0;
       CK(cudaEventElapsedTime(&ms, s->ev_a, s->ev_b));
       step_ms += ms;

@@ -103,6 +103,12 @@ __device__ __forceinline__ void select_commit_group(const float* conf_s, const i
   } else {
     if (rule.policy == 1) {
       n_sel = rule.k;
+    } else if (rule.policy == 4) {
+      // scheduled: the MASK count spread over the k steps left (may be 0)
+      for (int i = tid; i < B; i += nthr)
+        if (rank_s[i] >= 0) atomicAdd(shared_best, 1);
+      sync();
+      n_sel = *shared_best / max(rule.k, 1);
     } else if (rule.policy == 2) {
       // factor: largest n with (n+1)(1 - c_(n)) < f, c_(n) = confidence of rank n-1
       for (int i = tid; i < B; i += nthr) {

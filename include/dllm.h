@@ -58,7 +58,10 @@ typedef enum dllm_sel_policy {
     DLLM_SEL_THRESHOLD = 0, /* Algorithm 2: c >= tau, else the single best */
     DLLM_SEL_FIXED_K = 1,   /* the k most confident (min(k, remaining)) */
     DLLM_SEL_FACTOR = 2,    /* Algorithm 3 / eq. 13: largest n with (n+1)(1-c_(n)) < f */
-    DLLM_SEL_BUDGET = 3     /* eq. 9: largest prefix with sum eps + max eps < 1 */
+    DLLM_SEL_BUDGET = 3,    /* eq. 9: largest prefix with sum eps + max eps < 1 */
+    DLLM_SEL_SCHEDULE = 4   /* page 1's LLaDA remasking schedule: with k steps left in the
+                               block, the n_keep = (MASK count) / k most confident (n_keep
+                               may be 0); dllm_run counts k down from the given k per block */
 } dllm_sel_policy;
 
 /* Selection rule.  Ties in confidence go to the lowest position, ties in the

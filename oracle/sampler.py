@@ -19,6 +19,8 @@ Passages followed (zhongzhuzhou.org Fast-dLLM reading notes unless noted):
   the largest n with (n+1)(1 - c_(n)) < f, else the single best.
 * ``select_budget`` - eq. 9 (section 5.1): the largest confidence-ordered prefix
   with sum_j eps_j + max_j eps_j < 1, else the single best.
+* ``select_schedule`` - page 1's LLaDA low-confidence remasking inside a
+  block: with k steps left, the (MASK count) // k most confident are kept.
 * ``select_fixed_k`` - the fixed-count rule (page 1, opening paragraph: a fixed
   number of tokens per step; LLaDA's low-confidence remasking keeps the most
   confident predictions).
@@ -48,7 +50,7 @@ import numpy as np
 
 from . import model as M
 
-THRESHOLD, FIXED_K, FACTOR, BUDGET = 0, 1, 2, 3
+THRESHOLD, FIXED_K, FACTOR, BUDGET, SCHEDULE = 0, 1, 2, 3, 4
 
 
 @dataclasses.dataclass(frozen=True)
@@ -113,6 +115,14 @@ def select_budget(conf32: np.ndarray, eligible: np.ndarray) -> np.ndarray:
     return sel
 
 
+def select_schedule(conf32: np.ndarray, eligible: np.ndarray, steps_left: int) -> np.ndarray:
+    """Page 1's LLaDA remasking schedule: with steps_left steps to go, keep the
+    n_keep = (MASK count) // steps_left most confident predictions (possibly
+    none this step)."""
+    n_keep = int(eligible.sum()) // max(int(steps_left), 1)
+    return select_fixed_k(conf32, eligible, n_keep)
+
+
 def select(rule: Rule, conf32: np.ndarray, eligible: np.ndarray) -> np.ndarray:
     if rule.policy == THRESHOLD:
         return select_threshold(conf32, eligible, rule.tau)
@@ -122,6 +132,8 @@ def select(rule: Rule, conf32: np.ndarray, eligible: np.ndarray) -> np.ndarray:
         return select_factor(conf32, eligible, rule.factor)
     if rule.policy == BUDGET:
         return select_budget(conf32, eligible)
+    if rule.policy == SCHEDULE:            # rule.k: the steps left in the block
+        return select_schedule(conf32, eligible, rule.k)
     raise ValueError(rule.policy)
 
 
@@ -232,10 +244,14 @@ class Decoder:
         if cached:
             self.refresh()
         for j in range(self.n_blocks):
+            spb = 0
             while self.eligible(j).any():
                 if refresh_every_step and cached:
                     self.refresh()
-                trace.append(self.step(j, rule))
+                # the scheduled rule counts its k down within each block
+                r = dataclasses.replace(rule, k=max(1, rule.k - spb)) if rule.policy == SCHEDULE else rule
+                trace.append(self.step(j, r))
+                spb += 1
                 if max_steps is not None and len(trace) >= max_steps:
                     return self.x[:, self.P:].copy(), trace
             if cached and j < self.n_blocks - 1:

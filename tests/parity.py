@@ -11,6 +11,8 @@ select differently, the oracle's decision must sit within that tolerance of a
 decision boundary (a near tie, counted and reported).  The oracle then adopts the GPU's commit
 and both continue.
 """
+import dataclasses
+
 import numpy as np
 
 from cached_masked_decoding_gb300 import binding
@@ -44,7 +46,7 @@ def decision_margin(rule: OS.Rule, conf: np.ndarray, elig: np.ndarray) -> float:
     rank_gap = float(gaps.min()) if gaps.size else np.inf
     if rule.policy == OS.THRESHOLD:
         return min(float(np.abs(c - rule.tau).min()), rank_gap)
-    if rule.policy == OS.FIXED_K:
+    if rule.policy in (OS.FIXED_K, OS.SCHEDULE):
         return rank_gap
     if rule.policy == OS.FACTOR:
         n = np.arange(1, c.size + 1)
@@ -82,6 +84,7 @@ def logit_shift(dec: OS.Decoder, h_gpu: np.ndarray, h_orc: np.ndarray, toks: np.
 def run_synced(gpu: binding.State, dec: OS.Decoder, rule: OS.Rule, mode: str, check_hidden: bool = True,
                max_steps: int | None = None) -> Report:
     rep = Report()
+    base_rule = rule
     ctol = conf_tol(dec.cfg)
     grule = to_gpu_rule(rule)
     mask = dec.cfg.mask_id
@@ -91,12 +94,17 @@ def run_synced(gpu: binding.State, dec: OS.Decoder, rule: OS.Rule, mode: str, ch
         dec.refresh()
     for j in range(dec.n_blocks):
         s = dec.block_start(j)
+        spb = 0
         while True:
             x_before = gpu.tokens()
             np.testing.assert_array_equal(x_before, dec.x, err_msg="trajectories out of sync")
             elig = x_before[:, s:s + dec.B] == mask
             if not elig.any():
                 break
+            if rule.policy == OS.SCHEDULE:      # k counts down within the block
+                step_rule = dataclasses.replace(base_rule, k=max(1, base_rule.k - spb))
+                rule, grule = step_rule, to_gpu_rule(step_rule)
+            spb += 1
             gpu.step_ex(j, grule, mode)
             x_after, conf_g, arg_g = gpu.read()
             conf_o, arg_o, margin, hb, _ = dec.compute(j)

@@ -85,6 +85,7 @@ RULES = {
     "fixed4": OS.Rule(OS.FIXED_K, k=4),
     "factor": OS.Rule(OS.FACTOR, factor=1.0),
     "budget": OS.Rule(OS.BUDGET),
+    "schedule": OS.Rule(OS.SCHEDULE, k=6),
 }
 
 
@@ -102,7 +103,7 @@ def test_trajectory_matches_oracle(gmodel, omodel, mode, rule):
     st.free()
 
 
-@pytest.mark.parametrize("rule", ["tau_gt_1", "fixed1", "budget"])
+@pytest.mark.parametrize("rule", ["tau_gt_1", "fixed1", "budget", "schedule"])
 def test_other_rules_dual(gmodel, omodel, rule):
     P, gen, B = 32, 32, 16
     pr = synth.prompts(CFG, 0, 1, P)
@@ -111,6 +112,26 @@ def test_other_rules_dual(gmodel, omodel, rule):
     rep = run_synced(st, dec, RULES[rule], "dual")
     if rule in ("tau_gt_1", "fixed1"):
         assert rep.steps == gen       # exactly one token per step
+    if rule == "schedule":
+        assert rep.steps == 6 * (gen // B)   # the schedule's steps per block, exactly
+    st.free()
+
+
+def test_schedule_rule_is_llada_sampler_on_gpu(gmodel, omodel):
+    """Page 1's LLaDA sampler: no cache, the whole answer as one block, the
+    scheduled rule over 10 steps, step by step against the oracle (which the
+    CPU pins tie to its own restatement of the sampler); then dllm_run's own
+    countdown of k gives the same number of steps."""
+    P, gen, steps = 32, 64, 10
+    pr = synth.prompts(CFG, 5, 1, P)
+    st = binding.State(gmodel, pr, 1, P, gen, gen)
+    dec = OS.Decoder(omodel, pr, gen, gen, "none")
+    rep = run_synced(st, dec, OS.Rule(OS.SCHEDULE, k=steps), "none")
+    assert rep.steps == steps
+    st.free()
+    st = binding.State(gmodel, pr, 1, P, gen, gen)
+    stats = st.run(binding.make_select(binding.SEL_SCHEDULE, k=steps), "none")
+    assert stats["steps"] == steps and stats["committed"] == gen
     st.free()
 
 

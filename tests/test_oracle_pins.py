@@ -386,6 +386,22 @@ def test_tau_above_one_is_llada_one_per_step(tiny_w):
     np.testing.assert_array_equal(toks[0], ref)
 
 
+@pytest.mark.parametrize("steps", [4, 7, 16, 20])
+def test_schedule_rule_is_llada_sampler(tiny_w, steps):
+    """Page 1's LLaDA sampler (whole answer, full forward, n_keep = remaining
+    MASKs spread over the remaining steps) written out on its own, against the
+    block decoder with the scheduled rule, one block covering the answer and
+    no cache: the same tokens, exactly `steps` steps (more steps than MASKs
+    leave the early steps empty)."""
+    P, gen = 12, 16
+    pr = synth.prompts(tiny_w.cfg, 3, 1, P)
+    dec = S.Decoder(tiny_w, pr, gen, gen, "none")
+    toks, trace = dec.generate(S.Rule(S.SCHEDULE, k=steps))
+    assert len(trace) == steps
+    assert sum(int(st.committed.sum()) for st in trace) == gen
+    np.testing.assert_array_equal(toks[0], S.llada_sample(tiny_w, pr[0], gen, steps))
+
+
 @pytest.mark.parametrize("mode", ["prefix", "dual"])
 def test_refresh_every_step_equals_no_cache(tiny_w, mode):
     _, t_none, tr_none = _run(tiny_w, "none", S.Rule(S.THRESHOLD, 0.9), b=2)
