@@ -94,6 +94,7 @@ SIGNATURES = {
     "dllm_read_step_timeline": (_I32, [_P, _P, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "dllm_op_gemm_trace": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _P, ctypes.POINTER(_I32), _P]),
     "dllm_op_attention": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
+    "dllm_staleness": (_I32, [_P, _I32, _P, _P, _P, _P]),
     "dllm_op_attention_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
     "dllm_op_select_commit": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(Select), _P, _P]),
     "dllm_last_error": (ctypes.c_char_p, []),
@@ -303,6 +304,15 @@ class State:
         check(lib().dllm_kernel_times(self.h, _ptr(ms), _ptr(cnt), _ptr(by), n))
         return {k: {"ms": float(ms[i]), "launches": int(cnt[i]), "bytes": float(by[i])}
                 for i, k in enumerate(KERNEL_CLASSES)}
+
+    def staleness(self, block_idx: int) -> dict:
+        L = self.n_layers
+        k = np.zeros(L, dtype=np.float32)
+        v = np.zeros(L, dtype=np.float32)
+        agree = ctypes.c_float()
+        dconf = ctypes.c_float()
+        check(lib().dllm_staleness(self.h, block_idx, _ptr(k), _ptr(v), ctypes.byref(agree), ctypes.byref(dconf)))
+        return {"k_cos": k, "v_cos": v, "agree": agree.value, "max_dconf": dconf.value}
 
     def free(self):
         if self.h:

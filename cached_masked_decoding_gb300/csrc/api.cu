@@ -529,6 +529,11 @@ struct dllm_state {
   int map_kv = 0;
   StepPhase* d_phases = nullptr;  // [n_blocks][n_phases]
   CUtensorMap* d_maps = nullptr;
+  // staleness diagnostics (allocated on first use)
+  uint16_t* kv_fresh = nullptr;   // K/V of a full forward over the current canvas, the cache's layout
+  CUtensorMap tm_kv_fresh;
+  int32_t* x_save = nullptr;      // canvas saved around the diagnostic forwards
+  float* row_cos = nullptr;       // [L][K|V][b][H][T] cosine of cached and fresh rows
   int* d_flags = nullptr;         // dataflow flags of the persistent step, zeroed per launch
   int n_flags = 0;
   AttnPlan step_attn = {};
@@ -548,6 +553,9 @@ dllm_status state_free_device(dllm_state* s) {
   if (s->d_flags) cudaFree(s->d_flags);
   if (s->d_timeline) cudaFree(s->d_timeline);
   if (s->host_ce) cudaFreeHost(s->host_ce);
+  if (s->kv_fresh) cudaFree(s->kv_fresh);
+  if (s->x_save) cudaFree(s->x_save);
+  if (s->row_cos) cudaFree(s->row_cos);
   for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
   if (s->ev_a) cudaEventDestroy(s->ev_a);
   if (s->ev_b) cudaEventDestroy(s->ev_b);
@@ -2050,6 +2058,143 @@ extern "C" dllm_status dllm_op_select_commit(const float* conf, const int32_t* a
   SelectParams p{conf, arg, x, count, T, blk_start, B, mask_id, r};
   select_kernel<<<b, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
   CK(cudaGetLastError());
+  return DLLM_OK;
+}
+
+// ====================================================================== staleness diagnostics
+namespace {
+
+// Cosine of each cached K/V row (hi + lo) with the same row of a fresh full
+// forward: one warp per row of head_dim elements, lanes summing in a fixed
+// order.  rows = L * 2 * b * H * T; parts = 2 when the low halves are kept.
+__global__ void kv_cosine_kernel(const uint16_t* cached, const uint16_t* fresh, float* out, long long rows, int hd,
+                                 long long part_rows, int parts) {
+  const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  // row -> (layer*2 + kind, rest): the hi plane block of that (layer, kind), then
+  // the lo plane block part_rows rows later (the cache always has both)
+  const long long lk = row / part_rows, rest = row - lk * part_rows;
+  const long long hi_row = lk * 2 * part_rows + rest;
+  float dot = 0.0f, nc = 0.0f, nf = 0.0f;
+  for (int e = lane; e < hd; e += 32) {
+    float c = __uint_as_float((uint32_t)cached[hi_row * hd + e] << 16);
+    float f = __uint_as_float((uint32_t)fresh[hi_row * hd + e] << 16);
+    if (parts == 2) {
+      c += __uint_as_float((uint32_t)cached[(hi_row + part_rows) * hd + e] << 16);
+      f += __uint_as_float((uint32_t)fresh[(hi_row + part_rows) * hd + e] << 16);
+    }
+    dot = fmaf(c, f, dot);
+    nc = fmaf(c, c, nc);
+    nf = fmaf(f, f, nf);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    nc += __shfl_xor_sync(0xffffffffu, nc, o);
+    nf += __shfl_xor_sync(0xffffffffu, nf, o);
+  }
+  if (lane == 0) out[row] = (nc > 0.0f && nf > 0.0f) ? dot / sqrtf(nc * nf) : 1.0f;
+}
+
+// The block forward (DualCache rows) on the current cache, predictions only:
+// the canvas is restored afterwards.
+dllm_status block_predict(dllm_state* s, int j, std::vector<float>& conf, std::vector<int32_t>& arg) {
+  const int blk = s->P + j * s->B;
+  const size_t nb = (size_t)s->b * s->T;
+  CK(cudaMemcpyAsync(s->x_save, s->x, nb * 4, cudaMemcpyDeviceToDevice, s->st));
+  CK(cudaMemsetAsync(s->count_err, 0, (s->b + 1) * 4, s->st));
+  SelectRule keep_all{1, 0.0f, kMaxBlock, 1.0f};
+  CKS(run_forward(s, blk, s->B, false, blk, keep_all));
+  CKS(finish_sync(s));
+  conf.resize((size_t)s->b * s->B);
+  arg.resize((size_t)s->b * s->B);
+  CK(cudaMemcpy(conf.data(), s->conf, conf.size() * 4, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(arg.data(), s->arg, arg.size() * 4, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpyAsync(s->x, s->x_save, nb * 4, cudaMemcpyDeviceToDevice, s->st));
+  CK(cudaStreamSynchronize(s->st));
+  return DLLM_OK;
+}
+
+}  // namespace
+
+extern "C" dllm_status dllm_staleness(dllm_state* s, int32_t block_idx, float* k_cos, float* v_cos, float* agree,
+                                      float* max_dconf) {
+  if (!s || block_idx < 0 || block_idx >= s->n_blocks || !k_cos || !v_cos || !agree || !max_dconf) {
+    set_error("bad staleness arguments (block %d)", block_idx);
+    return DLLM_EINVAL;
+  }
+  const dllm_config& c = s->m->cfg;
+  const int L = c.n_layers, H = c.n_heads, hd = c.head_dim;
+  const size_t plane = (size_t)s->b * H * s->T * hd;          // elements of one (layer, kind, part) block
+  const size_t kv_elems = (size_t)L * 4 * plane;
+  const long long rows = (long long)L * 2 * s->b * H * s->T;
+  if (!s->kv_fresh) {
+    CKS(dev_alloc((void**)&s->kv_fresh, kv_elems * 2));
+    CKS(dev_alloc((void**)&s->x_save, (size_t)s->b * s->T * 4));
+    CKS(dev_alloc((void**)&s->row_cos, (size_t)rows * 4));
+    CKS(map_kv(&s->tm_kv_fresh, s->kv_fresh, hd, s->T, (uint64_t)L * 4 * s->b * H, kStateAttnKT));
+  }
+  // the cache's own prediction for block j
+  std::vector<float> conf_c, conf_f;
+  std::vector<int32_t> arg_c, arg_f;
+  CKS(block_predict(s, block_idx, conf_c, arg_c));
+  // a fresh full forward over the current canvas into the scratch K/V, and
+  // the block's prediction from it (= the prediction without a cache)
+  std::swap(s->kv, s->kv_fresh);
+  std::swap(s->tm_kv, s->tm_kv_fresh);
+  dllm_status st = DLLM_OK;
+  {
+    SelectRule none{0, 2.0f, 1, 1.0f};
+    CK(cudaMemsetAsync(s->count_err, 0, (s->b + 1) * 4, s->st));
+    st = run_forward(s, 0, s->T, true, 0, none);
+    if (st == DLLM_OK) st = finish_sync(s);
+    if (st == DLLM_OK) st = block_predict(s, block_idx, conf_f, arg_f);
+  }
+  std::swap(s->kv, s->kv_fresh);
+  std::swap(s->tm_kv, s->tm_kv_fresh);
+  CKS(st);
+  // cosines of cached and fresh rows; the fresh block rows were recomputed by
+  // the block forward into the scratch, so they match the block step's
+  const int parts = s->split ? 2 : 1;
+  const long long part_rows = (long long)s->b * H * s->T;
+  const int warps = 8;
+  kv_cosine_kernel<<<(unsigned)((rows + warps - 1) / warps), warps * 32, 0, s->st>>>(
+      s->kv, s->kv_fresh, s->row_cos, rows, hd, part_rows, parts);
+  CK(cudaGetLastError());
+  std::vector<float> cosv((size_t)rows);
+  CK(cudaMemcpyAsync(cosv.data(), s->row_cos, cosv.size() * 4, cudaMemcpyDeviceToHost, s->st));
+  CK(cudaStreamSynchronize(s->st));
+  const int blk = s->P + block_idx * s->B;
+  for (int l = 0; l < L; ++l) {
+    for (int kind = 0; kind < 2; ++kind) {
+      double sum = 0.0;
+      long long n = 0;
+      for (int i = 0; i < s->b; ++i)
+        for (int h = 0; h < H; ++h)
+          for (int t = 0; t < s->T; ++t) {
+            if (t >= blk && t < blk + s->B) continue;   // the block's own rows are recomputed every step
+            sum += cosv[(((size_t)(l * 2 + kind) * s->b + i) * H + h) * s->T + t];
+            ++n;
+          }
+      (kind == 0 ? k_cos : v_cos)[l] = n ? (float)(sum / n) : 1.0f;
+    }
+  }
+  // agreement at the block's MASK positions
+  std::vector<int32_t> x((size_t)s->b * s->T);
+  CK(cudaMemcpy(x.data(), s->x, x.size() * 4, cudaMemcpyDeviceToHost));
+  long long same = 0, total = 0;
+  float dmax = 0.0f;
+  for (int i = 0; i < s->b; ++i)
+    for (int k = 0; k < s->B; ++k) {
+      if (x[(size_t)i * s->T + blk + k] != c.vocab) continue;
+      const size_t o = (size_t)i * s->B + k;
+      same += arg_c[o] == arg_f[o];
+      ++total;
+      dmax = std::max(dmax, std::fabs(conf_c[o] - conf_f[o]));
+    }
+  *agree = total ? (float)same / (float)total : 1.0f;
+  *max_dconf = dmax;
   return DLLM_OK;
 }
 

@@ -336,6 +336,26 @@ dllm_status dllm_op_select_commit(const float* conf, const int32_t* arg, int32_t
                                   int32_t mask_id, const dllm_select* sel, int32_t* count,
                                   void* cuda_stream);
 
+/* Cache staleness diagnostics for block block_idx of the current canvas (the
+ * Fast-dLLM notes, section 14, Algorithm 4 steps 4-5: compare fresh and
+ * cached representations and predictions at the positions about to be
+ * committed; the notes' section 3 on what DualCache freezes).  Without
+ * changing the canvas or the cache's prefix/suffix rows it runs a full
+ * forward over all T positions of the current canvas into a scratch K/V
+ * ("fresh") and the block forward twice, on the cache and on the fresh K/V,
+ * and returns (host outputs):
+ *   k_cos[l], v_cos[l]  float32 [n_layers]: the mean over sequences, heads
+ *                       and every position outside the block of the cosine
+ *                       between the cached and the fresh K (V) row;
+ *   agree               the fraction of the block's MASK positions whose
+ *                       argmax is the same from both;
+ *   max_dconf           the largest |max-prob(cached) - max-prob(fresh)| there.
+ * The block's own K/V rows in the cache are rewritten with the current
+ * canvas's (as the next step would).  Allocates a second K/V of the cache's
+ * size on first use.  DLLM_EINVAL for a bad block or NULL output. */
+dllm_status dllm_staleness(dllm_state* s, int32_t block_idx, float* k_cos, float* v_cos, float* agree,
+                           float* max_dconf);
+
 /* ------------------------------------------------------------------ misc */
 
 const char* dllm_last_error(void);

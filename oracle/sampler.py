@@ -24,6 +24,9 @@ Passages followed (zhongzhuzhou.org Fast-dLLM reading notes unless noted):
 * ``select_fixed_k`` - the fixed-count rule (page 1, opening paragraph: a fixed
   number of tokens per step; LLaDA's low-confidence remasking keeps the most
   confident predictions).
+* ``staleness`` - Algorithm 4 of the notes (section 14), steps 4-5: fresh
+  versus cached K/V rows (cosine per layer) and predictions (argmax
+  agreement, max-prob difference) for the current block.
 * ``llada_sample`` - page 1's LLaDA sampler (section "what one step does"): a
   full bidirectional forward each step, n_keep = len(masked) // (steps - k) most
   confident masked positions committed, never changed afterwards.
@@ -257,6 +260,42 @@ class Decoder:
             if cached and j < self.n_blocks - 1:
                 self.refresh()
         return self.x[:, self.P:].copy(), trace
+
+
+def staleness(dec: Decoder, j: int) -> dict:
+    """Fresh versus cached representations and predictions for block j of the
+    current canvas (zhongzhuzhou.org notes, section 14, Algorithm 4 steps 4-5;
+    section 3 on what DualCache freezes between refreshes).
+
+    fresh: the K/V a full forward over the current canvas would cache.
+    k_cos[l], v_cos[l]: mean over sequences, heads and the positions outside
+    the block of cos(cached row, fresh row).  agree: fraction of the block's
+    MASK positions whose argmax from the cache equals the argmax without a
+    cache; max_dconf: the largest max-prob difference there.
+    """
+    cfg = dec.cfg
+    s = dec.block_start(j)
+    L, T = cfg.n_layers, dec.T
+    outside = np.ones(T, dtype=bool)
+    outside[s:s + dec.B] = False
+    sums = np.zeros((2, L))
+    count = 0
+    for i in range(dec.b):
+        fw = M.forward_rows(dec.w, dec.x[i], np.arange(T), None, None, skip_last_post_attn=True)
+        for kind, (cached, fresh) in enumerate(((dec.k_cache[i], fw.k), (dec.v_cache[i], fw.v))):
+            for l in range(L):
+                c, f = cached[l][outside], fresh[l][outside]          # [positions, H, hd]
+                cos = (c * f).sum(-1) / np.sqrt((c * c).sum(-1) * (f * f).sum(-1))
+                sums[kind, l] += cos.sum()
+        count += int(outside.sum()) * cfg.n_heads
+    conf_c, arg_c, _, _, _ = dec.compute(j)
+    none = Decoder(dec.w, dec.x[:, :dec.P], dec.gen, dec.B, "none")
+    none.x = dec.x.copy()
+    conf_f, arg_f, _, _, _ = none.compute(j)
+    elig = dec.eligible(j)
+    agree = float((arg_c == arg_f)[elig].mean()) if elig.any() else 1.0
+    dconf = float(np.abs(conf_c - conf_f)[elig].max()) if elig.any() else 0.0
+    return {"k_cos": sums[0] / count, "v_cos": sums[1] / count, "agree": agree, "max_dconf": dconf}
 
 
 def tau_bar(trace, b: int) -> np.ndarray:

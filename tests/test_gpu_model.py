@@ -303,3 +303,32 @@ def test_weight_file_round_trip(tmp_path, gmodel, torch):
     b, _ = binding.generate(m2, pr, 32, 16, 0.9, "dual")
     np.testing.assert_array_equal(a, b)
     m2.free()
+
+
+def test_staleness_matches_oracle(gmodel, omodel):
+    """The staleness diagnostic (fresh versus cached K/V and predictions) on
+    the GPU against the oracle's, on the GPU's canvas after two DualCache
+    steps; right after the refresh every cosine is 1."""
+    P, gen, B = 32, 64, 16
+    pr = synth.prompts(CFG, 1, 2, P)
+    st = binding.State(gmodel, pr, 2, P, gen, B)
+    st.refresh()
+    fresh = st.staleness(0)
+    np.testing.assert_allclose(fresh["k_cos"], 1.0, atol=1e-6)
+    np.testing.assert_allclose(fresh["v_cos"], 1.0, atol=1e-6)
+    assert fresh["agree"] == 1.0 and fresh["max_dconf"] == 0.0
+    dec = OS.Decoder(omodel, pr, gen, B, "dual")
+    dec.refresh()
+    for _ in range(2):
+        st.step_ex(0, binding.make_select(binding.SEL_FIXED_K, k=3), "dual")
+    dec.x = st.tokens().astype(np.int64)
+    got = st.staleness(0)
+    ref = OS.staleness(dec, 0)
+    print({k: (got[k], ref[k]) for k in ("agree", "max_dconf")})
+    np.testing.assert_allclose(got["k_cos"], ref["k_cos"], atol=2e-5)
+    np.testing.assert_allclose(got["v_cos"], ref["v_cos"], atol=2e-5)
+    assert abs(got["max_dconf"] - ref["max_dconf"]) <= 2 * conf_tol(CFG)
+    assert abs(got["agree"] - ref["agree"]) <= 1.0 / 32 + 1e-9   # one near tie at most
+    # the diagnostic leaves the canvas alone
+    np.testing.assert_array_equal(st.tokens(), dec.x)
+    st.free()

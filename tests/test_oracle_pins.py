@@ -402,6 +402,35 @@ def test_schedule_rule_is_llada_sampler(tiny_w, steps):
     np.testing.assert_array_equal(toks[0], S.llada_sample(tiny_w, pr[0], gen, steps))
 
 
+def test_staleness_zero_right_after_refresh(tiny_w):
+    """Right after a refresh the cache is the fresh forward: every cosine is 1
+    and the cached and uncached predictions are the same."""
+    pr = synth.prompts(tiny_w.cfg, 0, 2, 12)
+    dec = S.Decoder(tiny_w, pr, 16, 8, "dual")
+    dec.refresh()
+    st = S.staleness(dec, 0)
+    np.testing.assert_allclose(st["k_cos"], 1.0, atol=1e-12)
+    np.testing.assert_allclose(st["v_cos"], 1.0, atol=1e-12)
+    assert st["agree"] == 1.0 and st["max_dconf"] < 1e-12
+
+
+def test_staleness_after_commits(tiny_w):
+    """After two steps inside block 0 the prefix/suffix rows of layer 0 are
+    still exact (layer-0 K/V of a position depend on its own token alone), the
+    deeper layers' rows have gone stale (cosine below 1, the attention mixes
+    in the newly committed tokens), and everything stays a cosine."""
+    pr = synth.prompts(tiny_w.cfg, 0, 1, 12)
+    dec = S.Decoder(tiny_w, pr, 16, 8, "dual")
+    dec.refresh()
+    dec.step(0, S.Rule(S.FIXED_K, k=3))
+    dec.step(0, S.Rule(S.FIXED_K, k=3))
+    st = S.staleness(dec, 0)
+    np.testing.assert_allclose(st["k_cos"][0], 1.0, atol=1e-12)
+    np.testing.assert_allclose(st["v_cos"][0], 1.0, atol=1e-12)
+    assert (st["k_cos"][1:] < 1.0 - 1e-9).all() and (st["v_cos"][1:] < 1.0 - 1e-9).all()
+    assert (st["k_cos"] > 0.0).all() and 0.0 <= st["agree"] <= 1.0
+
+
 @pytest.mark.parametrize("mode", ["prefix", "dual"])
 def test_refresh_every_step_equals_no_cache(tiny_w, mode):
     _, t_none, tr_none = _run(tiny_w, "none", S.Rule(S.THRESHOLD, 0.9), b=2)
