@@ -538,6 +538,7 @@ struct dllm_state {
   int n_flags = 0;
   AttnPlan step_attn = {};
   int step_prefetch = 1 << 20;                // weight tiles loaded ahead of a phase barrier (ring depth cap)
+  bool block_causal = false;                  // DLLM_MASK_BLOCK_CAUSAL
   unsigned long long* d_timeline = nullptr;   // persistent-step phase timeline (diagnostics)
   bool timeline = false;
 };
@@ -932,6 +933,9 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
   p.q_tiles = a.q_tiles;
   p.splits = a.splits;
   p.kps = a.kps;
+  p.row0 = s->last_row0;
+  p.mask_P = s->P;
+  p.mask_B = s->block_causal ? s->B : 0;
   p.scale_log2 = kLog2e / std::sqrt((float)c.head_dim);
   p.ws_o = s->attn_o;
   p.ws_ml = s->attn_o + works * a.splits * QT * c.head_dim;
@@ -1375,6 +1379,9 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
   a.attn.b = s->b;
   a.attn.H = c.n_heads;
   a.attn.T = s->T;
+  a.attn.row0 = blk;
+  a.attn.mask_P = s->P;
+  a.attn.mask_B = s->block_causal ? s->B : 0;
   a.attn.q_tiles = ap.q_tiles;
   a.attn.splits = ap.splits;
   a.attn.kps = ap.kps;
@@ -1597,7 +1604,25 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
       active += act;
     }
     max_spb = std::max(max_spb, spb);
-    if (cached && j + 1 < s->n_blocks) CKS(timed_refresh());
+    if (cached && j + 1 < s->n_blocks) {
+      if (s->block_causal) {
+        // nothing earlier attends to a later block: caching the finished
+        // block's own K/V (one block forward) makes the cache exact again
+        CK(cudaEventRecord(s->ev_a, s->st));
+        CK(cudaMemsetAsync(s->count_err + s->b, 0, 4, s->st));
+        SelectRule none{0, 2.0f, 1, 1.0f};
+        const int blk = s->P + j * s->B;
+        CKS(run_forward(s, blk, s->B, true, blk, none));
+        CK(cudaEventRecord(s->ev_b, s->st));
+        CKS(finish_sync(s));
+        float ms = 0;
+        CK(cudaEventElapsedTime(&ms, s->ev_a, s->ev_b));
+        refresh_ms += ms;
+        ++refreshes;
+      } else {
+        CKS(timed_refresh());
+      }
+    }
   }
   if (stats) {
     stats->wall_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
@@ -1704,6 +1729,15 @@ extern "C" dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode) {
     return DLLM_EINVAL;
   }
   s->split = mode == DLLM_PREC_SPLIT;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_mask(dllm_state* s, int32_t mask) {
+  if (!s || (mask != DLLM_MASK_BIDIRECTIONAL && mask != DLLM_MASK_BLOCK_CAUSAL)) {
+    set_error("bad attention mask %d", mask);
+    return DLLM_EINVAL;
+  }
+  s->block_causal = mask == DLLM_MASK_BLOCK_CAUSAL;
   return DLLM_OK;
 }
 

@@ -19,6 +19,8 @@
 // cached K/V moves final hidden states by a few 1e-3 relative.
 #pragma once
 
+#include <climits>
+
 #include "ptx.cuh"
 
 namespace dllm {
@@ -32,6 +34,10 @@ struct AttnParams {
   int z_k0, z_v0;      // plane of (seq 0, head 0) in the K and V maps; plane = z0 + seq*H + head
   int z_kl0, z_vl0;    // the same for the low halves of K and V (kv_lo = 1)
   int kv_lo;           // 1: split-precision q, K, V and P
+  // block-causal mask (mask_B > 0): the query at position p = row0 + row sees
+  // keys below p's block end: mask_P for prompt positions (p < mask_P), else
+  // mask_P + ((p - mask_P) / mask_B + 1) * mask_B.  mask_B = 0: every key.
+  int row0, mask_P, mask_B;
   int q_tiles, splits, kps;  // query tiles per (seq, head), key splits, keys per split (multiple of 64)
   float scale_log2;    // log2(e) / sqrt(HD)
   float* ws_o;         // [works][splits][QT][HD]
@@ -119,8 +125,20 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
   const int wq = warp % WQ, wk = warp / WQ;
   const int g = lane >> 2, t4 = lane & 3;
   const int k_beg = split * p.kps;
-  const int k_end = min(p.T, k_beg + p.kps);
-  const int ntiles = (k_end - k_beg + KT - 1) / KT;
+  int k_end = min(p.T, k_beg + p.kps);
+  int lim_lo = INT_MAX, lim_hi = INT_MAX;   // key limits of this thread's two query rows
+  if (p.mask_B > 0) {
+    auto key_limit = [&](int row) {
+      const int pos = p.row0 + row;
+      return pos < p.mask_P ? p.mask_P : p.mask_P + ((pos - p.mask_P) / p.mask_B + 1) * p.mask_B;
+    };
+    const int qr = qt * QT + wq * 16 + g;
+    lim_lo = key_limit(qr);
+    lim_hi = key_limit(qr + 8);
+    // limits grow with position: the tile's last row bounds the keys to visit
+    k_end = min(k_end, key_limit(min(qt * QT + QT, p.R) - 1));
+  }
+  const int ntiles = k_end > k_beg ? (k_end - k_beg + KT - 1) / KT : 0;
   const int zk = p.z_k0 + seq * p.H + head, zv = p.z_v0 + seq * p.H + head;
   const int zkl = p.z_kl0 + seq * p.H + head, zvl = p.z_vl0 + seq * p.H + head;
   const bool lo = KT == 32 && p.kv_lo != 0;   // 64-key tiles are bf16 only (no room for the low halves)
@@ -221,9 +239,9 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int key = key_base + nt * 8 + 2 * t4 + e;
-          const bool ok = key < k_end;
-          sacc[nt][e] = ok ? sacc[nt][e] * p.scale_log2 : -INFINITY;
-          sacc[nt][2 + e] = ok ? sacc[nt][2 + e] * p.scale_log2 : -INFINITY;
+          const bool ok_lo = key < k_end && key < lim_lo, ok_hi = key < k_end && key < lim_hi;
+          sacc[nt][e] = ok_lo ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+          sacc[nt][2 + e] = ok_hi ? sacc[nt][2 + e] * p.scale_log2 : -INFINITY;
           mx_lo = fmaxf(mx_lo, sacc[nt][e]);
           mx_hi = fmaxf(mx_hi, sacc[nt][2 + e]);
         }

@@ -228,6 +228,20 @@ dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode);
  * attention key split; tracing always uses it). */
 dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable);
 
+/* Attention mask.  DLLM_MASK_BIDIRECTIONAL (default): every position sees
+ * every position, the Fast-dLLM setting, in which the cached prefix and
+ * suffix go stale and a block-boundary refresh recomputes them.
+ * DLLM_MASK_BLOCK_CAUSAL: a prompt position sees the prompt, a position of
+ * answer block j the prompt and blocks 0..j (block diffusion, BD3-LM style,
+ * which the tutorial's section on caches and the dian8dian summary name as
+ * the exact-cache alternative).  Nothing then attends to a later block, the
+ * cache never goes stale, PrefixCache and DualCache compute the same as no
+ * cache, and dllm_run replaces each block-boundary refresh by one forward
+ * over the finished block's rows that caches their K/V.  Set before
+ * dllm_prefill_refresh.  DLLM_EINVAL for another value. */
+typedef enum dllm_mask { DLLM_MASK_BIDIRECTIONAL = 0, DLLM_MASK_BLOCK_CAUSAL = 1 } dllm_mask;
+dllm_status dllm_state_set_mask(dllm_state* s, int32_t mask);
+
 /* Diagnostics of the persistent step: with enable 1 the next persistent steps
  * record, per CTA and phase, 10 %globaltimer nanosecond stamps (uint64
  * [ctas][phases][10]): 0 the CTA's workers finished the phase, 1 its TMA

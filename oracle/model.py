@@ -97,10 +97,14 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
-def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
-    """Non-causal multi-head attention, eq. 3. q: [n, H, hd]; k, v: [T, H, hd]."""
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, key_limit: np.ndarray | None = None) -> np.ndarray:
+    """Non-causal multi-head attention, eq. 3. q: [n, H, hd]; k, v: [T, H, hd].
+    key_limit (optional, [n]): query i sees keys t < key_limit[i] only."""
     hd = q.shape[-1]
     s = np.einsum("nhd,thd->hnt", q, k) / np.sqrt(hd)
+    if key_limit is not None:
+        hidden = np.arange(k.shape[0])[None, :] >= np.asarray(key_limit)[:, None]   # [n, T]
+        s = np.where(hidden[None], -np.inf, s)
     s = s - s.max(axis=-1, keepdims=True)
     p = np.exp(s)
     p = p / p.sum(axis=-1, keepdims=True)
@@ -127,10 +131,18 @@ def qkv(cfg: ModelConfig, lw: LayerWeights, h: np.ndarray, pos: np.ndarray):
     return q, k, v
 
 
+def block_key_limit(pos: np.ndarray, prompt_len: int, block: int) -> np.ndarray:
+    """Block-causal visibility (BD3-LM style, the tutorial's section on caches;
+    the dian8dian summary on block diffusion): a prompt position sees the
+    prompt, a position of answer block j sees the prompt and blocks 0..j."""
+    pos = np.asarray(pos)
+    return np.where(pos < prompt_len, prompt_len, prompt_len + ((pos - prompt_len) // block + 1) * block)
+
+
 def attn_ffn(cfg: ModelConfig, lw: LayerWeights, h: np.ndarray, q: np.ndarray,
-             k_all: np.ndarray, v_all: np.ndarray) -> np.ndarray:
+             k_all: np.ndarray, v_all: np.ndarray, key_limit: np.ndarray | None = None) -> np.ndarray:
     """h += W_o Attn(q, K, V); h += SwiGLU(RMSNorm(h))."""
-    o = attention(q, k_all, v_all).reshape(h.shape[0], cfg.d_model)
+    o = attention(q, k_all, v_all, key_limit).reshape(h.shape[0], cfg.d_model)
     h = h + o @ lw.wo.T
     x = rms_norm(h, lw.ffn_norm, cfg.norm_eps)
     return h + swiglu(x, lw.wg, lw.wu, lw.wd)
@@ -146,7 +158,7 @@ class RowsForward:
 
 def forward_rows(w: Weights, tokens: np.ndarray, rows: np.ndarray,
                  k_ctx: list | None, v_ctx: list | None, keep_layers: bool = False,
-                 skip_last_post_attn: bool = False) -> RowsForward:
+                 skip_last_post_attn: bool = False, key_limit: np.ndarray | None = None) -> RowsForward:
     """Run the layer stack over the positions ``rows`` of one sequence.
 
     ``tokens`` is the whole canvas [T]; the K/V of the other positions come from
@@ -176,7 +188,7 @@ def forward_rows(w: Weights, tokens: np.ndarray, rows: np.ndarray,
         vs.append(v_all)
         if skip_last_post_attn and l == cfg.n_layers - 1:
             break
-        h = attn_ffn(cfg, lw, h, q, k_all, v_all)
+        h = attn_ffn(cfg, lw, h, q, k_all, v_all, key_limit)
         if keep_layers:
             hl.append(h.copy())
     return RowsForward(h_final=h, k=ks, v=vs, h_layers=hl)

@@ -157,9 +157,13 @@ class StepOut:
 class Decoder:
     """Lockstep batch decoder following Algorithm 1 with one of three cache modes."""
 
-    def __init__(self, w: M.Weights, prompts: np.ndarray, gen_len: int, block: int, mode: str):
+    def __init__(self, w: M.Weights, prompts: np.ndarray, gen_len: int, block: int, mode: str,
+                 mask: str = "full"):
         if mode not in ("none", "prefix", "dual"):
             raise ValueError(mode)
+        if mask not in ("full", "block_causal"):
+            raise ValueError(mask)
+        self.mask = mask
         if gen_len % block != 0:
             raise ValueError("gen_len must be a multiple of block")
         self.w = w
@@ -187,10 +191,17 @@ class Decoder:
         """Full-sequence forward that rewrites every cached K/V (Algorithm 1, steps 2 and 11)."""
         rows = np.arange(self.T)
         for i in range(self.b):
-            fw = M.forward_rows(self.w, self.x[i], rows, None, None, skip_last_post_attn=True)
+            fw = M.forward_rows(self.w, self.x[i], rows, None, None, skip_last_post_attn=True,
+                                key_limit=self.key_limit(rows))
             self.k_cache[i] = fw.k
             self.v_cache[i] = fw.v
         self.refreshes += 1
+
+    def key_limit(self, rows: np.ndarray):
+        """Per-row key limits of the block-causal mask, or None (bidirectional)."""
+        if self.mask == "full":
+            return None
+        return M.block_key_limit(rows, self.P, self.B)
 
     def rows_of(self, j: int) -> np.ndarray:
         s = self.block_start(j)
@@ -211,10 +222,11 @@ class Decoder:
         layers = []
         for i in range(self.b):
             if self.mode == "none":
-                fw = M.forward_rows(self.w, self.x[i], rows, None, None, keep_layers=keep_layers)
+                fw = M.forward_rows(self.w, self.x[i], rows, None, None, keep_layers=keep_layers,
+                                    key_limit=self.key_limit(rows))
             else:
                 fw = M.forward_rows(self.w, self.x[i], rows, self.k_cache[i], self.v_cache[i],
-                                    keep_layers=keep_layers)
+                                    keep_layers=keep_layers, key_limit=self.key_limit(rows))
             sel = (rows >= s) & (rows < s + self.B)
             hs = fw.h_final[sel]
             st = M.lm_head(self.w, hs)

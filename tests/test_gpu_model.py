@@ -332,3 +332,36 @@ def test_staleness_matches_oracle(gmodel, omodel):
     # the diagnostic leaves the canvas alone
     np.testing.assert_array_equal(st.tokens(), dec.x)
     st.free()
+
+
+@pytest.mark.parametrize("mode", ["dual", "prefix", "none"])
+def test_block_causal_trajectory_matches_oracle(gmodel, omodel, mode):
+    """The block-causal attention mask on the GPU (per-row key limits in the
+    attention kernels) against the oracle with the same mask, step by step."""
+    P, gen, B = 32, 48, 16
+    pr = synth.prompts(CFG, 6, 1, P)
+    st = binding.State(gmodel, pr, 1, P, gen, B)
+    st.set_mask("block_causal")
+    dec = OS.Decoder(omodel, pr, gen, B, mode, mask="block_causal")
+    rep = run_synced(st, dec, RULES["threshold"], mode)
+    print(mode, rep)
+    assert (st.tokens()[:, P:] != CFG.mask_id).all()
+    st.free()
+
+
+def test_block_causal_commit_forward_keeps_cache_exact(gmodel, omodel):
+    """With the block-causal mask dllm_run replaces each block-boundary refresh
+    by one forward over the finished block; the cache stays exact, so the
+    DualCache run (persistent step) decodes what the oracle's no-cache decoder
+    does under the same mask."""
+    P, gen, B = 32, 64, 16
+    pr = synth.prompts(CFG, 7, 2, P)
+    st = binding.State(gmodel, pr, 2, P, gen, B)
+    st.set_mask("block_causal")
+    stats = st.run(binding.make_select(binding.SEL_THRESHOLD, 0.9), "dual")
+    assert stats["refreshes"] == gen // B       # the prefill plus one commit forward per finished block but the last
+    ref = OS.Decoder(omodel, pr, gen, B, "none", mask="block_causal")
+    toks, _ = ref.generate(OS.Rule(OS.THRESHOLD, 0.9))
+    got = st.tokens()[:, P:]
+    assert (got == toks).mean() > 0.95, f"agreement {(got == toks).mean():.3f}"
+    st.free()

@@ -402,6 +402,47 @@ def test_schedule_rule_is_llada_sampler(tiny_w, steps):
     np.testing.assert_array_equal(toks[0], S.llada_sample(tiny_w, pr[0], gen, steps))
 
 
+def test_attention_key_limit_closed_forms():
+    """A key limit of T is the unmasked attention; a limit of 1 returns v[0]."""
+    rng = np.random.default_rng(4)
+    q, k, v = rng.standard_normal((5, 2, 8)), rng.standard_normal((7, 2, 8)), rng.standard_normal((7, 2, 8))
+    np.testing.assert_allclose(M.attention(q, k, v, np.full(5, 7)), M.attention(q, k, v), atol=1e-14)
+    np.testing.assert_allclose(M.attention(q, k, v, np.ones(5, dtype=int)), np.broadcast_to(v[0], (5, 2, 8)),
+                               atol=1e-14)
+
+
+def test_block_key_limit():
+    np.testing.assert_array_equal(M.block_key_limit(np.arange(12), 4, 3), [4, 4, 4, 4, 7, 7, 7, 10, 10, 10, 13, 13])
+
+
+@pytest.mark.parametrize("mode", ["dual", "prefix"])
+def test_block_causal_cache_is_exact(tiny_w, mode):
+    """Under the block-causal mask nothing a block attends to changes after it
+    is cached: the cached decoders reproduce the no-cache decoder exactly, with
+    the same confidences at every step."""
+    pr = synth.prompts(tiny_w.cfg, 2, 2, 12)
+    ref = S.Decoder(tiny_w, pr, 24, 8, "none", mask="block_causal")
+    t_ref, tr_ref = ref.generate(S.Rule(S.THRESHOLD, 0.9))
+    dec = S.Decoder(tiny_w, pr, 24, 8, mode, mask="block_causal")
+    t, tr = dec.generate(S.Rule(S.THRESHOLD, 0.9))
+    np.testing.assert_array_equal(t, t_ref)
+    assert len(tr) == len(tr_ref)
+    for a, b in zip(tr, tr_ref):
+        np.testing.assert_allclose(a.conf, b.conf, atol=1e-12)
+
+
+def test_block_causal_prompt_ignores_answer(tiny_w):
+    """A prompt row under the block-causal mask sees the prompt only: its K/V
+    are those of a forward over the prompt alone."""
+    pr = synth.prompts(tiny_w.cfg, 1, 1, 10)
+    dec = S.Decoder(tiny_w, pr, 16, 8, "dual", mask="block_causal")
+    dec.refresh()
+    alone = M.forward_rows(tiny_w, pr[0], np.arange(10), None, None, skip_last_post_attn=True)
+    for l in range(tiny_w.cfg.n_layers):
+        np.testing.assert_allclose(dec.k_cache[0][l][:10], alone.k[l], atol=1e-12)
+        np.testing.assert_allclose(dec.v_cache[0][l][:10], alone.v[l], atol=1e-12)
+
+
 def test_staleness_zero_right_after_refresh(tiny_w):
     """Right after a refresh the cache is the fresh forward: every cosine is 1
     and the cached and uncached predictions are the same."""
