@@ -220,6 +220,7 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     state = binding.State(model, None, b, P, gen, B, stream=stream.cuda_stream)
     state.set_precision(args.precision)
     state.set_persistent(args.persistent)
+    state.set_mask(args.mask)
     sel = binding.make_select(binding.SEL_THRESHOLD, wl.tau)
     mode = args.mode
 
@@ -313,6 +314,7 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
             "model": f"{cfg.n_layers}L d{cfg.d_model} H{cfg.n_heads} F{cfg.d_ffn} V{cfg.vocab} (random init)",
             "global_batch": sh.global_batch, "seq_len": wl.T, "block": B, "tau": wl.tau, "cache_mode": mode,
             "precision": f"{args.precision} activations, bf16 weights and K/V, f32 accumulate",
+            "mask": "bidirectional" if args.mask == "full" else "block-causal (refresh = one block forward)",
             "step_launch": "persistent (one cooperative launch per denoise step)" if args.persistent
             else "one launch per kernel",
             "l2": "inputs larger than L2 (every step streams all weights)",
@@ -414,6 +416,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (profiling captures of a small case)")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--mask", default="full", choices=("full", "block_causal"),
+                    help="attention mask: bidirectional (the method's) or block-causal (exact cache)")
     ap.add_argument("--no-persistent", dest="persistent", action="store_false",
                     help="one launch per kernel instead of the persistent DualCache step")
     args = ap.parse_args()
