@@ -537,7 +537,10 @@ struct dllm_state {
   int* d_flags = nullptr;         // dataflow flags of the persistent step, zeroed per launch
   int n_flags = 0;
   AttnPlan step_attn = {};
-  int step_prefetch = 1 << 20;                // weight tiles loaded ahead of a phase barrier (ring depth cap)
+  // weight tiles a CTA loads for a phase before its inputs are ready: 4 of
+  // the 8 ring slots (8B workload, batch 1: 4.004 ms per step against 4.030
+  // with the whole ring; fewer loads queued when the phase tail runs)
+  int step_prefetch = 4;
   bool block_causal = false;                  // DLLM_MASK_BLOCK_CAUSAL
   unsigned long long* d_timeline = nullptr;   // persistent-step phase timeline (diagnostics)
   bool timeline = false;
