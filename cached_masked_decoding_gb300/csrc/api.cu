@@ -503,6 +503,7 @@ struct dllm_state {
   int32_t* host_ce = nullptr;     // pinned copy of count_err
   CUtensorMap tm_kv;
   std::map<std::tuple<const void*, int, int, int>, CUtensorMap> act_maps;
+  std::map<const void*, CUtensorMap> kv64_maps;   // 64-key K/V maps of the tensor-core attention, per cache buffer
   std::vector<int32_t> prompts;   // host copy of the prompt part
   std::vector<int32_t> remaining; // [b][n_blocks] MASK count per block
   // last step
@@ -913,8 +914,54 @@ dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int
   return DLLM_OK;
 }
 
+// Query rows per sequence from which attention runs on the tensor cores
+// (128-query tiles); fewer rows use the key-split kernel.
+constexpr int kAttnTcMinRows = 65;
+
 dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes) {
   const dllm_config& c = s->m->cfg;
+  if (R >= kAttnTcMinRows) {
+    const int d = c.d_model, n = s->b * R, bh = s->b * c.n_heads;
+    dllm_status st = DLLM_OK;
+    const CUtensorMap* tq = act_map(s, s->q, d, n, 128, &st);
+    if (!tq) return st;
+    const CUtensorMap* tqlo = tq;
+    if (s->split) {
+      tqlo = act_map(s, s->q_lo, d, n, 128, &st);
+      if (!tqlo) return st;
+    }
+    auto it = s->kv64_maps.find(s->kv);
+    if (it == s->kv64_maps.end()) {
+      CUtensorMap m;
+      CKS(map_kv(&m, s->kv, c.head_dim, s->T, (uint64_t)c.n_layers * 4 * bh, 64));
+      it = s->kv64_maps.emplace(s->kv, m).first;
+    }
+    AttnParams p = {};
+    p.q = s->q;
+    p.q_lo = s->split ? s->q_lo : nullptr;
+    p.kv_lo = s->split ? 1 : 0;
+    p.o = s->ao;
+    p.o_lo = s->split ? s->ao_lo : nullptr;
+    p.R = R;
+    p.b = s->b;
+    p.H = c.n_heads;
+    p.T = s->T;
+    p.z_k0 = ((layer * 2 + 0) * 2 + 0) * bh;
+    p.z_kl0 = ((layer * 2 + 0) * 2 + 1) * bh;
+    p.z_v0 = ((layer * 2 + 1) * 2 + 0) * bh;
+    p.z_vl0 = ((layer * 2 + 1) * 2 + 1) * bh;
+    p.row0 = s->last_row0;
+    p.mask_P = s->P;
+    p.mask_B = s->block_causal ? s->B : 0;
+    p.scale_log2 = kLog2e / std::sqrt((float)c.head_dim);
+    p.err = s->count_err + s->b;
+    if (s->timing) s->kt_bytes[cls] += bytes;
+    Timed t(s, cls, bytes);
+    CK(launch_attention_tc(c.head_dim, *tq, *tqlo, it->second, it->second, p,
+                           dim3(ceil_div(R, 128), c.n_heads, s->b), s->st, true));
+    ++s->launches;
+    return DLLM_OK;
+  }
   AttnPlan a = plan_attention(s->b, c.n_heads, R, s->T, s->m->sms);
   const int QT = 16 * a.wq;
   const long long works = (long long)s->b * c.n_heads * a.q_tiles;
@@ -1987,6 +2034,35 @@ extern "C" dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_ca
   p.err = w->err;
   CK(launch_attention(hd, a.wq, 64, tk, tv, p, dim3(a.splits, a.q_tiles * H, b), static_cast<cudaStream_t>(stream),
                       false));
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                            uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R, int32_t T,
+                                            void* stream) {
+  if (!q || !k_cache || !v_cache || !out || b < 1 || H < 1 || (hd != 64 && hd != 128) || R < 1 || T < 1 ||
+      !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) {
+    set_error("bad attention arguments: b=%d H=%d hd=%d R=%d T=%d", b, H, hd, R, T);
+    return DLLM_EINVAL;
+  }
+  std::lock_guard<std::mutex> lk(g_op_mu);
+  CUtensorMap tq, tk, tv;
+  CKS(map_2d(&tq, q, (uint64_t)H * hd, (uint64_t)b * R, 128));
+  CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H, 64));
+  CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H, 64));
+  OpWorkspace* w = nullptr;
+  CKS(op_workspace(&w, 1, 0, 0));
+  AttnParams p = {};
+  p.q = q;
+  p.o = out;
+  p.R = R;
+  p.b = b;
+  p.H = H;
+  p.T = T;
+  p.scale_log2 = kLog2e / std::sqrt((float)hd);
+  p.err = w->err;
+  CK(launch_attention_tc(hd, tq, tq, tk, tv, p, dim3(ceil_div(R, 128), H, b), static_cast<cudaStream_t>(stream),
+                         false));
   return DLLM_OK;
 }
 

@@ -1,5 +1,6 @@
 // Instantiations of the block-attention kernel (head_dim 64/128, 2 or 4 query
 // warps, 64-key tiles in bf16 or 32-key tiles that also carry the low halves).
+#include "attention_tc.cuh"
 #include "launch.h"
 
 namespace dllm {
@@ -33,6 +34,29 @@ cudaError_t launch_attention(int hd, int wq, int kt, const CUtensorMap& tk, cons
                                             : go_attn<128, 2, 64>(tk, tv, p, grid, st, pdl);
   if (hd == 128 && wq == 4) return kt == 32 ? go_attn<128, 4, 32>(tk, tv, p, grid, st, pdl)
                                             : go_attn<128, 4, 64>(tk, tv, p, grid, st, pdl);
+  return cudaErrorInvalidValue;
+}
+
+template <int HD>
+static cudaError_t go_attn_tc(const CUtensorMap& tq, const CUtensorMap& tqlo, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const AttnParams& p, dim3 grid, cudaStream_t st, bool pdl) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AttnTcCfg<HD>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(attn_tc_kernel<HD>, grid, dim3(192), AttnTcCfg<HD>::SMEM_BYTES, st, pdl, tq, tqlo, tk, tv, p);
+}
+
+cudaError_t launch_attention_tc(int hd, const CUtensorMap& tq, const CUtensorMap& tqlo, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const AttnParams& p, dim3 grid, cudaStream_t st, bool pdl) {
+  if (hd == 64) return go_attn_tc<64>(tq, tqlo, tk, tv, p, grid, st, pdl);
+  if (hd == 128) return go_attn_tc<128>(tq, tqlo, tk, tv, p, grid, st, pdl);
   return cudaErrorInvalidValue;
 }
 

@@ -1,0 +1,357 @@
+// Non-causal attention on the tensor cores for long query sets (the refresh's
+// full forward, PrefixCache and no-cache steps): eq. 3 of the zhongzhuzhou.org
+// notes, section 2, with every query of a 128-row tile reading every key of
+// its sequence (or, under the block-causal mask, the keys below its block's
+// end).
+//
+// One CTA per (128-query tile, head, sequence) walks all keys in 64-key tiles:
+//   warp 0     TMA: the query tile once, then K and V tiles (with their low
+//              halves in split precision) through a two-stage ring;
+//   warp 1     one thread issues tcgen05.mma: S = Q K^T into one of two
+//              64-column TMEM buffers, and O += P V into a HD-column TMEM
+//              accumulator; V is read as an MN-major operand straight from the
+//              TMA tile (keys along K, head dims along N);
+//   warps 2-5  one query row per thread: read S from TMEM, online softmax in
+//              base 2 (the row's reference max moves only when a tile's max
+//              exceeds it by more than 8, so P <= 256 and O is rescaled
+//              rarely, in TMEM), write P as bf16 (hi and lo) into the
+//              K-major operand tile, and at the end O / l to global memory.
+// S of tile t+1 runs on the tensor cores while the softmax of tile t runs.
+//
+// Split precision (kv_lo = 1): q, K, V and P are bf16 pairs x = hi + lo;
+// S = Qh Kh + Ql Kh + Qh Kl and O += Ph Vh + Pl Vh + Ph Vl (lo*lo dropped).
+#pragma once
+
+#include <climits>
+
+#include "attention.cuh"
+#include "ptx.cuh"
+
+namespace dllm {
+
+template <int HD>
+struct AttnTcCfg {
+  static constexpr int KT = 64;                      // keys per tile
+  static constexpr int Q_BYTES = 128 * HD * 2;       // one part (hi or lo) of the query tile
+  static constexpr int KV_BYTES = KT * HD * 2;       // one part of a K or V tile
+  static constexpr int P_BYTES = 128 * KT * 2;       // one part of the probabilities
+  static constexpr int STAGE_BYTES = 4 * KV_BYTES;   // K hi, K lo, V hi, V lo
+  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + 2 * STAGE_BYTES + 2 * P_BYTES + 256;
+  static constexpr int S_COL = 0;                    // two S buffers of KT columns
+  static constexpr int O_COL = 2 * KT;               // O accumulator, HD columns
+  static constexpr int TMEM_COLS = 2 * KT + HD <= 256 ? 256 : 512;
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// Shared-memory descriptor of an MN-major operand written by TMA with the
+// 128-byte swizzle: each 128-byte row holds 64 consecutive MN elements of one
+// K index, 8 K rows form a 1024-byte atom (SBO between atoms along K), and
+// the next 64 MN elements start lbo bytes further.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// 32 lanes x 32 consecutive 32-bit columns written back from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
+      "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
+      "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
+      "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Key limit of query position pos: T, or under the block-causal mask the end
+// of pos's block (the prompt counts as one block).
+__device__ __forceinline__ int tc_key_limit(const AttnParams& p, int pos) {
+  if (p.mask_B <= 0) return p.T;
+  const int lim = pos < p.mask_P ? p.mask_P : p.mask_P + ((pos - p.mask_P) / p.mask_B + 1) * p.mask_B;
+  return lim < p.T ? lim : p.T;
+}
+
+// grid (query tiles of 128, H, b), 192 threads.  tmQ/tmQlo: 2-D maps over
+// q / q_lo [b*R][H*HD] with 128-row boxes; tmK/tmV: 3-D maps over the K and V
+// planes with 64-key boxes (the same map may serve both).
+template <int HD>
+__global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                        const __grid_constant__ CUtensorMap tmQlo,
+                                                        const __grid_constant__ CUtensorMap tmK,
+                                                        const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using C = AttnTcCfg<HD>;
+  constexpr int KT = C::KT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                                   // Q hi, Q lo
+  uint8_t* sKV = sQ + 2 * C::Q_BYTES;                   // per stage: K hi, K lo, V hi, V lo
+  uint8_t* sP = sKV + 2 * C::STAGE_BYTES;               // P hi, P lo
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * C::P_BYTES);
+  uint64_t* qfull = bars;
+  uint64_t* kvfull = bars + 1;    // [2]
+  uint64_t* kvempty = bars + 3;   // [2]
+  uint64_t* sfull = bars + 5;     // [2]
+  uint64_t* sfree = bars + 7;     // [2]
+  uint64_t* pready = bars + 9;
+  uint64_t* pvdone = bars + 10;
+  uint64_t* mdone = bars + 11;    // every MMA of the CTA finished (before TMEM is freed)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, head = blockIdx.y, seq = blockIdx.z;
+  const bool lo = p.kv_lo != 0;
+  const int parts = lo ? 2 : 1;
+  // keys this tile's rows see at most: limits grow with the position
+  const int last_row = min(p.R, qt * 128 + 128) - 1;
+  const int k_end = tc_key_limit(p, p.row0 + last_row);
+  const int nt = (k_end + KT - 1) / KT;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qfull, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kvfull[s], 1);
+      mbar_init(&kvempty[s], 1);
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sfree[s], 4);
+    }
+    mbar_init(pready, 4);
+    mbar_init(pvdone, 1);
+    mbar_init(mdone, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();   // the other query tiles of this head read the same keys
+      const int row = seq * p.R + qt * 128;
+      mbar_arrive_expect_tx(qfull, (uint32_t)(parts * C::Q_BYTES));
+      for (int part = 0; part < parts; ++part)
+        for (int bx = 0; bx < HD / 64; ++bx)
+          tma_load_2d(sQ + part * C::Q_BYTES + bx * (128 * 128), part ? &tmQlo : &tmQ, qfull, head * HD + bx * 64,
+                      row, pol_q);
+      const int zk = p.z_k0 + seq * p.H + head, zv = p.z_v0 + seq * p.H + head;
+      const int zkl = p.z_kl0 + seq * p.H + head, zvl = p.z_vl0 + seq * p.H + head;
+      int issued = 0;
+      for (int t = 0; t < nt; ++t) {
+        const int s = t & 1;
+        if (t >= 2 && !mbar_wait(&kvempty[s], (uint32_t)((t >> 1) - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL)) break;
+        uint8_t* st = sKV + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&kvfull[s], (uint32_t)(2 * parts * C::KV_BYTES));
+        for (int bx = 0; bx < HD / 64; ++bx) {
+          tma_load_3d(st + 0 * C::KV_BYTES + bx * (KT * 128), &tmK, &kvfull[s], bx * 64, t * KT, zk, pol_kv);
+          tma_load_3d(st + 2 * C::KV_BYTES + bx * (KT * 128), &tmV, &kvfull[s], bx * 64, t * KT, zv, pol_kv);
+          if (lo) {
+            tma_load_3d(st + 1 * C::KV_BYTES + bx * (KT * 128), &tmK, &kvfull[s], bx * 64, t * KT, zkl, pol_kv);
+            tma_load_3d(st + 3 * C::KV_BYTES + bx * (KT * 128), &tmV, &kvfull[s], bx * 64, t * KT, zvl, pol_kv);
+          }
+        }
+        issued = t + 1;
+      }
+      // nothing may land in shared memory after the CTA is gone
+      mbar_wait(qfull, 0u, nullptr, p.err, ERR_ATTN_FULL);
+      for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
+        mbar_wait(&kvfull[t & 1], (uint32_t)(t >> 1) & 1u, nullptr, p.err, ERR_ATTN_FULL);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, KT);
+      const uint32_t idesc_o = idesc_bf16_f32(128, HD) | (1u << 16);   // B (V) MN-major
+      const uint32_t q0 = smem_u32(sQ), p0 = smem_u32(sP);
+      bool ok = mbar_wait(qfull, 0u, abort_flag, p.err, ERR_ATTN_FULL);
+      auto issue_s = [&](int t) -> bool {
+        const int s = t & 1;
+        if (!mbar_wait(&kvfull[s], (uint32_t)(t >> 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL)) return false;
+        if (t >= 2 && !mbar_wait(&sfree[s], (uint32_t)((t >> 1) - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL))
+          return false;
+        tc_fence_after();
+        const uint32_t k0 = smem_u32(sKV + s * C::STAGE_BYTES);
+        const uint32_t d = tmem + (uint32_t)(C::S_COL + s * KT);
+        // (Q part, K part): hi*hi, then lo*hi and hi*lo in split precision
+        for (int pr = 0; pr < (lo ? 3 : 1); ++pr) {
+          const uint32_t qa = q0 + (pr == 1 ? C::Q_BYTES : 0);
+          const uint32_t kb = k0 + (pr == 2 ? C::KV_BYTES : 0);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t bx = kk >> 2, ko = (kk & 3) * 32;
+            mma_bf16_ss(d, sdesc_sw128(qa + bx * (128 * 128) + ko), sdesc_sw128(kb + bx * (KT * 128) + ko), idesc_s,
+                        (pr > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&sfull[s]);
+        return true;
+      };
+      if (ok && nt > 0) ok = issue_s(0);
+      for (int t = 0; t < nt && ok; ++t) {
+        if (t + 1 < nt && !issue_s(t + 1)) break;
+        if (!mbar_wait(pready, (uint32_t)t & 1u, abort_flag, p.err, ERR_ATTN_FULL)) break;
+        tc_fence_after();
+        const int s = t & 1;
+        const uint32_t v0 = smem_u32(sKV + s * C::STAGE_BYTES + 2 * C::KV_BYTES);
+        const uint32_t d = tmem + (uint32_t)C::O_COL;
+        // (P part, V part): hi*hi, then lo*hi and hi*lo
+        for (int pr = 0; pr < (lo ? 3 : 1); ++pr) {
+          const uint32_t pa = p0 + (pr == 1 ? C::P_BYTES : 0);
+          const uint32_t vb = v0 + (pr == 2 ? C::KV_BYTES : 0);
+#pragma unroll
+          for (int kk = 0; kk < KT / 16; ++kk)
+            mma_bf16_ss(d, sdesc_sw128(pa + kk * 32), sdesc_sw128_mn(vb + kk * 2048, KT * 128), idesc_o,
+                        (t > 0 || pr > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&kvempty[s]);
+        mma_commit(pvdone);
+      }
+      mma_commit(mdone);
+      mbar_wait(mdone, 0u, nullptr, p.err, ERR_ATTN_FULL);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax rows
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const int qi = qt * 128 + row;
+    const bool valid = qi < p.R;
+    const int lim = valid ? tc_key_limit(p, p.row0 + qi) : 0;
+    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t & 1;
+      // waits decided warp-wide: the TMEM loads and stores below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&sfull[s], (uint32_t)(t >> 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[KT];
+      tmem_ld32(trow + (uint32_t)(C::S_COL + s * KT), sv);
+      tmem_ld32(trow + (uint32_t)(C::S_COL + s * KT + 32), sv + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[s]);
+      const int key0 = t * KT;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < KT; ++c) {
+        sv[c] = key0 + c < lim ? sv[c] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sv[c]);
+      }
+      const bool up = mx > m + 8.0f;
+      const float mn = up ? mx : m;
+      const float use = mn == -INFINITY ? 0.0f : mn;
+      const float corr = up ? exp2f(m - use) : 1.0f;
+      float sum = 0.0f;
+#pragma unroll
+      for (int c = 0; c < KT; ++c) {
+        sv[c] = exp2f(sv[c] - use);
+        sum += sv[c];
+      }
+      l = l * corr + sum;
+      m = mn;
+      // P's buffer and O are free once the previous tile's P V is done
+      if (t > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(pvdone, (uint32_t)(t - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, up)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            float o[32];
+            tmem_ld32(trow + (uint32_t)(C::O_COL + c0), o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= corr;
+            tmem_st32(trow + (uint32_t)(C::O_COL + c0), o);
+          }
+        }
+      }
+      // P row into the K-major operand tile (128-byte swizzle): 8 chunks of
+      // 8 keys, chunk j of row r at ((j ^ (r % 8)) * 16) within the row
+      uint8_t* ph = sP + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t h[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          h[e] = pack_bf16(sv[8 * j + 2 * e], sv[8 * j + 2 * e + 1]);
+          lw[e] = pack_lo(sv[8 * j + 2 * e], sv[8 * j + 2 * e + 1], h[e]);
+        }
+        const int off = ((j ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(ph + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        if (lo) *reinterpret_cast<uint4*>(ph + C::P_BYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pready);
+    }
+    if (ok && nt > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(pvdone, (uint32_t)(nt - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL));
+    tc_fence_after();
+    // O / l as bf16 (and its low half)
+    const float il = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
+    const long long obase = ((long long)seq * p.R + qi) * p.H * HD + head * HD;
+#pragma unroll 1
+    for (int c0 = 0; c0 < HD; c0 += 32) {
+      float o[32];
+      if (nt > 0) {
+        tmem_ld32(trow + (uint32_t)(C::O_COL + c0), o);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+      }
+      if (valid) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t h[4], lw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = o[8 * j + 2 * e] * il, b = o[8 * j + 2 * e + 1] * il;
+            h[e] = pack_bf16(a, b);
+            lw[e] = pack_lo(a, b, h[e]);
+          }
+          *reinterpret_cast<uint4*>(&p.o[obase + c0 + 8 * j]) = make_uint4(h[0], h[1], h[2], h[3]);
+          if (p.o_lo) *reinterpret_cast<uint4*>(&p.o_lo[obase + c0 + 8 * j]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace dllm

@@ -59,6 +59,12 @@ cudaError_t launch_step_hd128(int bn, const StepArgs& a, int grid, cudaStream_t 
 cudaError_t launch_attention(int hd, int wq, int kt, const CUtensorMap& tk, const CUtensorMap& tv,
                              const AttnParams& p, dim3 grid, cudaStream_t st, bool pdl);
 
+// Tensor-core attention over 128-query tiles (attention_tc.cuh): grid
+// (ceil(R/128), H, b); tq/tqlo: 128-row maps over q and q_lo (tqlo unused
+// unless p.kv_lo); tk/tv: K/V maps with 64-key boxes.  hd in {64, 128}.
+cudaError_t launch_attention_tc(int hd, const CUtensorMap& tq, const CUtensorMap& tqlo, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const AttnParams& p, dim3 grid, cudaStream_t st, bool pdl);
+
 }  // namespace dllm
 
 // Instantiate launch_gemm_<name> for the four activation-tile widths.

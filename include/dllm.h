@@ -306,6 +306,20 @@ dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_cache, const 
                               uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R,
                               int32_t T, void* cuda_stream);
 
+/* The same attention (eq. 3 of the Fast-dLLM reading notes, section 2; same
+ * arguments, layouts and output as dllm_op_attention) on the tensor cores:
+ * one CTA per (128-query tile, head, sequence) runs S = q K^T and O = P V as
+ * tcgen05.mma with S and O in tensor memory, over all T keys without a key
+ * split, so it needs no workspace beyond the library's error word.  This is
+ * the kernel the library uses for 65 or more query rows per sequence (the
+ * refresh's full forward, PrefixCache and no-cache steps); block queries use
+ * the key-split kernel.  q, k_cache, v_cache and out must be 16-byte aligned.
+ * Results agree with dllm_op_attention to bf16 rounding of the probabilities
+ * and the output, not bit for bit. */
+dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                 uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R,
+                                 int32_t T, void* cuda_stream);
+
 /* dllm_op_attention with no allocation of any kind.  The pages have no
  * counterpart: the operation is the same non-causal attention (eq. 3 of the
  * Fast-dLLM reading notes, section 2), same arguments, layouts and output,

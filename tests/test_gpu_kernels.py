@@ -122,6 +122,60 @@ def test_attention_matches_oracle(torch, b, H, hd, R, T):
     assert torch.equal(o, o2)
 
 
+TC_ATTN_SHAPES = [
+    (1, 4, 64, 96, 96),      # tiny refresh: one 128-query tile, 32 rows past R
+    (1, 8, 128, 768, 768),   # 8B refresh-sized: 6 query tiles, 12 key tiles
+    (2, 3, 128, 200, 200),   # ragged R and T (T not a multiple of 64), two sequences
+    (1, 4, 128, 130, 70),    # a second query tile with 2 rows; 2 key tiles, the last with 6 keys
+    (3, 2, 64, 65, 1000),    # smallest row count that takes this kernel; long keys
+]
+
+
+@pytest.mark.parametrize("b,H,hd,R,T", TC_ATTN_SHAPES)
+def test_tensor_core_attention_matches_oracle(torch, b, H, hd, R, T):
+    rng = np.random.default_rng(7 * b + H + hd + R + T)
+    qb = bf16_bits(rng.standard_normal((b, R, H, hd)).astype(np.float32))
+    kb = bf16_bits(rng.standard_normal((b, H, T, hd)).astype(np.float32))
+    vb = bf16_bits(rng.standard_normal((b, H, T, hd)).astype(np.float32))
+    q, k, v = to_dev(torch, qb), to_dev(torch, kb), to_dev(torch, vb)
+    o = torch.zeros((b * R, H * hd), dtype=torch.int16, device="cuda")
+    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), b, H, hd, R, T)
+    torch.cuda.synchronize()
+    got = bits_to_f64(dev_bits(torch, o)).reshape(b, R, H, hd)
+    for s in range(b):
+        ref = OM.attention(bits_to_f64(qb[s]), bits_to_f64(kb[s]).transpose(1, 0, 2),
+                           bits_to_f64(vb[s]).transpose(1, 0, 2))
+        vmax = np.abs(bits_to_f64(vb[s])).max()
+        err = np.abs(got[s] - ref)
+        # P rounded to bf16 (2^-8 of sum p|v|) plus the bf16 output (2^-9 |o|)
+        assert (err <= 6e-3 * vmax + 4e-3 * np.abs(ref)).all(), f"seq {s}: max err {err.max():.3e}"
+    o2 = torch.zeros_like(o)
+    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), b, H, hd, R, T)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+
+
+def test_tensor_core_attention_peaked_rows(torch):
+    # rows whose max moves by far more than 8 (base 2) between key tiles:
+    # the running output is rescaled in tensor memory
+    b, H, hd, R, T = 1, 2, 128, 128, 512
+    rng = np.random.default_rng(11)
+    qf = rng.standard_normal((b, R, H, hd)).astype(np.float32)
+    kf = rng.standard_normal((b, H, T, hd)).astype(np.float32)
+    kf[:, :, 300:] *= 4.0           # later keys score much higher
+    qb, kb = bf16_bits(qf), bf16_bits(kf)
+    vb = bf16_bits(rng.standard_normal((b, H, T, hd)).astype(np.float32))
+    q, k, v = to_dev(torch, qb), to_dev(torch, kb), to_dev(torch, vb)
+    o = torch.zeros((b * R, H * hd), dtype=torch.int16, device="cuda")
+    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), b, H, hd, R, T)
+    torch.cuda.synchronize()
+    got = bits_to_f64(dev_bits(torch, o)).reshape(R, H, hd)
+    ref = OM.attention(bits_to_f64(qb[0]), bits_to_f64(kb[0]).transpose(1, 0, 2), bits_to_f64(vb[0]).transpose(1, 0, 2))
+    vmax = np.abs(bits_to_f64(vb[0])).max()
+    err = np.abs(got - ref)
+    assert (err <= 6e-3 * vmax + 4e-3 * np.abs(ref)).all(), f"max err {err.max():.3e}"
+
+
 def test_attention_identical_keys_is_mean_of_values(torch):
     b, H, hd, R, T = 1, 2, 128, 32, 300
     rng = np.random.default_rng(5)
