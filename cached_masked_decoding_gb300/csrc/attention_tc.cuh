@@ -189,12 +189,8 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       const uint32_t idesc_o = idesc_bf16_f32(128, HD) | (1u << 16);   // B (V) MN-major
       const uint32_t q0 = smem_u32(sQ), p0 = smem_u32(sP);
       bool ok = mbar_wait(qfull, 0u, abort_flag, p.err, ERR_ATTN_FULL);
-      auto issue_s = [&](int t) -> bool {
+      auto issue_s = [&](int t) {
         const int s = t & 1;
-        if (!mbar_wait(&kvfull[s], (uint32_t)(t >> 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL)) return false;
-        if (t >= 2 && !mbar_wait(&sfree[s], (uint32_t)((t >> 1) - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL))
-          return false;
-        tc_fence_after();
         const uint32_t k0 = smem_u32(sKV + s * C::STAGE_BYTES);
         const uint32_t d = tmem + (uint32_t)(C::S_COL + s * KT);
         // (Q part, K part): hi*hi, then lo*hi and hi*lo in split precision
@@ -209,13 +205,8 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
           }
         }
         mma_commit(&sfull[s]);
-        return true;
       };
-      if (ok && nt > 0) ok = issue_s(0);
-      for (int t = 0; t < nt && ok; ++t) {
-        if (t + 1 < nt && !issue_s(t + 1)) break;
-        if (!mbar_wait(pready, (uint32_t)t & 1u, abort_flag, p.err, ERR_ATTN_FULL)) break;
-        tc_fence_after();
+      auto issue_pv = [&](int t) {
         const int s = t & 1;
         const uint32_t v0 = smem_u32(sKV + s * C::STAGE_BYTES + 2 * C::KV_BYTES);
         const uint32_t d = tmem + (uint32_t)C::O_COL;
@@ -228,8 +219,42 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
             mma_bf16_ss(d, sdesc_sw128(pa + kk * 32), sdesc_sw128_mn(vb + kk * 2048, KT * 128), idesc_o,
                         (t > 0 || pr > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kvempty[s]);
+        mma_commit(&kvempty[s]);   // the stage may be refilled
         mma_commit(pvdone);
+      };
+      // Issue whichever is ready: P V of the oldest tile whose P is written
+      // (it frees a K/V stage for the next load), or S of the next tile once
+      // its keys have landed and its S buffer has been read.  Neither waits
+      // behind the other.
+      int ns = 0, np = 0;
+      unsigned long long idle_since = 0;
+      uint32_t spins = 0;
+      while (ok && np < nt) {
+        bool did = false;
+        if (np < ns && mbar_test_wait(smem_u32(pready), (uint32_t)np & 1u)) {
+          tc_fence_after();
+          issue_pv(np++);
+          did = true;
+        }
+        if (ns < nt && mbar_test_wait(smem_u32(&kvfull[ns & 1]), (uint32_t)(ns >> 1) & 1u) &&
+            (ns < 2 || mbar_test_wait(smem_u32(&sfree[ns & 1]), (uint32_t)((ns >> 1) - 1) & 1u))) {
+          tc_fence_after();
+          issue_s(ns++);
+          did = true;
+        }
+        if (did) {
+          idle_since = 0;
+          spins = 0;
+        } else if ((++spins & 63u) == 0) {
+          const unsigned long long now = globaltimer();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (*abort_flag || now - idle_since > kWaitLimitNs) {
+            if (!*abort_flag) record_error(p.err, ERR_ATTN_FULL);
+            *abort_flag = 1;
+            ok = false;
+          }
+        }
       }
       mma_commit(mdone);
       mbar_wait(mdone, 0u, nullptr, p.err, ERR_ATTN_FULL);
