@@ -97,6 +97,101 @@ __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
   return (uint32_t)((ch >> 3) * (KT * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
+// The last split of a work (seq, head, query tile of QT rows) combines the
+// partials (o, m, l) of all splits, in split order: per row, weights
+// exp2(m_s - M) / L computed once, then every output element is an
+// independent weighted sum over the splits.  128 threads (named barrier 2);
+// xo holds at least QT * splits floats.  Returns true.
+template <int HD, int QT>
+__device__ __forceinline__ bool attn_merge(const AttnParams& p, long long work, int qt, int head, int seq, float* xo,
+                                           int tid) {
+  const float* base_o = p.ws_o + work * p.splits * QT * HD;
+  const float* base_ml = p.ws_ml + work * p.splits * QT * 2;
+  float* wn = xo;   // [QT][splits] normalised split weights (the key-group buffer is free now)
+  const int S = p.splits;
+  // The partials were written by other CTAs: every load is an L2 round trip,
+  // so they are issued in unrolled, predicated batches rather than one
+  // dependent load per split.
+  for (int rl = tid; rl < QT; rl += 128) {
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float mv[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mv[t] = s0 + t < S ? __ldcg(&base_ml[((s0 + t) * QT + rl) * 2]) : -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) M = fmaxf(M, mv[t]);
+    }
+    const float u = (M == -INFINITY) ? 0.0f : M;
+    float L = 0.0f;
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float2 ml[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        ml[t] = s0 + t < S ? __ldcg(reinterpret_cast<const float2*>(&base_ml[((s0 + t) * QT + rl) * 2]))
+                           : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (s0 + t < S) {
+          const float a = exp2f(ml[t].x - u);
+          wn[rl * S + s0 + t] = a;
+          L += ml[t].y * a;
+        }
+      }
+    }
+    const float il = L > 0.0f ? 1.0f / L : 0.0f;
+    for (int s = 0; s < S; ++s) wn[rl * S + s] *= il;
+  }
+  named_bar_sync(2, 128);
+  // four output vectors per thread and pass, four splits per batch: sixteen
+  // loads in flight; the sum over splits keeps split order
+  for (int e0 = tid; e0 < QT * HD / 4; e0 += 4 * 128) {
+    float4 acc[4];
+#pragma unroll
+    for (int u4 = 0; u4 < 4; ++u4) acc[u4] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 4) {
+      float4 v[4][4];
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const int e4 = e0 + u4 * 128;
+        const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          v[u4][t] = (e4 < QT * HD / 4 && s0 + t < S)
+                         ? __ldcg(reinterpret_cast<const float4*>(&base_o[((s0 + t) * QT + rl) * HD + col]))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const int e4 = e0 + u4 * 128;
+        const int rl = (e4 * 4) / HD;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (e4 < QT * HD / 4 && s0 + t < S) {
+            const float w = wn[rl * S + s0 + t];
+            acc[u4].x += v[u4][t].x * w;
+            acc[u4].y += v[u4][t].y * w;
+            acc[u4].z += v[u4][t].z * w;
+            acc[u4].w += v[u4][t].w * w;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u4 = 0; u4 < 4; ++u4) {
+      const int e4 = e0 + u4 * 128;
+      if (e4 >= QT * HD / 4) continue;
+      const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
+      const int row = qt * QT + rl;
+      if (row >= p.R) continue;
+      const float4 a4 = acc[u4];
+      const long long oi = ((long long)seq * p.R + row) * p.H * HD + head * HD + col;
+      store_pair(p.o, p.o_lo, oi, a4.x, a4.y);
+      store_pair(p.o, p.o_lo, oi + 2, a4.z, a4.w);
+    }
+  }
+  return true;
+}
+
 // One work item (key split, query tile, head, sequence) of block attention,
 // run by a group of 128 threads (tid 0..127, named barrier 2).  sK/sV hold ST
 // stages of [KT keys][HD] tiles (1024-byte aligned), each stage followed by its
@@ -416,93 +511,7 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
   }
   named_bar_sync(2, 128);
   if (!*bcast) return false;
-  // combine the splits: per row, weights exp2(m_s - M) / L computed once, then
-  // every output element is an independent weighted sum over the splits
-  const float* base_o = p.ws_o + work * p.splits * QT * HD;
-  const float* base_ml = p.ws_ml + work * p.splits * QT * 2;
-  float* wn = xo;   // [QT][splits] normalised split weights (the key-group buffer is free now)
-  const int S = p.splits;
-  // The partials were written by other CTAs: every load is an L2 round trip,
-  // so they are issued in unrolled, predicated batches rather than one
-  // dependent load per split.
-  for (int rl = tid; rl < QT; rl += 128) {
-    float M = -INFINITY;
-    for (int s0 = 0; s0 < S; s0 += 8) {
-      float mv[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mv[t] = s0 + t < S ? __ldcg(&base_ml[((s0 + t) * QT + rl) * 2]) : -INFINITY;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) M = fmaxf(M, mv[t]);
-    }
-    const float u = (M == -INFINITY) ? 0.0f : M;
-    float L = 0.0f;
-    for (int s0 = 0; s0 < S; s0 += 8) {
-      float2 ml[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        ml[t] = s0 + t < S ? __ldcg(reinterpret_cast<const float2*>(&base_ml[((s0 + t) * QT + rl) * 2]))
-                           : make_float2(-INFINITY, 0.0f);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        if (s0 + t < S) {
-          const float a = exp2f(ml[t].x - u);
-          wn[rl * S + s0 + t] = a;
-          L += ml[t].y * a;
-        }
-      }
-    }
-    const float il = L > 0.0f ? 1.0f / L : 0.0f;
-    for (int s = 0; s < S; ++s) wn[rl * S + s] *= il;
-  }
-  named_bar_sync(2, 128);
-  // four output vectors per thread and pass, four splits per batch: sixteen
-  // loads in flight; the sum over splits keeps split order
-  for (int e0 = tid; e0 < QT * HD / 4; e0 += 4 * 128) {
-    float4 acc[4];
-#pragma unroll
-    for (int u4 = 0; u4 < 4; ++u4) acc[u4] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < S; s0 += 4) {
-      float4 v[4][4];
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const int e4 = e0 + u4 * 128;
-        const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          v[u4][t] = (e4 < QT * HD / 4 && s0 + t < S)
-                         ? __ldcg(reinterpret_cast<const float4*>(&base_o[((s0 + t) * QT + rl) * HD + col]))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const int e4 = e0 + u4 * 128;
-        const int rl = (e4 * 4) / HD;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (e4 < QT * HD / 4 && s0 + t < S) {
-            const float w = wn[rl * S + s0 + t];
-            acc[u4].x += v[u4][t].x * w;
-            acc[u4].y += v[u4][t].y * w;
-            acc[u4].z += v[u4][t].z * w;
-            acc[u4].w += v[u4][t].w * w;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int u4 = 0; u4 < 4; ++u4) {
-      const int e4 = e0 + u4 * 128;
-      if (e4 >= QT * HD / 4) continue;
-      const int rl = (e4 * 4) / HD, col = e4 * 4 - rl * HD;
-      const int row = qt * QT + rl;
-      if (row >= p.R) continue;
-      const float4 a4 = acc[u4];
-      const long long oi = ((long long)seq * p.R + row) * p.H * HD + head * HD + col;
-      store_pair(p.o, p.o_lo, oi, a4.x, a4.y);
-      store_pair(p.o, p.o_lo, oi + 2, a4.z, a4.w);
-    }
-  }
-  return true;
+  return attn_merge<HD, QT>(p, work, qt, head, seq, xo, tid);
 }
 
 // Standalone launch: one work item per CTA.  KT = 32 also takes the low
