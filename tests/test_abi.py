@@ -59,6 +59,13 @@ def test_host_side_errors_without_gpu_work():
     assert L.dllm_load(b"/nonexistent/weights.bin", ctypes.byref(h)) == binding.EIO
     assert L.dllm_prefill_refresh(None) == binding.EINVAL
     assert L.dllm_denoise_step(None, 0, 0.9, 2, None) == -binding.EINVAL
+    # the single-kernel attention entries reject bad shapes and unaligned pointers before any launch
+    for fn in (L.dllm_op_attention, L.dllm_op_attention_tc, L.dllm_op_attention_noalloc):
+        assert fn(None, None, None, None, 1, 1, 128, 1, 1, None) == binding.EINVAL
+        assert fn(16, 16, 16, 16, 1, 1, 96, 1, 1, None) == binding.EINVAL      # hd not 64 or 128
+        assert fn(16, 16, 16, 16, 1, 1, 128, 0, 1, None) == binding.EINVAL     # no query rows
+    assert L.dllm_op_attention_tc(18, 16, 16, 16, 1, 1, 128, 1, 1, None) == binding.EINVAL   # q not 16-byte aligned
+    assert b"bad attention arguments" in L.dllm_last_error()
 
 
 def test_fault_injection_io(monkeypatch, tmp_path):
