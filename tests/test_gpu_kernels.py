@@ -128,6 +128,9 @@ TC_ATTN_SHAPES = [
     (2, 3, 128, 200, 200),   # ragged R and T (T not a multiple of 64), two sequences
     (1, 4, 128, 130, 70),    # a second query tile with 2 rows; 2 key tiles, the last with 6 keys
     (3, 2, 64, 65, 1000),    # smallest row count that takes this kernel; long keys
+    (1, 1, 64, 70, 1),       # a single key
+    (3, 1, 128, 65, 63),     # fewer keys than one tile; three sequences of 65 rows
+    (2, 2, 64, 129, 129),    # one row and one key past a tile boundary
 ]
 
 
