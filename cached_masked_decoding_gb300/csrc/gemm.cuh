@@ -682,27 +682,37 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t use = (uint32_t)(seg >> 1);
 
       if (n_idx != rs_tile) {
-        // RMSNorm row factors of this activation tile: partial sums of squares
-        // staged in smem with parallel loads, then each row sums its partials
-        // in order
+        // RMSNorm row factors of this activation tile.  One row per thread:
+        // its partial sums of squares are contiguous, read as 16-byte vectors
+        // in a single round of loads and summed in order.  (The tile order
+        // changes the row tile at almost every tile, so this runs per tile;
+        // staged through shared memory in four dependent rounds it had cost
+        // ~17 us per tile in the refresh.)
         rs_tile = n_idx;
         named_bar_sync(1, 128);
         if (p.ss_in) {
           const int tiles = p.ss_in_tiles;
-          for (int c0 = 0; c0 < BN; c0 += 32) {
-            for (int e = l128; e < 32 * tiles; e += 128) {
-              const int c = e / tiles, t = e - c * tiles;
-              const int r = n_idx * BN + c0 + c;
-              xch[e] = r < p.N ? __ldcg(&p.ss_in[(long long)r * tiles + t]) : 0.0f;
+          for (int c = l128; c < BN; c += 128) {
+            const int r = n_idx * BN + c;
+            float sum = 0.0f;
+            if (r < p.N) {
+              const float* src = p.ss_in + (long long)r * tiles;
+              if ((tiles & 3) == 0) {
+                for (int t0 = 0; t0 < tiles; t0 += 32) {
+                  const int nv = (tiles - t0) / 4 < 8 ? (tiles - t0) / 4 : 8;
+                  float4 x[8];
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    x[j] = j < nv ? __ldcg(reinterpret_cast<const float4*>(src + t0) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    if (j < nv) sum = (((sum + x[j].x) + x[j].y) + x[j].z) + x[j].w;
+                }
+              } else {
+                for (int t = 0; t < tiles; ++t) sum += __ldcg(&src[t]);
+              }
             }
-            named_bar_sync(1, 128);
-            if (l128 < 32) {
-              const int r = n_idx * BN + c0 + l128;
-              float sum = 0.0f;
-              for (int t = 0; t < tiles; ++t) sum += xch[l128 * tiles + t];
-              rs_s[c0 + l128] = r < p.N ? rsqrtf(sum * p.inv_d + p.eps) : 0.0f;
-            }
-            named_bar_sync(1, 128);
+            rs_s[c] = r < p.N ? rsqrtf(sum * p.inv_d + p.eps) : 0.0f;
           }
         } else {
           for (int c = l128; c < BN; c += 128) rs_s[c] = 1.0f;
