@@ -101,14 +101,16 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, key_limit: np.ndarray
     """Non-causal multi-head attention, eq. 3. q: [n, H, hd]; k, v: [T, H, hd].
     key_limit (optional, [n]): query i sees keys t < key_limit[i] only."""
     hd = q.shape[-1]
-    s = np.einsum("nhd,thd->hnt", q, k) / np.sqrt(hd)
+    # per head: S = q k^T / sqrt(hd) as a batched matrix product [H][n][T]
+    s = np.matmul(q.transpose(1, 0, 2), k.transpose(1, 2, 0)) / np.sqrt(hd)
     if key_limit is not None:
         hidden = np.arange(k.shape[0])[None, :] >= np.asarray(key_limit)[:, None]   # [n, T]
         s = np.where(hidden[None], -np.inf, s)
     s = s - s.max(axis=-1, keepdims=True)
     p = np.exp(s)
     p = p / p.sum(axis=-1, keepdims=True)
-    return np.einsum("hnt,thd->nhd", p, v)
+    # O = P V per head, back to [n][H][hd]
+    return np.matmul(p, v.transpose(1, 0, 2)).transpose(1, 0, 2)
 
 
 def silu(x: np.ndarray) -> np.ndarray:

@@ -27,9 +27,13 @@ Passages followed (zhongzhuzhou.org Fast-dLLM reading notes unless noted):
 * ``staleness`` - Algorithm 4 of the notes (section 14), steps 4-5: fresh
   versus cached K/V rows (cosine per layer) and predictions (argmax
   agreement, max-prob difference) for the current block.
-* ``llada_sample`` - page 1's LLaDA sampler (section "what one step does"): a
-  full bidirectional forward each step, n_keep = len(masked) // (steps - k) most
-  confident masked positions committed, never changed afterwards.
+* ``llada_sample`` - page 1's LLaDA sampler (the tutorial's prose on one
+  step from time t to s): a full bidirectional forward predicts every masked
+  position, low-confidence remasking puts about s/t of them back under MASK
+  (the least confident) and writes the rest, which never change afterwards.
+* ``Decoder.run`` with ``refresh_interval`` - the refresh schedule separated
+  from the block schedule (notes, section 11, Table 10's refresh intervals
+  and the section's closing paragraph).
 
 Readings where the pages are silent (each also listed in the design notes):
 eligible positions are the MASK positions of the current block only; ties in
@@ -42,8 +46,9 @@ float32 on the float32-rounded confidence.
 Pins (tests/test_oracle_pins.py): the poker example (page 1 and page 2) and
 the invariants - committed tokens never change, every step commits >= 1 while
 MASK remains, tau > 1 reproduces ``llada_sample`` with one commit per step,
-refreshing before every step reproduces the no-cache trajectory, at most B
-steps per block.
+refreshing before every step reproduces the no-cache trajectory, a refresh
+interval of at least B is the block-boundary schedule, at most B steps per
+block, the tutorial's worked example of two steps keeping two tokens each.
 """
 from __future__ import annotations
 
@@ -252,25 +257,50 @@ class Decoder:
         self.steps += 1
         return StepOut(j, x_before, conf, conf32, arg, margin, hb, sel, sel.sum(axis=1), elig)
 
-    def generate(self, rule: Rule, refresh_every_step: bool = False, max_steps: int | None = None):
-        """Algorithm 1.  Returns (answer tokens [b][gen], list of StepOut)."""
-        trace = []
+    def run(self, rule: Rule, refresh_interval: int = 0, max_steps: int | None = None):
+        """Algorithm 1 as a stream of events, in the order the loop takes them.
+
+        Yields ``("refresh", j)`` after each cache refresh (j = the block the
+        loop is in, 0 for the prefill) and ``("step", j, StepOut)`` after each
+        denoise step.  A consumer may ``send`` a canvas [b][T] back in reply to
+        a step event; the decoder then continues from that canvas instead of
+        its own commit (used to follow another decoder's trajectory).
+
+        ``refresh_interval`` r separates the refresh schedule from the block
+        schedule (zhongzhuzhou.org notes, section 11, Table 10 and the closing
+        paragraph of the section): with r > 0 the cached K/V are also
+        refreshed before every r-th step inside a block (before steps r, 2r,
+        ... counted from the block's first step, which follows the
+        block-boundary refresh); r = 0 refreshes at block boundaries only.
+        """
         cached = self.mode != "none"
         if cached:
             self.refresh()
+            yield ("refresh", 0)
+        n = 0
         for j in range(self.n_blocks):
             spb = 0
             while self.eligible(j).any():
-                if refresh_every_step and cached:
+                if cached and refresh_interval > 0 and spb > 0 and spb % refresh_interval == 0:
                     self.refresh()
+                    yield ("refresh", j)
                 # the scheduled rule counts its k down within each block
                 r = dataclasses.replace(rule, k=max(1, rule.k - spb)) if rule.policy == SCHEDULE else rule
-                trace.append(self.step(j, r))
+                out = self.step(j, r)
+                adopt = yield ("step", j, out)
+                if adopt is not None:
+                    self.x = np.asarray(adopt, dtype=np.int64).copy()
                 spb += 1
-                if max_steps is not None and len(trace) >= max_steps:
-                    return self.x[:, self.P:].copy(), trace
+                n += 1
+                if max_steps is not None and n >= max_steps:
+                    return
             if cached and j < self.n_blocks - 1:
                 self.refresh()
+                yield ("refresh", j)
+
+    def generate(self, rule: Rule, refresh_interval: int = 0, max_steps: int | None = None):
+        """Algorithm 1 (section 3).  Returns (answer tokens [b][gen], list of StepOut)."""
+        trace = [ev[2] for ev in self.run(rule, refresh_interval, max_steps) if ev[0] == "step"]
         return self.x[:, self.P:].copy(), trace
 
 
@@ -321,23 +351,36 @@ def tau_bar(trace, b: int) -> np.ndarray:
     return committed / np.maximum(active, 1)
 
 
+def llada_remask_count(masked: int, steps: int, k: int) -> int:
+    """How many of this step's predictions go back under MASK in page 1's
+    LLaDA sampler.  The step runs from time t = (steps - k) / steps to
+    s = (steps - k - 1) / steps and re-masks about s/t of the positions that
+    were masked: ceil(masked * s / t) of them, in exact integer arithmetic
+    (so that the positions kept, masked minus this, spread the remaining MASKs
+    evenly over the remaining steps, rounded down)."""
+    left = steps - k
+    return -((-masked * (left - 1)) // left)
+
+
 def llada_sample(w: M.Weights, prompt: np.ndarray, gen_len: int, steps: int) -> np.ndarray:
-    """Page 1's LLaDA sampler: full forward per step, commit the n_keep most
-    confident masked positions (n_keep spreads the remaining MASKs over the
-    remaining steps), committed tokens never change."""
+    """Page 1's LLaDA sampler (tutorial, section on what one step does): each
+    step one full bidirectional forward predicts every masked position, and
+    low-confidence remasking puts the least confident predictions back under
+    MASK (``llada_remask_count`` of them) while the rest are written; a written
+    token is never changed again.  Ties: among equal confidences the later
+    position is re-masked first (so the earlier one is kept)."""
     cfg = w.cfg
+    P = int(np.asarray(prompt).shape[0])
     x = np.concatenate([np.asarray(prompt, dtype=np.int64), np.full(gen_len, cfg.mask_id, dtype=np.int64)])
-    T = x.shape[0]
-    rows = np.arange(T)
     for k in range(steps):
-        fw = M.forward_rows(w, x, rows, None, None)
-        st = M.lm_head(w, fw.h_final)
         masked = np.flatnonzero(x == cfg.mask_id)
         if masked.size == 0:
             break
-        n_keep = masked.size // (steps - k)
-        conf32 = st.conf.astype(np.float32)
-        order = masked[np.lexsort((masked, -conf32[masked].astype(np.float64)))]
-        for i in order[:n_keep]:
-            x[i] = st.arg[i]
-    return x[prompt.shape[0]:]
+        pred = M.lm_head(w, M.forward_rows(w, x, np.arange(x.shape[0]), None, None).h_final)
+        c32 = pred.conf.astype(np.float32)
+        back = llada_remask_count(masked.size, steps, k)
+        # least confident first; among equals the higher position first
+        worst_first = masked[np.lexsort((-masked, c32[masked].astype(np.float64)))]
+        write = worst_first[back:]
+        x[write] = pred.arg[write]
+    return x[P:]

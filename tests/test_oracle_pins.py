@@ -295,15 +295,86 @@ def test_attention_closed_forms():
     np.testing.assert_allclose(M.attention(q, k[perm], v[perm]), M.attention(q, k, v), rtol=1e-12)
 
 
+# silu(t) = t * sigmoid(t) at fixed points: sigmoid(1) = e / (1 + e) and
+# sigmoid(-2) = 1 / (1 + e^2), as published decimal constants.
+SILU_1 = 0.7310585786300049
+SILU_M2 = -0.2384058440442351
+
+
+def test_silu_fixed_values():
+    np.testing.assert_allclose(M.silu(np.array([1.0, -2.0, 0.0])), [SILU_1, SILU_M2, 0.0], rtol=1e-15, atol=0)
+    # silu(t) - silu(-t) = t  (sigmoid(t) + sigmoid(-t) = 1)
+    t = np.linspace(-6, 6, 13)
+    np.testing.assert_allclose(M.silu(t) - M.silu(-t), t, atol=1e-14)
+
+
 def test_swiglu_hand_weights():
     x = np.array([[1.0, -2.0]])
     wg = np.array([[1.0, 0.0], [0.0, 1.0]])
     wu = np.array([[2.0, 0.0], [0.0, 1.0]])
     wd = np.array([[1.0, 1.0]])
-    silu = lambda t: t / (1 + np.exp(-t))
-    expect = silu(1.0) * 2.0 + silu(-2.0) * (-2.0)
+    # W_d (silu(W_g x) * W_u x) = silu(1) * 2 + silu(-2) * (-2)
+    expect = SILU_1 * 2.0 + SILU_M2 * (-2.0)
     assert M.swiglu(x, wg, wu, wd)[0, 0] == pytest.approx(expect, rel=1e-14)
-    assert M.silu(np.array([0.0]))[0] == 0.0
+
+
+def _hand_cfg(**kw):
+    base = dict(name="hand", n_layers=1, d_model=4, n_heads=2, head_dim=2, d_ffn=4, vocab=5, norm_eps=0.0)
+    base.update(kw)
+    return configs.ModelConfig(**base)
+
+
+COS1, SIN1 = 0.5403023058681398, 0.8414709848078965       # cos(1 rad), sin(1 rad)
+
+
+def test_qkv_hand_model():
+    """A one-layer, d = 4, two-head (hd = 2) model whose q, k and v come out of
+    distinct weights (W_q = I, W_k = 2I, W_v = 3I): RMSNorm scales a unit
+    basis row e_c to 2 e_c; RoPE turns q and k of a head by pos * theta^0 =
+    pos radians at absolute position pos, and leaves v alone; column c feeds
+    head c // 2."""
+    cfg = _hand_cfg()
+    eye = np.eye(4)
+    z = np.zeros((4, 4))
+    lw = M.LayerWeights(attn_norm=np.ones(4), wq=eye, wk=2 * eye, wv=3 * eye, wo=z, ffn_norm=np.ones(4),
+                        wg=z, wu=z, wd=z)
+    h = np.array([[1.0, 0.0, 0.0, 0.0], [0.0, 0.0, 1.0, 0.0], [1.0, 0.0, 0.0, 0.0]])
+    pos = np.array([1, 1, 0])
+    q, k, v = M.qkv(cfg, lw, h, pos)
+    assert q.shape == k.shape == v.shape == (3, 2, 2)
+    # row 0: head 0 holds (2, 0), turned by 1 rad; head 1 is zero
+    np.testing.assert_allclose(q[0], [[2 * COS1, 2 * SIN1], [0, 0]], atol=1e-15)
+    np.testing.assert_allclose(k[0], [[4 * COS1, 4 * SIN1], [0, 0]], atol=1e-15)
+    np.testing.assert_allclose(v[0], [[6.0, 0.0], [0, 0]], atol=1e-15)        # no rotation of v
+    # row 1: the same vector in head 1
+    np.testing.assert_allclose(q[1], [[0, 0], [2 * COS1, 2 * SIN1]], atol=1e-15)
+    np.testing.assert_allclose(k[1], [[0, 0], [4 * COS1, 4 * SIN1]], atol=1e-15)
+    np.testing.assert_allclose(v[1], [[0, 0], [6.0, 0.0]], atol=1e-15)
+    # row 2: position 0 turns nothing
+    np.testing.assert_allclose(q[2], [[2.0, 0.0], [0, 0]], atol=1e-15)
+    np.testing.assert_allclose(k[2], [[4.0, 0.0], [0, 0]], atol=1e-15)
+
+
+def test_lm_head_hand_logits_margin_and_ties():
+    """Final RMSNorm of an all-ones row is the row itself (eps 0), so each
+    logit is the sum of its LM-head row: logits (1, 4, 3.5, 3.25, -2) give the
+    argmax 1 and a top-1/top-2 margin of 0.5; an equal top pair gives margin 0
+    and the lower id."""
+    cfg = _hand_cfg()
+    rows = np.array([1.0, 4.0, 3.5, 3.25, -2.0])
+    lm = np.zeros((5, 4))
+    lm[:, 0] = rows
+    w = M.Weights(cfg=cfg, embed=np.zeros((6, 4)), layers=[], final_norm=np.ones(4), lm_head=lm)
+    st = M.lm_head(w, np.ones((1, 4)))
+    np.testing.assert_allclose(st.logits[0], rows, atol=0)
+    assert st.arg[0] == 1 and st.margin[0] == 0.5
+    lm[3, 0] = 4.0
+    st = M.lm_head(w, np.ones((1, 4)))
+    assert st.arg[0] == 1 and st.margin[0] == 0.0
+    # a dominant logit: confidence 1 / (1 + 4 e^-40) to double precision
+    lm[:, 0] = [0.0, 40.0, 0.0, 0.0, 0.0]
+    st = M.lm_head(w, np.ones((1, 4)))
+    assert st.conf[0] == pytest.approx(1.0, abs=1e-16) and st.margin[0] == 40.0
 
 
 def _tiny_weights(random_norms=False, cfg=configs.TINY_SPREAD):
@@ -402,6 +473,36 @@ def test_schedule_rule_is_llada_sampler(tiny_w, steps):
     np.testing.assert_array_equal(toks[0], S.llada_sample(tiny_w, pr[0], gen, steps))
 
 
+def test_llada_remask_count_worked_example():
+    """The tutorial's worked example ('the tea is cold'): four positions, two
+    steps, two tokens kept per step; tea's 0.3 at step 1 puts it back under
+    MASK, and at step 2 everything left is written."""
+    g = golden("tea_is_cold.json")
+    m = g["gen_len"]
+    kept = []
+    for k in range(g["steps"]):
+        back = S.llada_remask_count(m, g["steps"], k)
+        kept.append(m - back)
+        m = back
+    assert kept == g["kept_per_step"] and m == 0
+    # the selection at step 1: tea (0.3) is among the re-masked, the and is are kept
+    words = ["the", "tea", "is", "cold"]
+    conf = np.array([0.9, g["tea_confidence"]["step_1"], 0.8, 0.2], dtype=np.float32)
+    sel = S.select_schedule(conf, np.ones(4, dtype=bool), g["steps"])
+    assert [w for w, s_ in zip(words, sel) if s_] == g["kept_at_step_1"]
+
+
+def test_llada_remask_count_spreads_evenly():
+    """Keeping masked - remask positions spreads the remaining MASKs evenly
+    over the remaining steps, rounded down, and the last step writes them all."""
+    for steps in range(1, 25):
+        for m in range(0, 70):
+            for k in range(steps):
+                kept = m - S.llada_remask_count(m, steps, k)
+                assert kept * (steps - k) <= m < (kept + 1) * (steps - k)
+            assert S.llada_remask_count(m, steps, steps - 1) == 0
+
+
 def test_attention_key_limit_closed_forms():
     """A key limit of T is the unmasked attention; a limit of 1 returns v[0]."""
     rng = np.random.default_rng(4)
@@ -475,11 +576,73 @@ def test_staleness_after_commits(tiny_w):
 @pytest.mark.parametrize("mode", ["prefix", "dual"])
 def test_refresh_every_step_equals_no_cache(tiny_w, mode):
     _, t_none, tr_none = _run(tiny_w, "none", S.Rule(S.THRESHOLD, 0.9), b=2)
-    _, t_c, tr_c = _run(tiny_w, mode, S.Rule(S.THRESHOLD, 0.9), b=2, refresh_every_step=True)
+    _, t_c, tr_c = _run(tiny_w, mode, S.Rule(S.THRESHOLD, 0.9), b=2, refresh_interval=1)
     np.testing.assert_array_equal(t_none, t_c)
     assert len(tr_none) == len(tr_c)
     for a, b in zip(tr_none, tr_c):
         np.testing.assert_allclose(a.conf, b.conf, rtol=1e-9, atol=1e-12)
+
+
+def test_refresh_interval_of_a_block_is_the_block_schedule(tiny_w):
+    """A block takes at most B steps, so a refresh interval r >= B never
+    refreshes inside a block: the same events as the block-boundary schedule
+    (r = 0), the same tokens and confidences."""
+    B = 8
+    pr = synth.prompts(tiny_w.cfg, 1, 2, 16)
+    runs = []
+    for r in (0, B, 3 * B):
+        dec = S.Decoder(tiny_w, pr, 32, B, "dual")
+        runs.append([(ev[0], ev[1], ev[2].conf if ev[0] == "step" else None)
+                     for ev in dec.run(S.Rule(S.FIXED_K, k=1), refresh_interval=r)])
+    for other in runs[1:]:
+        assert [e[:2] for e in other] == [e[:2] for e in runs[0]]
+        for a, b in zip(other, runs[0]):
+            if a[0] == "step":
+                np.testing.assert_array_equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("r", [1, 2, 3])
+def test_refresh_interval_counts(tiny_w, r):
+    """With fixed k = 1 every block of B positions takes exactly B steps, so an
+    interval r refreshes ceil(B / r) - 1 times inside each block, on top of
+    the prefill and the n_blocks - 1 block-boundary refreshes; a refresh
+    always comes right before the step whose in-block index is a multiple of r."""
+    B, gen = 4, 12
+    pr = synth.prompts(tiny_w.cfg, 2, 1, 8)
+    dec = S.Decoder(tiny_w, pr, gen, B, "dual")
+    evs = [e[:2] for e in dec.run(S.Rule(S.FIXED_K, k=1), refresh_interval=r)]
+    n_blocks = gen // B
+    expect = [("refresh", 0)]
+    for j in range(n_blocks):
+        for i in range(B):
+            if i > 0 and i % r == 0:
+                expect.append(("refresh", j))
+            expect.append(("step", j))
+        if j + 1 < n_blocks:
+            expect.append(("refresh", j))
+    assert evs == expect
+    inside = -(-B // r) - 1
+    assert dec.refreshes == 1 + (n_blocks - 1) + n_blocks * inside
+
+
+def test_refresh_interval_two_differs_from_block_schedule_but_matches_no_cache_at_refresh_points(tiny_w):
+    """Right after an in-block refresh the cache is the full forward of the
+    current canvas: the step that follows computes exactly what the no-cache
+    decoder computes on that canvas."""
+    pr = synth.prompts(tiny_w.cfg, 3, 1, 12)
+    dec = S.Decoder(tiny_w, pr, 16, 8, "dual")
+    prev = None
+    checked = 0
+    for ev in dec.run(S.Rule(S.FIXED_K, k=1), refresh_interval=2):
+        if ev[0] == "step" and prev is not None and prev[0] == "refresh":
+            none = S.Decoder(tiny_w, pr, 16, 8, "none")
+            none.x = ev[2].x_before.copy()
+            conf, arg, _, _, _ = none.compute(ev[1])
+            np.testing.assert_allclose(ev[2].conf, conf, rtol=1e-9, atol=1e-12)
+            np.testing.assert_array_equal(ev[2].arg, arg)
+            checked += 1
+        prev = ev
+    assert checked >= 4
 
 
 def test_dual_cache_reads_stale_suffix(tiny_w):
