@@ -128,15 +128,17 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- CPU oracle sample
-def oracle_sample(wl: configs.Workload, steps: int, refreshes: int, budget_s: float = 25.0) -> dict:
+def oracle_sample(wl: configs.Workload, steps: int, refreshes: int, refresh_frac: int = 1) -> dict:
     """Time the CPU oracle on a bounded sample of the workload and extrapolate.
 
     Sample: one transformer layer of the model at the workload's shapes - a
     DualCache denoise step over the block rows (batch*block rows attending to a
-    T-long K/V context) and a refresh forward over all T rows - plus the final
+    T-long K/V context) and a refresh forward over the T rows (or over T /
+    refresh_frac of them against all T keys, scaled up by refresh_frac: every
+    cost of a forward is linear in its query rows at fixed T) - plus the final
     norm and LM head over the block rows.  A generation's time is then
     steps*(L*layer_step + head) + refreshes*(L*layer_refresh), with the step and
-    refresh counts of the GPU run on the same workload.
+    refresh counts the GPU path takes on the same workload.
     """
     from oracle import model as OM
 
@@ -163,7 +165,8 @@ def oracle_sample(wl: configs.Workload, steps: int, refreshes: int, budget_s: fl
         return OM.attn_ffn(cfg, lw, h, q, kk, vv)
 
     h_step = rng.standard_normal((B, d)) * 0.5
-    h_all = rng.standard_normal((T, d)) * 0.5
+    n_ref = max(1, T // refresh_frac)
+    h_ref = rng.standard_normal((n_ref, d)) * 0.5
     t0 = time.perf_counter()
     reps = 0
     while True:
@@ -181,14 +184,58 @@ def oracle_sample(wl: configs.Workload, steps: int, refreshes: int, budget_s: fl
     t_head = time.perf_counter() - t0
     t0 = time.perf_counter()
     for _ in range(b):
-        layer(h_all, np.arange(T))
-    t_layer_refresh = time.perf_counter() - t0
+        layer(h_ref, np.arange(n_ref))
+    t_ref_part = time.perf_counter() - t0
+    t_layer_refresh = t_ref_part * (T / n_ref)
     step_s = cfg.n_layers * t_layer_step + t_head
     refresh_s = cfg.n_layers * t_layer_refresh
     gen_s = steps * step_s + refreshes * refresh_s
     return {"gen_s": gen_s, "step_s": step_s, "refresh_s": refresh_s, "setup_s": setup_s,
-            "sample_s": t_layer_step * reps + t_head + t_layer_refresh,
+            "sample_s": t_layer_step * reps + t_head + t_ref_part,
             "tokens_per_gen": wl.batch * wl.gen_len}
+
+
+def blas_threads() -> int | None:
+    """Threads of numpy's BLAS (threadpoolctl where installed, else the
+    OPENBLAS_NUM_THREADS / OMP_NUM_THREADS setting, else None)."""
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return None
+
+
+def oracle_sample_one_thread(workload: str, steps: int, refreshes: int, batch: int, tau: float) -> dict | None:
+    """The same sample in a fresh interpreter whose BLAS runs one thread; the
+    refresh part over an eighth of the rows (scaled up), to stay within tens
+    of seconds."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", workload,
+           "--batch", str(batch), "--tau", str(tau), "--ref-steps-per-gen", str(steps),
+           "--ref-refreshes-per-gen", str(refreshes)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+    except (OSError, subprocess.TimeoutExpired):
+        return None
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def generation_counts(wl: configs.Workload, mode: str) -> tuple:
+    """(steps, refreshes, source) per generation for the oracle's extrapolation."""
+    rec = configs.STEPS_PER_GENERATION.get(wl.name)
+    base = configs.WORKLOADS.get(wl.name)
+    if rec and mode == "dual" and base is not None and wl.tau == base.tau and wl.batch == base.batch:
+        return rec[0], rec[1], "the GPU path's measured steps and refreshes on this workload"
+    return max(1, int(round(wl.gen_len / 3.0))), wl.gen_len // wl.block, "assumed tau-bar 3 (no measured count)"
 
 
 def cpu_cores() -> int:
@@ -300,9 +347,11 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     d2h = b * wl.T * 4 + (e2e_steps // max(args.steps, 1)) * (b + 1) * 4
 
     traffic, traffic_src = measured_traffic(dom, wl.name) if mode == "dual" and b == wl.batch else (None, None)
-    # split precision keeps the K/V cache as hi/lo bf16 pairs: twice the K/V bytes
-    kv_parts = 2 if args.precision == "split" else 1
-    step_bytes = roofline.dual_step_bytes(cfg.weight_bytes_step(), kv_parts * cfg.kv_bytes(wl.T, b))
+    # algorithmic bytes count every weight and the bf16 K/V cache once; split
+    # precision also reads the K/V low halves, an implementation cost reported
+    # on its own
+    step_bytes = roofline.dual_step_bytes(cfg.weight_bytes_step(), cfg.kv_bytes(wl.T, b))
+    split_extra = cfg.kv_bytes(wl.T, b) if args.precision == "split" else 0
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -328,6 +377,8 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
             "peak_source": f"{peaks['source']} HBM copy bandwidth",
             "timing": "per-launch CUDA events around each kernel, one extra generation after the timed region",
             "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
+            "split_kv_extra_bytes": split_extra if dom == "persistent_step" else None,
+            "traffic_over_algorithmic": traffic / per_launch_bytes if traffic else None,
         },
         "step_roofline": {
             "bound": "hbm", "what": "one denoise step (all kernels, launch gaps included)",
@@ -354,14 +405,21 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
         "clocks": clk, "gpu_launches": launches,
     }
     if args.cpu_baseline and rank == 0 and world == 1:
-        samp = oracle_sample(wl, steps // args.steps, refreshes // args.steps)
+        g_steps, g_refreshes = steps // args.steps, refreshes // args.steps
+        samp = oracle_sample(wl, g_steps, g_refreshes)
+        one = oracle_sample_one_thread(wl.name, g_steps, g_refreshes, b, wl.tau)
         out["cpu_baseline"] = {
             "value": samp["tokens_per_gen"] / samp["gen_s"], "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "blas_threads": blas_threads(),
             "sample": (f"one layer of the {cfg.name} model at the workload's shapes (a DualCache step over "
                        f"{b}x{B} block rows against a {wl.T}-key context, a refresh over {wl.T} rows) plus "
                        f"the LM head; extrapolated to {cfg.n_layers} layers and to this run's "
-                       f"{steps // args.steps} steps and {refreshes // args.steps} refreshes per generation"),
+                       f"{g_steps} steps and {g_refreshes} refreshes per generation"),
+            "extrapolated": True,
             "sample_seconds": samp["sample_s"], "extrapolated_generation_s": samp["gen_s"],
+            "one_thread": ({"value": one["tokens_per_gen"] / one["gen_s"], "cores": 1, "blas_threads": 1,
+                            "sample_seconds": one["sample_s"],
+                            "sample": "the same, refresh over T/8 query rows scaled by 8"} if one else None),
         }
     state.free()
     model.free()
@@ -373,26 +431,32 @@ def run_reference(args, wl: configs.Workload, rank: int) -> dict | None:
     if rank != 0:
         return None
     cfg = wl.model
-    # per-generation step/refresh counts: the tau-bar of the random-init model
-    # measured by the GPU arm on this workload (the oracle's sample cannot
-    # decode a whole 8B generation); defaults follow gen/block blocks
-    steps = args.ref_steps_per_gen or max(1, int(round(wl.gen_len / 3.0)))
-    refreshes = wl.gen_len // wl.block
+    steps, refreshes, count_src = generation_counts(wl, args.mode)
+    if args.ref_steps_per_gen:
+        steps, count_src = args.ref_steps_per_gen, "given on the command line"
     samples = []
+    wall = []
     for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         s = oracle_sample(wl, steps, refreshes)
         if i >= args.warmup:
             samples.append(s)
+            wall.append(time.perf_counter() - t0)
     gen_s = statistics.mean(s["gen_s"] for s in samples)
     value = wl.batch * wl.gen_len / gen_s
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": gen_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "ms_per_step_kind": "extrapolated: one generation's time from a timed one-layer sample",
+        "sample_wall_ms_per_step": statistics.mean(wall) * 1e3,
         "config": {"workload": f"{wl.name}: {cfg.name}-shaped dLLM, batch {wl.batch}, prompt {wl.prompt_len}, "
                                f"gen {wl.gen_len}, block {wl.block}, tau {wl.tau}, {args.mode} cache",
-                   "global_batch": wl.batch, "seq_len": wl.T, "parallelism": "CPU oracle"},
+                   "global_batch": wl.batch, "seq_len": wl.T, "parallelism": "CPU oracle",
+                   "steps_per_generation": steps, "refreshes_per_generation": refreshes,
+                   "counts_source": count_src},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "blas_threads": blas_threads(), "extrapolated": True,
                          "sample": "one layer step + one layer refresh + LM head per bench step, extrapolated to "
                                    f"{cfg.n_layers} layers, {steps} steps and {refreshes} refreshes per generation"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -412,6 +476,9 @@ def main():
     ap.add_argument("--precision", default="split", choices=("split", "bf16"))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--ref-steps-per-gen", type=int, default=0)
+    ap.add_argument("--ref-refreshes-per-gen", type=int, default=0)
+    ap.add_argument("--oracle-sample", action="store_true",
+                    help="print one timed oracle sample as JSON (the bench runs this with a one-thread BLAS)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (profiling captures of a small case)")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
@@ -429,6 +496,9 @@ def main():
         wl = dataclasses.replace(wl, model=dataclasses.replace(wl.model, n_layers=args.layers,
                                                                name=f"{wl.model.name}-{args.layers}L"))
     rank, world, local_rank = dist_env()
+    if args.oracle_sample:
+        print(json.dumps(oracle_sample(wl, args.ref_steps_per_gen, args.ref_refreshes_per_gen, refresh_frac=8)))
+        return
     if args.impl == "reference":
         out = run_reference(args, wl, rank)
     else:

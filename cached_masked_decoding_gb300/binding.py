@@ -17,7 +17,8 @@ from .configs import ModelConfig
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libdllm.so")
 
-OK, EINVAL, ENOMEM, ECUDA, EIO, ESTATE, ETIMEOUT = range(7)
+OK, EINVAL, ENOMEM, ECUDA, EIO, ESTATE, ETIMEOUT, ECANCELLED = range(8)
+EVENT_REFRESH, EVENT_STEP, EVENT_COMMIT_FORWARD = 0, 1, 2
 CACHE_NONE, CACHE_PREFIX, CACHE_DUAL = 0, 1, 2
 MODES = {"none": CACHE_NONE, "prefix": CACHE_PREFIX, "dual": CACHE_DUAL}
 SEL_THRESHOLD, SEL_FIXED_K, SEL_FACTOR, SEL_BUDGET, SEL_SCHEDULE = 0, 1, 2, 3, 4
@@ -61,6 +62,8 @@ class Stats(ctypes.Structure):
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
+# int32 (*)(void* user, int32 event, int32 block_idx, int32 step_in_block)
+RunHook = ctypes.CFUNCTYPE(ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32)
 _I64 = ctypes.c_int64
 _F = ctypes.c_float
 
@@ -83,6 +86,7 @@ SIGNATURES = {
     "dllm_read_state": (_I32, [_P, _P, _P, _P]),
     "dllm_read_hidden": (_I32, [_P, _P]),
     "dllm_read_kv": (_I32, [_P, _I32, _P, _P]),
+    "dllm_state_set_run_hook": (_I32, [_P, RunHook, _P]),
     "dllm_state_set_trace": (_I32, [_P, _I32]),
     "dllm_read_trace": (_I32, [_P, _P, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "dllm_state_set_kernel_timing": (_I32, [_P, _I32]),
@@ -98,6 +102,8 @@ SIGNATURES = {
     "dllm_staleness": (_I32, [_P, _I32, _P, _P, _P, _P]),
     "dllm_op_attention_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
     "dllm_op_attention_tc": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
+    "dllm_op_check": (_I32, [ctypes.POINTER(_I32), _P]),
+    "dllm_op_wait_probe": (_I32, [_P, _I32, _I32, _P]),
     "dllm_op_select_commit": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(Select), _P, _P]),
     "dllm_last_error": (ctypes.c_char_p, []),
     "dllm_status_string": (ctypes.c_char_p, [_I32]),
@@ -244,6 +250,16 @@ class State:
         check(lib().dllm_run(self.h, ctypes.byref(sel), MODES.get(mode, mode), refresh_interval, ctypes.byref(st)))
         return st.as_dict()
 
+    def set_run_hook(self, fn=None):
+        """Install fn(event, block_idx, step_in_block) -> int as dllm_run's
+        observer (None removes it).  A nonzero return stops the run."""
+        if fn is None:
+            self._hook = None
+            check(lib().dllm_state_set_run_hook(self.h, RunHook(), None))
+            return
+        self._hook = RunHook(lambda _u, ev, j, spb: int(fn(ev, j, spb)))
+        check(lib().dllm_state_set_run_hook(self.h, self._hook, None))
+
     def tokens(self) -> np.ndarray:
         t = np.zeros((self.b, self.T), dtype=np.int32)
         check(lib().dllm_read_state(self.h, _ptr(t), None, None))
@@ -373,6 +389,19 @@ def op_attention_noalloc(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, b: int,
                          T: int, stream: int = 0):
     check(lib().dllm_op_attention_noalloc(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                                           ctypes.c_void_p(o_ptr), b, H, hd, R, T, ctypes.c_void_p(stream)))
+
+
+def op_check(stream: int = 0) -> int:
+    """Raise DllmError(ETIMEOUT) if a dllm_op_* kernel gave up a bounded wait
+    since the last check; returns the site code (0)."""
+    site = ctypes.c_int32()
+    check(lib().dllm_op_check(ctypes.byref(site), ctypes.c_void_p(stream)))
+    return site.value
+
+
+def op_wait_probe(flag_ptr: int, need: int, limit_us: int, stream: int = 0) -> int:
+    """Status of the bounded-wait probe (OK or ETIMEOUT), without raising."""
+    return int(lib().dllm_op_wait_probe(ctypes.c_void_p(flag_ptr), need, limit_us, ctypes.c_void_p(stream)))
 
 
 def op_select_commit(conf_ptr: int, arg_ptr: int, x_ptr: int, b: int, T: int, blk_start: int, B: int,

@@ -94,5 +94,15 @@ WORKLOADS = {
     "8b_long": Workload("8b_long", M8B, 1, 1024, 1024, 32),
     "8b_batch": Workload("8b_batch", M8B, 1, 128, 128, 32),
 }
+# Denoise steps and refreshes per generation that the GPU path takes on a
+# workload's seeded inputs (batch as listed, DualCache, the workload's tau,
+# bidirectional mask, split precision): measured on GB300, deterministic for
+# the seed.  The CPU oracle's timed sample is extrapolated with these counts,
+# so that both arms of the bench describe the same generation.
+STEPS_PER_GENERATION = {
+    "8b": (117, 8),
+    "1b": (59, 4),
+}
+
 BATCH_SWEEP = (1, 2, 4, 8, 16, 32, 64)
 TAU_SWEEP = (0.7, 0.8, 0.9, 0.95)

@@ -20,6 +20,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <set>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -545,6 +546,8 @@ struct dllm_state {
   bool block_causal = false;                  // DLLM_MASK_BLOCK_CAUSAL
   unsigned long long* d_timeline = nullptr;   // persistent-step phase timeline (diagnostics)
   bool timeline = false;
+  dllm_run_hook hook = nullptr;               // observer of dllm_run's events (nullable)
+  void* hook_user = nullptr;
 };
 
 namespace {
@@ -859,19 +862,19 @@ const CUtensorMap* act_map(dllm_state* s, const void* base, int K, int N, int BN
   return &(s->act_maps[key] = m);
 }
 
-// Same L1/shared split for the small kernels as for the GEMM and attention.
+// Same L1/shared split for the small kernels as for the GEMM and attention
+// (a per-device function attribute: set once per device).
 dllm_status pin_carveouts() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    const void* ks[] = {(const void*)embed_kernel, (const void*)merge_select_kernel};
-    for (const void* k : ks) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                           cudaSharedmemCarveoutMaxShared);
-      if (e != cudaSuccess) err = e;
-    }
-  });
-  CK(err);
+  static std::mutex mu;
+  static std::set<int> done;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count(dev)) return DLLM_OK;
+  const void* ks[] = {(const void*)embed_kernel, (const void*)merge_select_kernel};
+  for (const void* k : ks)
+    CK(cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
+  done.insert(dev);
   return DLLM_OK;
 }
 
@@ -1022,7 +1025,9 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
     ++s->launches;
   }
   if (s->trace) CK(cudaMemcpyAsync(s->trace_buf, s->h, (size_t)n * d * 4, cudaMemcpyDeviceToDevice, s->st));
-  const double kv_bytes = (double)s->b * s->T * d * 2 * 2 * (s->split ? 2 : 1);
+  // algorithmic K/V bytes: K and V once, bf16 (the split's low halves are an
+  // implementation cost, not counted)
+  const double kv_bytes = (double)s->b * s->T * d * 2 * 2;
   for (int l = 0; l < L; ++l) {
     const LayerW& w = m->layers[l];
     const bool last = l == L - 1;
@@ -1467,7 +1472,7 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
   CK(cudaMemsetAsync(s->d_flags, 0, (size_t)s->n_flags * 4, s->st));
   const double bytes = (double)s->m->cfg.n_layers * 2.0 *
                            (4.0 * d * d + 3.0 * (double)d * c.d_ffn) +
-                       2.0 * V * d + (double)s->b * s->T * d * 2 * 2 * c.n_layers * (s->split ? 2 : 1);
+                       2.0 * V * d + (double)s->b * s->T * d * 2 * 2 * c.n_layers;   // K/V once, bf16
   if (s->timing) s->kt_bytes[KC_PSTEP] += bytes;
   Timed t(s, KC_PSTEP, bytes);
   const int grid = s->m->sms;
@@ -1621,6 +1626,14 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
   long long committed = 0, active = 0;
   const bool cached = cache_mode != DLLM_CACHE_NONE;
   std::vector<int32_t> cnt(s->b);
+  // the observer sees each event after it completed; a nonzero answer stops the run
+  auto notify = [&](int event, int j, int spb) -> dllm_status {
+    if (s->hook && s->hook(s->hook_user, event, j, spb) != 0) {
+      set_error("the run hook stopped the run at event %d (block %d, step %d of the block)", event, j, spb);
+      return DLLM_ECANCELLED;
+    }
+    return DLLM_OK;
+  };
   auto timed_refresh = [&]() -> dllm_status {
     CKS(do_refresh(s, s->ev_a, s->ev_b));
     float ms = 0;
@@ -1629,7 +1642,10 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
     ++refreshes;
     return DLLM_OK;
   };
-  if (cached && s->n_blocks > 0) CKS(timed_refresh());
+  if (cached && s->n_blocks > 0) {
+    CKS(timed_refresh());
+    CKS(notify(DLLM_EVENT_REFRESH, 0, 0));
+  }
   for (int j = 0; j < s->n_blocks; ++j) {
     int spb = 0;
     for (;;) {
@@ -1640,7 +1656,10 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
         act += rem > 0;
       }
       if (!any) break;
-      if (cached && refresh_interval > 0 && spb > 0 && spb % refresh_interval == 0) CKS(timed_refresh());
+      if (cached && refresh_interval > 0 && spb > 0 && spb % refresh_interval == 0) {
+        CKS(timed_refresh());
+        CKS(notify(DLLM_EVENT_REFRESH, j, spb));
+      }
       int total = 0;
       SelectRule rs = r;
       if (r.policy == 4) rs.k = std::max(1, r.k - spb);   // steps left in this block
@@ -1652,6 +1671,7 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
       ++spb;
       committed += total;
       active += act;
+      CKS(notify(DLLM_EVENT_STEP, j, spb - 1));
     }
     max_spb = std::max(max_spb, spb);
     if (cached && j + 1 < s->n_blocks) {
@@ -1669,8 +1689,10 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
         CK(cudaEventElapsedTime(&ms, s->ev_a, s->ev_b));
         refresh_ms += ms;
         ++refreshes;
+        CKS(notify(DLLM_EVENT_COMMIT_FORWARD, j, spb));
       } else {
         CKS(timed_refresh());
+        CKS(notify(DLLM_EVENT_REFRESH, j, spb));
       }
     }
   }
@@ -1825,6 +1847,16 @@ extern "C" dllm_status dllm_read_step_timeline(const dllm_state* s, uint64_t* ou
   }
   CK(cudaStreamSynchronize(s->st));
   CK(cudaMemcpy(out, s->d_timeline, n * 8, cudaMemcpyDeviceToHost));
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_run_hook(dllm_state* s, dllm_run_hook hook, void* user) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  s->hook = hook;
+  s->hook_user = user;
   return DLLM_OK;
 }
 
@@ -2066,11 +2098,26 @@ extern "C" dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k
   return DLLM_OK;
 }
 
+// ---------------------------------------------------------------- bounded-wait probe
+namespace dllm {
+// One thread waits, with the persistent step's own dataflow wait, until
+// *flag >= need or limit_ns have passed; on expiry the wait records
+// ERR_PROBE in err and the kernel returns.  Nothing else is in flight.
+__global__ void wait_probe_kernel(const int* flag, int need, unsigned long long limit_ns, int* err) {
+  __shared__ int abort_s;
+  if (threadIdx.x == 0) {
+    abort_s = 0;
+    flag_wait_for(flag, need, &abort_s, err, limit_ns, ERR_PROBE);
+  }
+}
+}  // namespace dllm
+
 // ---------------------------------------------------------------- attention without allocation
 // Scratch of dllm_op_attention_noalloc, in static storage of this library's
 // module: the key-split partials (o, m, l) and the per-work merge counters.
 // Module load zero-fills it; each work's last-arriving split puts its counter
-// back to 0, so the counters are zero again after every completed launch.
+// back to 0, and every call also clears the counters it uses before its
+// launch.  The error word stays set until dllm_op_check reads it.
 constexpr size_t kNoAllocAttnFloats = size_t(1) << 20;   // 4 MiB of split partials
 constexpr int kNoAllocAttnWorks = 4096;                   // merge counters (b * H * query tiles)
 static __device__ __align__(256) float g_noalloc_attn_ws[kNoAllocAttnFloats];
@@ -2136,6 +2183,10 @@ extern "C" dllm_status dllm_op_attention_noalloc(const uint16_t* q, const uint16
   CUtensorMap tk, tv;
   CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H, 64));
   CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H, 64));
+  // the merge counters this launch uses start at zero even if an earlier
+  // launch gave up a bounded wait and left them counted (stream-ordered, no
+  // allocation)
+  if (a.splits > 1) CK(cudaMemsetAsync(sc.cnt, 0, works * sizeof(int), static_cast<cudaStream_t>(stream)));
   AttnParams p = {};
   p.q = q;
   p.o = out;
@@ -2157,6 +2208,51 @@ extern "C" dllm_status dllm_op_attention_noalloc(const uint16_t* q, const uint16
   CK(launch_attention(hd, a.wq, 64, tk, tv, p, dim3(a.splits, a.q_tiles * H, b), static_cast<cudaStream_t>(stream),
                       false));
   return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_op_check(int32_t* site, void* stream) {
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  int words[2] = {0, 0};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  OpWorkspace* w = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_op_mu);
+    auto it = g_op_ws.find(dev);
+    if (it != g_op_ws.end() && it->second.err) w = &it->second;
+  }
+  NoAllocScratch sc;
+  CKS(noalloc_scratch(&sc));
+  if (w) CK(cudaMemcpyAsync(&words[0], w->err, 4, cudaMemcpyDeviceToHost, st));
+  CK(cudaMemcpyAsync(&words[1], sc.err, 4, cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  if (w) CK(cudaMemsetAsync(w->err, 0, 4, st));
+  CK(cudaMemsetAsync(sc.err, 0, 4, st));
+  CK(cudaStreamSynchronize(st));
+  const int code = words[0] ? words[0] : words[1];
+  if (site) *site = code;
+  if (code != 0) {
+    set_error("a kernel-level call gave up a bounded wait (site %d)", code);
+    return DLLM_ETIMEOUT;
+  }
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_op_wait_probe(const int32_t* flag, int32_t need, int32_t limit_us, void* stream) {
+  if (!flag || limit_us < 1 || limit_us > 2000000 || (reinterpret_cast<uintptr_t>(flag) & 3) != 0) {
+    set_error("bad wait probe arguments: limit_us=%d (1 .. 2000000), flag 4-byte aligned", limit_us);
+    return DLLM_EINVAL;
+  }
+  OpWorkspace* w = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_op_mu);
+    CKS(op_workspace(&w, 1, 0, 0));
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  wait_probe_kernel<<<1, 32, 0, st>>>(flag, need, (unsigned long long)limit_us * 1000ull, w->err);
+  CK(cudaGetLastError());
+  int32_t site = 0;
+  return dllm_op_check(&site, stream);
 }
 
 extern "C" dllm_status dllm_op_select_commit(const float* conf, const int32_t* arg, int32_t* x, int32_t b, int32_t T,
@@ -2323,6 +2419,7 @@ extern "C" const char* dllm_status_string(int32_t st) {
     case DLLM_EIO: return "I/O error";
     case DLLM_ESTATE: return "invalid state";
     case DLLM_ETIMEOUT: return "kernel wait timed out";
+    case DLLM_ECANCELLED: return "stopped by the run hook";
     default: return "unknown status";
   }
 }

@@ -8,18 +8,9 @@ namespace dllm {
 template <int HD, int WQ, int KT>
 static cudaError_t go_attn(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
                            cudaStream_t st, bool pdl) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, WQ, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         AttnCfg<HD, KT>::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    // every kernel of the step asks for the same L1/shared split, so an SM
-    // never has to drain and reconfigure between them
-    e = cudaFuncSetAttribute(attn_kernel<HD, WQ, KT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = smem_attrs_once(reinterpret_cast<const void*>(attn_kernel<HD, WQ, KT>),
+                                        AttnCfg<HD, KT>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   return launch_ex(attn_kernel<HD, WQ, KT>, grid, dim3(128), AttnCfg<HD, KT>::SMEM_BYTES, st, pdl, tk, tv, p);
 }
 
@@ -40,16 +31,8 @@ cudaError_t launch_attention(int hd, int wq, int kt, const CUtensorMap& tk, cons
 template <int HD>
 static cudaError_t go_attn_tc(const CUtensorMap& tq, const CUtensorMap& tqlo, const CUtensorMap& tk,
                               const CUtensorMap& tv, const AttnParams& p, dim3 grid, cudaStream_t st, bool pdl) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         AttnTcCfg<HD>::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = smem_attrs_once(reinterpret_cast<const void*>(attn_tc_kernel<HD>), AttnTcCfg<HD>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   return launch_ex(attn_tc_kernel<HD>, grid, dim3(192), AttnTcCfg<HD>::SMEM_BYTES, st, pdl, tq, tqlo, tk, tv, p);
 }
 

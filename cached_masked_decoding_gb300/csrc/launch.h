@@ -5,11 +5,36 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "attention.cuh"
 #include "gemm.cuh"
 #include "step_kernel.cuh"
 
 namespace dllm {
+
+// A kernel's dynamic shared-memory limit and carveout are attributes of the
+// function on the current device: set them once per (kernel, device), under a
+// lock, so that host threads and devices do not race or miss them.
+inline cudaError_t smem_attrs_once(const void* kernel, int smem_bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  // every kernel of the step asks for the same L1/shared split, so an SM
+  // never has to drain and reconfigure between them
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  done.insert({kernel, dev});
+  return cudaSuccess;
+}
 
 // Launch with programmatic dependent launch allowed (pdl) on stream st.
 template <typename Kern, typename... Args>
@@ -73,16 +98,9 @@ cudaError_t launch_attention_tc(int hd, const CUtensorMap& tq, const CUtensorMap
   template <int BN>                                                                                             \
   static cudaError_t go_##NAME(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p, int grid,       \
                                cudaStream_t st, bool pdl) {                                                     \
-    static bool attr_set = false;                                                                               \
-    if (!attr_set) {                                                                                            \
-      cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                           GemmCfg<BN>::SMEM_BYTES);                                            \
-      if (e != cudaSuccess) return e;                                                                           \
-      e = cudaFuncSetAttribute(gemm_kernel<BN, KIND>, cudaFuncAttributePreferredSharedMemoryCarveout,          \
-                               cudaSharedmemCarveoutMaxShared);                                                 \
-      if (e != cudaSuccess) return e;                                                                           \
-      attr_set = true;                                                                                          \
-    }                                                                                                           \
+    const cudaError_t e = smem_attrs_once(reinterpret_cast<const void*>(gemm_kernel<BN, KIND>),                 \
+                                          GemmCfg<BN>::SMEM_BYTES);                                             \
+    if (e != cudaSuccess) return e;                                                                             \
     return launch_ex(gemm_kernel<BN, KIND>, dim3(grid), dim3(192), GemmCfg<BN>::SMEM_BYTES, st, pdl, a, b, blo, p);  \
   }                                                                                                             \
   cudaError_t launch_gemm_##NAME(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, const GemmParams& p,       \

@@ -6,16 +6,9 @@ namespace dllm {
 
 template <int BN>
 static cudaError_t go_step_64(const StepArgs& a, int grid, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(step_kernel<BN, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         StepCfg<BN, 64>::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(step_kernel<BN, 64>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = smem_attrs_once(reinterpret_cast<const void*>(step_kernel<BN, 64>),
+                                        StepCfg<BN, 64>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);

@@ -125,9 +125,10 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
 }
 
 // Wait until *f >= need (acquire), then order later TMA reads after it.
-// Bounded by kWaitLimitNs; gives up early once this CTA raised *abort or any
-// CTA recorded an error.
-__device__ __forceinline__ bool flag_wait(const int* f, int need, volatile int* abort, int* err) {
+// Bounded by limit_ns; gives up early once this CTA raised *abort or any
+// CTA recorded an error; on giving up records `site` in err.
+__device__ __forceinline__ bool flag_wait_for(const int* f, int need, volatile int* abort, int* err,
+                                              unsigned long long limit_ns, int site) {
   if (ld_acquire_gpu(f) < need) {
     const unsigned long long t0 = globaltimer();
     for (;;) {
@@ -137,15 +138,19 @@ __device__ __forceinline__ bool flag_wait(const int* f, int need, volatile int* 
         *abort = 1;
         return false;
       }
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
-        record_error(err, ERR_STEP_FLAG);
+        record_error(err, site);
         return false;
       }
     }
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
   return true;
+}
+
+__device__ __forceinline__ bool flag_wait(const int* f, int need, volatile int* abort, int* err) {
+  return flag_wait_for(f, need, abort, err, kWaitLimitNs, ERR_STEP_FLAG);
 }
 
 // Wait until *f0 >= need0 and *f1 >= need1 (f1 may be null).  The first

@@ -45,7 +45,8 @@ typedef enum dllm_status {
     DLLM_EIO = 4,       /* weight file missing, short or malformed */
     DLLM_ESTATE = 5,    /* a step committed nothing while MASK remained, or the
                            call does not fit the state (e.g. wrong block) */
-    DLLM_ETIMEOUT = 6   /* a kernel gave up a bounded wait; outputs are invalid */
+    DLLM_ETIMEOUT = 6,  /* a kernel gave up a bounded wait; outputs are invalid */
+    DLLM_ECANCELLED = 7 /* dllm_run stopped because its run hook returned nonzero */
 } dllm_status;
 
 typedef enum dllm_cache_mode {
@@ -128,7 +129,10 @@ dllm_status dllm_model_create(const dllm_config* cfg, dllm_model** out);
 dllm_status dllm_model_set_tensor(dllm_model* m, int32_t tensor, int32_t layer,
                                   const uint16_t* src, int64_t count, int32_t src_on_device);
 
-/* Read a weight file (8-byte magic "DLLMW001", int32 n_layers, d_model,
+/* Read a weight file and upload it: the model-loading call the decoder's
+ * interface starts from (a trained model's weights in the pages' setting;
+ * here seeded random-init weights of the same shapes).  Format: 8-byte magic
+ * "DLLMW001", int32 n_layers, d_model,
  * n_heads, head_dim, d_ffn, vocab, float32 rope_theta, norm_eps, then every
  * tensor's bf16 bits: embed; per layer attn_norm wq wk wv wo ffn_norm wg wu wd;
  * final_norm; lm_head) and upload it.  DLLM_EIO on a short/malformed file. */
@@ -140,7 +144,9 @@ void dllm_free_model(dllm_model* m);
 /* ------------------------------------------------------------------ state */
 
 /* Create the decoding state of b sequences: canvas x = prompt ++ MASK*gen_len
- * (Algorithm 1, step 1), K/V cache [layer][K|V][b][head][T][head_dim] bf16 with
+ * (Algorithm 1 of the Fast-dLLM reading notes, section 3, step 1: append
+ * gen_len MASK positions to the prompt; the tutorial's sampler starts from the
+ * same all-MASK answer), K/V cache [layer][K|V][b][head][T][head_dim] bf16 with
  * T = P + gen_len, activations and workspaces.  prompts: host [b][P] int32, or
  * NULL to leave the prompt part for dllm_state_set_prompts_device.
  * gen_len % block == 0 and 1 <= block <= 256 are required.  cuda_stream is a
@@ -187,6 +193,25 @@ dllm_status dllm_denoise_step_ex(dllm_state* s, int32_t block_idx, const dllm_se
 dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t cache_mode,
                      int32_t refresh_interval, dllm_stats* stats);
 
+/* Observer of dllm_run (and of nothing else): called on the calling thread
+ * after each event of the loop has completed on the GPU, with the event kind,
+ * the block index j and the step's index inside the block (for a refresh: the
+ * number of steps the block had taken).  Events: DLLM_EVENT_REFRESH after the
+ * prefill and every refresh (block boundary, or the refresh interval inside a
+ * block), DLLM_EVENT_STEP after every denoise step, DLLM_EVENT_COMMIT_FORWARD
+ * after the forward over a finished block that replaces the block-boundary
+ * refresh under the block-causal mask.  Inside the hook the state may be read
+ * (dllm_read_state, dllm_read_hidden, dllm_read_kv) but not changed.  A
+ * nonzero return stops the run: dllm_run returns DLLM_ECANCELLED, with the
+ * canvas as the last completed event left it.  Use: stream committed tokens
+ * to a caller, or follow the loop's decisions step by step. */
+typedef enum dllm_event { DLLM_EVENT_REFRESH = 0, DLLM_EVENT_STEP = 1, DLLM_EVENT_COMMIT_FORWARD = 2 } dllm_event;
+typedef int32_t (*dllm_run_hook)(void* user, int32_t event, int32_t block_idx, int32_t step_in_block);
+
+/* Install (or with hook NULL remove) the state's run hook; user is passed back
+ * unchanged.  It stays installed until changed or the state is freed. */
+dllm_status dllm_state_set_run_hook(dllm_state* s, dllm_run_hook hook, void* user);
+
 /* End-to-end call: prompts (host [b][P]) in, answers (host [b][gen_len]) out.
  * Creates a state on a private stream, runs Algorithm 1 with the threshold
  * rule, copies the answer back and frees the state. */
@@ -194,8 +219,10 @@ dllm_status dllm_generate(dllm_model* m, const int32_t* prompts, int32_t b, int3
                           int32_t gen_len, int32_t block, float tau, int32_t cache_mode,
                           int32_t* out_tokens, dllm_stats* stats);
 
-/* Copy state to the host: tokens [b][T] (the whole canvas), and the last
- * step's conf [b][block] (float32 max-softmax) and arg [b][block] (argmax id).
+/* Copy state to the host: tokens [b][T] (the whole canvas; Algorithm 1 of the
+ * Fast-dLLM reading notes, section 3, returns its answer part), and the last
+ * step's conf [b][block] (float32 max-softmax c_i) and arg [b][block] (argmax
+ * y_i), the candidates and confidences of Algorithm 2 (section 4, steps 1-2).
  * Any pointer may be NULL. */
 dllm_status dllm_read_state(const dllm_state* s, int32_t* tokens, float* conf, int32_t* arg);
 
@@ -222,8 +249,9 @@ dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode);
 /* DualCache steps with at most 128 activation rows (b * block <= 128, block
  * <= 32) run by default as one persistent cooperative launch: one CTA per SM
  * walks through every phase of the step (embedding, each layer's projections
- * and attention, LM head, merge and selection) with grid barriers between
- * them, and streams the next phase's weights while a phase finishes.
+ * and attention, LM head, merge and selection), ordered by dataflow flags (a
+ * consumer waits only for the row tiles or heads it reads, no grid-wide
+ * barrier), and streams the next phase's weights while a phase finishes.
  * enable 0 selects one launch per kernel instead (same arithmetic except the
  * attention key split; tracing always uses it). */
 dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable);
@@ -321,18 +349,19 @@ dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k_cache, con
                                  int32_t T, void* cuda_stream);
 
 /* dllm_op_attention with no allocation of any kind.  The pages have no
- * counterpart: the operation is the same non-causal attention (eq. 3 of the
- * Fast-dLLM reading notes, section 2), same arguments, layouts and output,
- * bit-identical to dllm_op_attention for every shape it accepts.  What
- * differs is where the scratch lives.  dllm_op_attention grows a
- * library-owned workspace with cudaMalloc + cudaMemset the first time a shape
- * needs more; this variant uses a fixed scratch in static device storage of
- * the library (key-split partials: 1 Mi floats = 4 MiB; merge counters: 4096)
- * and never calls cudaMalloc, cudaFree or an allocating library.  It serves
- * callers that must not allocate device memory at call time: a caller whose
- * device memory is fully reserved up front (weights and K/V pools sized to
- * the card), or one that issues work where an allocation, or the device-wide
- * synchronisation a cudaMalloc/cudaMemset may imply, is not allowed.
+ * counterpart to this entry point: it computes the same attention as
+ * dllm_op_attention, with the same arguments, layouts and output, and is
+ * bit-identical to it for every shape it accepts.  What differs is where the
+ * scratch lives.  dllm_op_attention grows a library-owned workspace with
+ * cudaMalloc + cudaMemset the first time a shape needs more; this variant uses
+ * a fixed scratch in static device storage of the library (key-split
+ * partials: 1 Mi floats = 4 MiB; merge counters: 4096; every device that
+ * loads the library holds it until the process exits) and never calls
+ * cudaMalloc, cudaFree or an allocating library.  It serves callers that must
+ * not allocate device memory at call time: a caller whose device memory is
+ * fully reserved up front (weights and K/V pools sized to the card), or one
+ * that issues work where an allocation, or the device-wide synchronisation a
+ * cudaMalloc may imply, is not allowed.
  *  - Set-up: the first call on each device looks up the scratch's device
  *    address (cudaGetSymbolAddress with that device current) and the driver's
  *    tensor-map entry point; make that first call before any stream capture.
@@ -342,9 +371,11 @@ dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k_cache, con
  *    returns DLLM_EINVAL, launches nothing and names the limit in
  *    dllm_last_error(); use dllm_op_attention for it.  The 8B DualCache block
  *    (b=1, H=32, hd=128, R=32, T=768) fits.
- *  - Zero state: the merge counters must be zero when a launch starts.  They
- *    are zero at library load and every completed launch leaves them zero; a
- *    launch that ended in a bounded-wait timeout leaves them undefined.
+ *  - Zero state: each call clears the merge counters it uses (a
+ *    cudaMemsetAsync on the caller's stream) before its launch, so a call
+ *    after one that gave up a bounded wait starts clean.
+ *  - Errors: a launch that gives up a bounded wait sets the scratch's error
+ *    word; dllm_op_check reports it (DLLM_ETIMEOUT) and clears it.
  *  - Concurrency: all calls on a device share the one scratch.  Calls ordered
  *    on one stream are safe; calls that may overlap (different streams, or
  *    different host threads without ordering) race on the scratch and give
@@ -354,6 +385,24 @@ dllm_status dllm_op_attention_noalloc(const uint16_t* q, const uint16_t* k_cache
                                       const uint16_t* v_cache, uint16_t* out, int32_t b,
                                       int32_t H, int32_t hd, int32_t R, int32_t T,
                                       void* cuda_stream);
+
+/* Synchronise cuda_stream, then report whether any kernel launched by the
+ * dllm_op_* calls on the current device (the no-alloc attention included)
+ * gave up a bounded wait since the last check: DLLM_ETIMEOUT with the wait's
+ * site code in *site (nullable), else DLLM_OK with *site = 0.  Clears the
+ * error words it read.  Outputs of a call that timed out are invalid.
+ * Allocates nothing. */
+dllm_status dllm_op_check(int32_t* site, void* cuda_stream);
+
+/* Failure detection without a fault: one GPU thread waits, with the same
+ * bounded dataflow wait the persistent step uses between its phases, until
+ * the device int32 *flag reaches need or limit_us microseconds (1 ..
+ * 2,000,000) have passed.  Synchronous; returns DLLM_OK if the flag was
+ * reached and DLLM_ETIMEOUT if the wait gave up (through dllm_op_check, which
+ * also clears the error word, so the next call starts clean).  With a flag
+ * that nothing raises it exercises the give-up path: error word set, the
+ * kernel returns, the context stays usable. */
+dllm_status dllm_op_wait_probe(const int32_t* flag, int32_t need, int32_t limit_us, void* cuda_stream);
 
 /* The selection/commit kernel alone: given conf [b][B] float32 and arg [b][B]
  * int32 (device), select on the MASK positions x[s][blk_start .. +B) of the

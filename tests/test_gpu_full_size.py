@@ -17,7 +17,7 @@ from cached_masked_decoding_gb300 import binding, configs, synth
 from gpu_util import torch_cuda
 from oracle import model as OM
 from oracle import sampler as OS
-from parity import TOL, conf_tol, logit_shift, run_synced
+from parity import TOL, Report, conf_tol, run_synced
 
 pytestmark = pytest.mark.gpu
 
@@ -60,8 +60,31 @@ def test_1b_generation_trajectory(torch):
     dec = OS.Decoder(OM.load_weights(cfg, wl.seed), pr, wl.gen_len, wl.block, "dual")
     rep = run_synced(st, dec, OS.Rule(OS.THRESHOLD, wl.tau), "dual")
     print("1b:", rep)
+    rep.log(workload="1b", T=wl.T)
     assert rep.steps >= wl.gen_len // wl.block
     assert (st.tokens()[:, wl.prompt_len:] != cfg.mask_id).all()
+    st.free()
+    gm.free()
+
+
+def test_1b_long_context_two_blocks(torch):
+    """T = 2048 (the long-output shape: prompt 1024, gen 1024, block 32) on the
+    1B-shaped model through the persistent step: the prefill refresh, block 0
+    to completion, the block-boundary refresh and block 1, under the
+    trajectory-sync rule.  The step's attention then splits 2048 keys 8 ways
+    (256 keys, eight 32-key tiles per item), past every other tested shape."""
+    cfg = configs.M1B
+    wl = configs.Workload("1b_long", cfg, 1, 1024, 1024, 32)
+    gm = binding.Model.from_synth(cfg, seed=wl.seed)
+    pr = synth.prompts(cfg, wl.seed, wl.batch, wl.prompt_len)
+    st = binding.State(gm, pr, wl.batch, wl.prompt_len, wl.gen_len, wl.block)
+    st.set_persistent(True)
+    dec = OS.Decoder(OM.load_weights(cfg, wl.seed), pr, wl.gen_len, wl.block, "dual")
+    rep = run_synced(st, dec, OS.Rule(OS.THRESHOLD, wl.tau), "dual", max_blocks=2)
+    print("1b T=2048:", rep)
+    rep.log(workload="1b_long", T=wl.T)
+    assert rep.refreshes == 2
+    assert (st.tokens()[:, wl.prompt_len:wl.prompt_len + 2 * wl.block] != cfg.mask_id).all()
     st.free()
     gm.free()
 
@@ -95,10 +118,9 @@ def test_8b_refresh_and_first_step(torch):
     assert rel.max() <= 1e-2, f"final hidden relative error {rel.max():.3e}"
     err = np.abs(conf_g[0].astype(np.float64) - conf_o[0])
     assert err.max() <= conf_tol(cfg), f"max-prob error {err.max():.3e}"
-    for i in np.flatnonzero(arg_g[0] != arg_o[0]):
-        shift = logit_shift(dec, h_g[0, i:i + 1], hb[0, i:i + 1], np.array([arg_g[0, i]]))[0] - \
-            logit_shift(dec, h_g[0, i:i + 1], hb[0, i:i + 1], np.array([arg_o[0, i]]))[0]
-        assert margin[0, i] < TOL + abs(shift), f"argmax differs at position {i} with margin {margin[0, i]:.3e}"
+    mism = np.flatnonzero(arg_g[0] != arg_o[0])
+    for i in mism:
+        assert margin[0, i] < TOL, f"argmax differs at position {i} with oracle margin {margin[0, i]:.3e}"
     # the commit is the threshold rule on the GPU's own confidences
     s = wl.prompt_len
     elig = np.ones(wl.block, dtype=bool)
@@ -107,4 +129,9 @@ def test_8b_refresh_and_first_step(torch):
     expect[s + np.flatnonzero(sel)] = arg_g[0, np.flatnonzero(sel)]
     np.testing.assert_array_equal(x_after[0], expect)
     assert int(cnt.sum()) == int(sel.sum()) >= 1
-    print(f"8b: max conf err {err.max():.2e}, hidden rel {rel.max():.2e}, committed {int(cnt.sum())}")
+    rep = Report()
+    rep.steps, rep.refreshes, rep.decisions, rep.arg_near_ties = 1, 1, wl.block, int(mism.size)
+    rep.max_conf_err, rep.max_hidden_rel = float(err.max()), float(rel.max())
+    rep.log(workload="8b", T=wl.T)
+    print(f"8b: max conf err {err.max():.2e}, hidden rel {rel.max():.2e}, committed {int(cnt.sum())}, "
+          f"argmax near ties {mism.size}")

@@ -8,7 +8,7 @@ from cached_masked_decoding_gb300 import binding, configs, synth
 from gpu_util import torch_cuda
 from oracle import model as OM
 from oracle import sampler as OS
-from parity import conf_tol, run_synced
+from parity import conf_tol, run_loop_synced, run_synced
 
 pytestmark = pytest.mark.gpu
 
@@ -232,20 +232,59 @@ def test_run_is_deterministic_and_generate_agrees(gmodel):
     assert stats["steps"] == outs[0][3]["steps"] and stats["tau_bar"] > 0
 
 
-def test_refresh_every_step_equals_no_cache_on_gpu(gmodel):
-    """Refreshing before every step makes DualCache read exactly the no-cache K/V:
-    the trajectories agree (the GPU computes both; near ties aside they match)."""
+def test_refresh_every_step_equals_no_cache_on_gpu(gmodel, omodel):
+    """Invariant (iv) of the cached decoders: refreshing before every step makes
+    DualCache read exactly the K/V a no-cache forward computes.  dllm_run with
+    refresh interval 1 is followed step by step against the oracle's no-cache
+    decoder: every step of the cached GPU run must be the no-cache step on
+    the same canvas, under the trajectory-sync rule (near ties counted)."""
     P, gen, B = 32, 32, 16
     pr = synth.prompts(CFG, 2, 1, P)
     st = binding.State(gmodel, pr, 1, P, gen, B)
-    st.run(binding.make_select(binding.SEL_THRESHOLD, 0.9), "none")
-    t_none = st.tokens()
+    dec = OS.Decoder(omodel, pr, gen, B, "none")
+    rep, stats = run_loop_synced(st, dec, RULES["threshold"], "dual", refresh_interval=1, ignore_refreshes=True)
+    print(rep)
+    # the prefill, one refresh before every step but a block's first, and one
+    # at each of the n_blocks - 1 block boundaries: as many as steps
+    assert stats["refreshes"] == stats["steps"]
     st.free()
+
+
+@pytest.mark.parametrize("mode", ["dual", "prefix", "none"])
+@pytest.mark.parametrize("rule", ["threshold", "schedule"])
+def test_run_loop_matches_oracle(gmodel, omodel, mode, rule):
+    """dllm_run - the block/step loop the bench times, with its refresh
+    points, the skipped refresh after the last block, the lockstep batch and
+    the scheduled rule's countdown - against the oracle's Algorithm 1, event
+    by event (notes, section 3, Algorithm 1)."""
+    P, gen, B, b = 24, 48, 16, 2
+    pr = synth.prompts(CFG, 8, b, P)
+    st = binding.State(gmodel, pr, b, P, gen, B)
+    dec = OS.Decoder(omodel, pr, gen, B, mode)
+    rep, stats = run_loop_synced(st, dec, RULES[rule], mode)
+    print(mode, rule, rep)
+    assert stats["refreshes"] == (gen // B if mode != "none" else 0)
+    assert stats["committed"] == b * gen and (st.tokens()[:, P:] != CFG.mask_id).all()
+    if rule == "schedule":
+        assert stats["steps"] == RULES[rule].k * (gen // B)
+    st.free()
+
+
+@pytest.mark.parametrize("r", [2, 4])
+def test_refresh_interval_matches_oracle(gmodel, omodel, r):
+    """The refresh interval separated from the block schedule (notes, section
+    11, Table 10): dllm_run(refresh_interval = r) against the oracle with the
+    same interval, event by event (the in-block refreshes included)."""
+    P, gen, B = 32, 48, 16
+    pr = synth.prompts(CFG, 9, 1, P)
     st = binding.State(gmodel, pr, 1, P, gen, B)
-    st.run(binding.make_select(binding.SEL_THRESHOLD, 0.9), "dual", refresh_interval=1)
-    t_dual = st.tokens()
+    dec = OS.Decoder(omodel, pr, gen, B, "dual")
+    rep, stats = run_loop_synced(st, dec, OS.Rule(OS.FIXED_K, k=2), "dual", refresh_interval=r)
+    print(r, rep)
+    # fixed k = 2: B / 2 steps per block, a refresh before every r-th of them
+    inside = -(-(B // 2) // r) - 1
+    assert stats["refreshes"] == 1 + (gen // B - 1) + (gen // B) * inside
     st.free()
-    assert (t_none == t_dual).mean() > 0.95
 
 
 def test_edge_cases(gmodel, omodel):
@@ -352,16 +391,32 @@ def test_block_causal_trajectory_matches_oracle(gmodel, omodel, mode):
 def test_block_causal_commit_forward_keeps_cache_exact(gmodel, omodel):
     """With the block-causal mask dllm_run replaces each block-boundary refresh
     by one forward over the finished block; the cache stays exact, so the
-    DualCache run (persistent step) decodes what the oracle's no-cache decoder
-    does under the same mask."""
+    DualCache run (persistent step) must decode what the oracle's no-cache
+    decoder does under the same mask, step by step under the
+    trajectory-sync rule."""
     P, gen, B = 32, 64, 16
     pr = synth.prompts(CFG, 7, 2, P)
     st = binding.State(gmodel, pr, 2, P, gen, B)
     st.set_mask("block_causal")
-    stats = st.run(binding.make_select(binding.SEL_THRESHOLD, 0.9), "dual")
-    assert stats["refreshes"] == gen // B       # the prefill plus one commit forward per finished block but the last
     ref = OS.Decoder(omodel, pr, gen, B, "none", mask="block_causal")
-    toks, _ = ref.generate(OS.Rule(OS.THRESHOLD, 0.9))
-    got = st.tokens()[:, P:]
-    assert (got == toks).mean() > 0.95, f"agreement {(got == toks).mean():.3f}"
+    rep, stats = run_loop_synced(st, ref, RULES["threshold"], "dual", ignore_refreshes=True)
+    print(rep)
+    assert stats["refreshes"] == gen // B       # the prefill plus one commit forward per finished block but the last
+    assert (st.tokens()[:, P:] != CFG.mask_id).all()
+    st.free()
+
+
+@pytest.mark.parametrize("b,B", [(16, 16), (64, 16), (16, 32)])
+def test_per_kernel_decode_batches(gmodel, omodel, b, B):
+    """Batches over 128 block rows leave the persistent step for one launch
+    per kernel: GEMMs over 256-1024 activation rows in several row tiles and
+    the key-split attention over b x B query rows.  Whole generations against
+    the oracle under the trajectory-sync rule."""
+    P, gen = 32, 2 * B
+    pr = synth.prompts(CFG, 10 + b, b, P)
+    st = binding.State(gmodel, pr, b, P, gen, B)
+    dec = OS.Decoder(omodel, pr, gen, B, "dual")
+    rep = run_synced(st, dec, RULES["threshold"], "dual")
+    print(b, B, rep)
+    assert (st.tokens()[:, P:] != CFG.mask_id).all()
     st.free()
