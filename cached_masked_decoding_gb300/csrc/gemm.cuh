@@ -236,7 +236,21 @@ __device__ __forceinline__ void warp_transpose_argmax(float (&v)[32], int (&id)[
 // tile in the exchange buffer: 16-byte aligned rows, 128 * 33 floats in all.
 constexpr int kStageLd = 132;
 
-// Eight consecutive floats as bf16 pairs: hi = bf16(x), lo = bf16(x - hi).
+// Eight floats as bf16 pairs: hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split8v(const float (&f)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint16_t b0 = f32_to_bf16_bits(f[2 * t]), b1 = f32_to_bf16_bits(f[2 * t + 1]);
+    h[t] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+    l[t] = (uint32_t)f32_to_bf16_bits(f[2 * t] - bf16_bits_to_f32(b0)) |
+           ((uint32_t)f32_to_bf16_bits(f[2 * t + 1] - bf16_bits_to_f32(b1)) << 16);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Eight consecutive floats (16-byte aligned) as bf16 pairs.
 __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
   const float4 a = *reinterpret_cast<const float4*>(x);
   const float4 b = *reinterpret_cast<const float4*>(x + 4);
@@ -262,7 +276,8 @@ __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
 // would force every later load to wait for it.
 template <int KIND>
 __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], int m_idx, int r0, int l128,
-                                          int lane, int q, float* xch, const float* rs, float* red) {
+                                          int lane, int q, float* xch, const float* rs, float* red,
+                                          const float* h_pre = nullptr) {
   const int m = m_idx * 128 + l128;
   const int N = p.N;
   if constexpr (KIND == GEMM_PLAIN) {
@@ -351,20 +366,36 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
     const int fb = m_idx * 128 + lane * 4;
     const uint2 graw = __ldg(reinterpret_cast<const uint2*>(p.g_next + fb));
     float hv[8][4];
+    if (h_pre) {
+      // the rows r0.. were copied to h_pre ([32][128]) by this thread group's
+      // asynchronous copies; the barrier below makes every thread's visible
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int r = r0 + q + 4 * k;
-      const float4 x = r < N ? __ldcg(reinterpret_cast<const float4*>(&h[(long long)r * d + fb]))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      hv[k][0] = x.x;
-      hv[k][1] = x.y;
-      hv[k][2] = x.z;
-      hv[k][3] = x.w;
+      for (int k = 0; k < 8; ++k) {
+        const int r = r0 + q + 4 * k;
+        const float4 x = r < N ? __ldcg(reinterpret_cast<const float4*>(&h[(long long)r * d + fb]))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        hv[k][0] = x.x;
+        hv[k][1] = x.y;
+        hv[k][2] = x.z;
+        hv[k][3] = x.w;
+      }
     }
     named_bar_sync(1, 128);
 #pragma unroll
     for (int c = 0; c < 32; ++c) xch[c * kStageLd + l128] = v[c];
     named_bar_sync(1, 128);
+    if (h_pre) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 x = *reinterpret_cast<const float4*>(h_pre + (q + 4 * k) * 128 + lane * 4);
+        hv[k][0] = x.x;
+        hv[k][1] = x.y;
+        hv[k][2] = x.z;
+        hv[k][3] = x.w;
+      }
+    }
     const float g4[4] = {__uint_as_float(graw.x << 16), __uint_as_float(graw.x & 0xffff0000u),
                          __uint_as_float(graw.y << 16), __uint_as_float(graw.y & 0xffff0000u)};
 #pragma unroll
@@ -405,40 +436,37 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
       if (lane == 0 && r < N && ro >= 0) sso[(long long)ro * (d >> 7) + m_idx] = sq;
     }
   } else if constexpr (KIND == GEMM_SWIGLU) {
+    // The tile's 128 weight rows are 64 gate rows then the 64 matching up
+    // rows.  Staged as [feature][row]; then every thread forms 16 outputs of
+    // one activation row, silu(gate) * up with the fast reciprocal (an IEEE
+    // division here cost about 2 us per tile), and stores them as bf16 pairs.
     uint16_t* __restrict__ act = p.act;
     uint16_t* __restrict__ act_lo = p.act_lo;
     const int ld = p.act_ld;
-#pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] *= rs[c];
     named_bar_sync(1, 128);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) xch[l128 * 33 + c] = v[c];
+    for (int c = 0; c < 32; ++c) xch[l128 * 33 + c] = v[c] * rs[c];
     named_bar_sync(1, 128);
-    float a[32];
-    if (l128 < 64) {
+    const int row = l128 >> 2, j0 = (l128 & 3) * 16;
+    const int r = r0 + row;
+    float a[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float gt = v[c], up = xch[(l128 + 64) * 33 + c];
-        a[c] = gt / (1.0f + __expf(-gt)) * up;
+    for (int i = 0; i < 16; ++i) {
+      const float gt = xch[(j0 + i) * 33 + row], up = xch[(j0 + i + 64) * 33 + row];
+      a[i] = __fdividef(gt, 1.0f + __expf(-gt)) * up;
+    }
+    if (r < N) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float f8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f8[i] = a[hf * 8 + i];
+        uint4 hi, lo;
+        split8v(f8, hi, lo);
+        const long long o = (long long)r * ld + m_idx * 64 + j0 + hf * 8;
+        *reinterpret_cast<uint4*>(&act[o]) = hi;
+        if (act_lo) *reinterpret_cast<uint4*>(&act_lo[o]) = lo;
       }
-    }
-    // staged as [32 rows][64 features], stored 8 features per thread and store
-    named_bar_sync(1, 128);
-    if (l128 < 64) {
-#pragma unroll
-      for (int c = 0; c < 32; ++c) xch[c * kStageLd + l128] = a[c];
-    }
-    named_bar_sync(1, 128);
-#pragma unroll
-    for (int e = l128; e < 32 * 8; e += 128) {
-      const int row = e >> 3, f8 = (e & 7) * 8;
-      const int r = r0 + row;
-      if (r >= N) continue;
-      uint4 hi, lo;
-      split8(xch + row * kStageLd + f8, hi, lo);
-      const long long o = (long long)r * ld + m_idx * 64 + f8;
-      *reinterpret_cast<uint4*>(&act[o]) = hi;
-      if (act_lo) *reinterpret_cast<uint4*>(&act_lo[o]) = lo;
     }
   } else if constexpr (KIND == GEMM_LMHEAD) {
     const int M = p.M;

@@ -103,7 +103,12 @@ struct StepCfg {
   // the ring, idle in ATTN phases
   static constexpr int AST = (STAGES * B_BYTES) / (4 * ATT_TILE) >= 2 ? 2 : 1;
   static constexpr int TMEM_COLS = 2 * B_ROWS;
-  static constexpr int SMEM_BYTES = FIXED + STAGES * STAGE_BYTES;
+  // with 32 activation rows, the residual rows of a RESID tile (32 x 128
+  // floats) fit in the shared memory left over: they are copied there while
+  // the tile's MMAs stream, so the epilogue does not wait for L2 reads
+  static constexpr int H_BYTES = 32 * 128 * 4;
+  static constexpr bool H_PRE = BN == 32 && FIXED + STAGES * STAGE_BYTES + H_BYTES <= MAX_SMEM;
+  static constexpr int SMEM_BYTES = FIXED + STAGES * STAGE_BYTES + (H_PRE ? H_BYTES : 0);
   static_assert(STAGES >= 4, "ring too shallow");
   static_assert(AST * 4 * ATT_TILE <= STAGES * B_BYTES, "attention tiles fit the activation half of the ring");
   static_assert(32 * HD * 4 + 64 * 4 <= XCH_BYTES, "attention scratch");
@@ -112,12 +117,6 @@ struct StepCfg {
 };
 
 // ---------------------------------------------------------------- dataflow flags
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -127,6 +126,12 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
 // Wait until *f >= need (acquire), then order later TMA reads after it.
 // Bounded by limit_ns; gives up early once this CTA raised *abort or any
 // CTA recorded an error; on giving up records `site` in err.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ bool flag_wait_for(const int* f, int need, volatile int* abort, int* err,
                                               unsigned long long limit_ns, int site) {
   if (ld_acquire_gpu(f) < need) {
@@ -175,11 +180,14 @@ __device__ __forceinline__ bool flags_wait2(const int* f0, int need0, const int*
 
 // Raise two counters by one with release semantics.  Called by one thread
 // after a barrier over the threads whose writes it publishes; the proxy fence
-// makes those writes visible to other CTAs' TMA reads.
+// makes those writes visible to other CTAs' TMA reads.  One acq_rel fence
+// followed by two relaxed reductions releases both (two release reductions
+// would wait for the stores twice: about 0.6 us each).
 __device__ __forceinline__ void flag_publish(int* a, int* b) {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a) : "memory");
-  if (b) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(b) : "memory");
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(a) : "memory");
+  if (b) asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(b) : "memory");
 }
 
 // ---------------------------------------------------------------- worker phases
@@ -286,6 +294,7 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
   int* bcast = reinterpret_cast<int*>(tmem_slot + 2);
   int* abcast = reinterpret_cast<int*>(tmem_slot + 3);
   volatile int* att_done = reinterpret_cast<volatile int*>(tmem_slot + 4);   // layers whose attention items this CTA finished
+  float* hs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xch) + C::XCH_BYTES + 1536);   // [32][128] (H_PRE)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x, cta = blockIdx.x;
@@ -552,6 +561,28 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
         const int kc = p.kc, n_tiles = p.n_tiles;
         const bool split = BN <= 128 && p.split != 0;
         const uint32_t start = sk_begin((uint32_t)cta, uG, total), end = sk_begin((uint32_t)cta + 1, uG, total);
+        // RESID: the first tile whose epilogue this CTA runs (the first tile
+        // starting in its range) has its residual rows copied to shared memory
+        // now; they were written by an earlier phase whose completion this
+        // CTA's workers have already acquired
+        int h_tile = -1;
+        if constexpr (C::H_PRE) {
+          if (P.gemm_kind == GEMM_RESID) {
+            const uint32_t tf = (start + (uint32_t)kc - 1) / (uint32_t)kc;
+            if (tf * (uint32_t)kc < end) {
+              h_tile = (int)tf;
+              const int hm = h_tile / n_tiles, hr0 = (h_tile - hm * n_tiles) * BN;
+              for (int e = l128; e < 32 * 32; e += 128) {
+                const int row = e >> 5, c4 = (e & 31) * 4;
+                if (hr0 + row < p.N)
+                  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(hs + row * 128 + c4)),
+                               "l"(p.h + (long long)(hr0 + row) * p.d_model + hm * 128 + c4)
+                               : "memory");
+              }
+              asm volatile("cp.async.commit_group;" ::: "memory");
+            }
+          }
+        }
         uint32_t g = start;
         ChunkPos cp;
         cp.init(start, kc, n_tiles);
@@ -616,7 +647,7 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
               }
               switch (P.gemm_kind) {
                 case GEMM_QKV: epi_chunk<GEMM_QKV>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
-                case GEMM_RESID: epi_chunk<GEMM_RESID>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
+                case GEMM_RESID: epi_chunk<GEMM_RESID>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red, tile == h_tile ? hs : nullptr); break;
                 case GEMM_SWIGLU: epi_chunk<GEMM_SWIGLU>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
                 default: epi_chunk<GEMM_LMHEAD>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
               }
@@ -734,7 +765,7 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
                 if (tl && l128 == 0 && c0 == 0) tl[ph * kTimelineSlots + 8] = globaltimer();
                 switch (P.gemm_kind) {
                   case GEMM_QKV: epi_chunk<GEMM_QKV>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
-                  case GEMM_RESID: epi_chunk<GEMM_RESID>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
+                  case GEMM_RESID: epi_chunk<GEMM_RESID>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red, tile == h_tile ? hs : nullptr); break;
                   case GEMM_SWIGLU: epi_chunk<GEMM_SWIGLU>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
                   default: epi_chunk<GEMM_LMHEAD>(p, v, m_idx, n_idx * BN + c0, l128, lane, q, xch, rs_s + c0, red); break;
                 }
@@ -752,6 +783,7 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
           }
           ++seg;
         }
+        if (h_tile >= 0) asm volatile("cp.async.wait_all;" ::: "memory");
         if (stop) break;
       }
       if (tl && l128 == 0) tl[ph * kTimelineSlots] = globaltimer();

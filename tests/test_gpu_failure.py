@@ -44,8 +44,9 @@ def test_bounded_wait_gives_up_and_the_next_call_is_clean(torch):
     M, N, K = 256, 32, 512
     w = bf16_bits(rng.standard_normal((M, K)).astype(np.float32) * 0.05)
     x = bf16_bits(rng.standard_normal((N, K)).astype(np.float32))
+    w_d, x_d = to_dev(torch, w), to_dev(torch, x)
     y = torch.zeros((N, M), dtype=torch.float32, device="cuda")
-    binding.op_gemm(to_dev(torch, w).data_ptr(), to_dev(torch, x).data_ptr(), y.data_ptr(), M, N, K)
+    binding.op_gemm(w_d.data_ptr(), x_d.data_ptr(), y.data_ptr(), M, N, K)
     assert binding.op_check() == 0
     ref = bits_to_f64(x) @ bits_to_f64(w).T
     np.testing.assert_allclose(y.cpu().numpy(), ref, rtol=1e-4, atol=1e-4)
