@@ -43,7 +43,7 @@ UNIT = "tokens/s"
 STEP_SOURCES = ("attention.cuh", "gemm.cuh", "ptx.cuh", "small_kernels.cuh", "step_kernel.cuh",
                 "step_hd64.cu", "step_hd128.cu")
 MEASURED_TRAFFIC = {
-    ("persistent_step", "8b"): (15.89e9 + 116.77e6, "61c0d98499d593c8",
+    ("persistent_step", "8b"): (15892084736 + 114503424, "ee00270e1c7da66c",
                                 "ncu one-pass capture of dram__bytes_read.sum + dram__bytes_write.sum, one launch"),
 }
 
@@ -267,12 +267,15 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     state.set_precision(args.precision)
     state.set_persistent(args.persistent)
     state.set_mask(args.mask)
-    sel = binding.make_select(binding.SEL_THRESHOLD, wl.tau)
+    if args.rule == "fixed":
+        sel = binding.make_select(binding.SEL_FIXED_K, wl.tau, args.k)
+    else:
+        sel = binding.make_select(binding.SEL_THRESHOLD, wl.tau)
     mode = args.mode
 
     def one_generation():
         state.set_prompts_device(prompts_dev.data_ptr())
-        return state.run(sel, mode)
+        return state.run(sel, mode, refresh_interval=args.refresh_interval)
 
     for _ in range(args.warmup):
         one_generation()
@@ -336,7 +339,7 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     e2e_steps = 0
     for _ in range(args.steps if args.e2e else 0):
         e2e_state.reset(host_prompts)                   # H2D: canvas b*T int32
-        st = e2e_state.run(sel, mode)
+        st = e2e_state.run(sel, mode, refresh_interval=args.refresh_interval)
         toks[:] = e2e_state.tokens()                    # D2H: canvas b*T int32
         e2e_tokens += st["committed"]
         e2e_steps += st["steps"]
@@ -361,6 +364,8 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
                         f"block {B}, tau {wl.tau}, {mode} cache",
             "model": f"{cfg.n_layers}L d{cfg.d_model} H{cfg.n_heads} F{cfg.d_ffn} V{cfg.vocab} (random init)",
             "global_batch": sh.global_batch, "seq_len": wl.T, "block": B, "tau": wl.tau, "cache_mode": mode,
+            "rule": "threshold" if args.rule == "threshold" else f"fixed k={args.k}",
+            "refresh_interval": args.refresh_interval,
             "precision": f"{args.precision} activations, bf16 weights and K/V, f32 accumulate",
             "mask": "bidirectional" if args.mask == "full" else "block-causal (refresh = one block forward)",
             "step_launch": "persistent (one cooperative launch per denoise step)" if args.persistent
@@ -401,6 +406,8 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
         "tau_bar": sum(s["committed"] for s in stats) / max(sum(s["steps"] for s in stats) * b, 1),
         "denoise_steps_per_s": steps / (sum(s["step_ms"] for s in stats) / 1e3),
         "steps_per_generation": steps / args.steps, "refreshes_per_generation": refreshes / args.steps,
+        "steps_per_block": steps / args.steps / max(gen // B, 1),
+        "max_steps_per_block": max(s["max_steps_per_block"] for s in stats),
         "eq15": {"S": steps / args.steps, "C_active_ms": step_ms, "R_ms": refresh_ms * refreshes / args.steps},
         "clocks": clk, "gpu_launches": launches,
     }
@@ -474,6 +481,11 @@ def main():
     ap.add_argument("--tau", type=float, default=None)
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--precision", default="split", choices=("split", "bf16"))
+    ap.add_argument("--rule", default="threshold", choices=("threshold", "fixed"),
+                    help="selection rule: the threshold rule (Algorithm 2) or a fixed k tokens per step")
+    ap.add_argument("--k", type=int, default=1, help="tokens per step of the fixed rule")
+    ap.add_argument("--refresh-interval", type=int, default=0,
+                    help="also refresh the cache every this many steps inside a block (0: block boundaries only)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--ref-steps-per-gen", type=int, default=0)
     ap.add_argument("--ref-refreshes-per-gen", type=int, default=0)
