@@ -257,10 +257,33 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
   if (tid == 0)
     for (int t = 0; t < ST && t < ntiles; ++t) issue(t, (int)((tc0 + t) % ST));
 
-  // Q fragments of this warp's 16 query rows
+  // Q fragments of this warp's 16 query rows.  With 32 query rows (WQ == 2)
+  // the tile (hi and lo) is staged once in xo, 16-byte chunks XOR-swizzled by
+  // row so that ldmatrix reads are conflict-free, and the fragments are
+  // re-read per k-step: holding all of them in registers (64 per thread) made
+  // the persistent step kernel spill.  xo is free until the key loop ends.
   const int qrow0 = qt * QT + wq * 16;
-  uint32_t qa[KS][4], ql[KS][4];
-  {
+  uint32_t qa[WQ == 2 ? 1 : KS][4], ql[WQ == 2 ? 1 : KS][4];
+  uint16_t* const qs_hi = reinterpret_cast<uint16_t*>(xo);
+  uint16_t* const qs_lo = qs_hi + 32 * HD;
+  if constexpr (WQ == 2) {
+    constexpr int CH = HD / 8;                   // 16-byte chunks per row
+    for (int e = tid; e < 32 * CH; e += 128) {
+      const int rl = e / CH, c = e - rl * CH;
+      const int row = qt * QT + rl;
+      uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
+      if (row < p.R) {
+        // L2-coherent loads: q was written by other CTAs of the same launch (persistent step)
+        const long long base = (((long long)seq * p.R + row) * p.H + head) * HD + c * 8;
+        hv = __ldcg(reinterpret_cast<const uint4*>(p.q + base));
+        if (lo) lv = __ldcg(reinterpret_cast<const uint4*>(p.q_lo + base));
+      }
+      const int pc = c ^ (rl & 7);
+      *reinterpret_cast<uint4*>(qs_hi + rl * HD + pc * 8) = hv;
+      *reinterpret_cast<uint4*>(qs_lo + rl * HD + pc * 8) = lv;
+    }
+    named_bar_sync(2, 128);
+  } else {
     const long long base_lo = (((long long)seq * p.R + qrow0 + g) * p.H + head) * HD;
     const long long base_hi = base_lo + 8LL * p.H * HD;
     const bool lo_ok = qrow0 + g < p.R, hi_ok = qrow0 + g + 8 < p.R;
@@ -311,14 +334,35 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
           const int ch = 2 * kk + (lane >> 3);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + swz_off<KT>(r, ch), b0, b1, b2, b3);
-          mma16816(acc[0], qa[kk], b0, b1);
-          mma16816(acc[1], qa[kk + 1], b2, b3);
+          uint32_t fa0[4], fa1[4], fl0[4], fl1[4];
+          if constexpr (WQ == 2) {
+            // rows wq*16 + 0..15: lanes 8-15 and 24-31 address rows 8-15,
+            // lanes 16-31 the second 8 dims of the k-step
+            const int rr = wq * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int c0 = (2 * kk + (lane >> 4)) ^ (rr & 7), c1 = (2 * kk + 2 + (lane >> 4)) ^ (rr & 7);
+            ldsm_x4(smem_u32(qs_hi + rr * HD + c0 * 8), fa0[0], fa0[1], fa0[2], fa0[3]);
+            ldsm_x4(smem_u32(qs_hi + rr * HD + c1 * 8), fa1[0], fa1[1], fa1[2], fa1[3]);
+            if (lo) {
+              ldsm_x4(smem_u32(qs_lo + rr * HD + c0 * 8), fl0[0], fl0[1], fl0[2], fl0[3]);
+              ldsm_x4(smem_u32(qs_lo + rr * HD + c1 * 8), fl1[0], fl1[1], fl1[2], fl1[3]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              fa0[i] = qa[kk][i];
+              fa1[i] = qa[kk + 1][i];
+              fl0[i] = ql[kk][i];
+              fl1[i] = ql[kk + 1][i];
+            }
+          }
+          mma16816(acc[0], fa0, b0, b1);
+          mma16816(acc[1], fa1, b2, b3);
           if (lo) {
-            mma16816(acc[2], ql[kk], b0, b1);
-            mma16816(acc[3], ql[kk + 1], b2, b3);
+            mma16816(acc[2], fl0, b0, b1);
+            mma16816(acc[3], fl1, b2, b3);
             ldsm_x4(kb + TILE_BYTES + swz_off<KT>(r, ch), b0, b1, b2, b3);
-            mma16816(acc[4], qa[kk], b0, b1);
-            mma16816(acc[5], qa[kk + 1], b2, b3);
+            mma16816(acc[4], fa0, b0, b1);
+            mma16816(acc[5], fa1, b2, b3);
           }
         }
 #pragma unroll

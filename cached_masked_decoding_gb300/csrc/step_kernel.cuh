@@ -123,15 +123,15 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
   return v;
 }
 
-// Wait until *f >= need (acquire), then order later TMA reads after it.
-// Bounded by limit_ns; gives up early once this CTA raised *abort or any
-// CTA recorded an error; on giving up records `site` in err.
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
+// Wait until *f >= need (acquire), then order later TMA reads after it.
+// Bounded by limit_ns; gives up early once this CTA raised *abort or any
+// CTA recorded an error; on giving up records `site` in err.
 __device__ __forceinline__ bool flag_wait_for(const int* f, int need, volatile int* abort, int* err,
                                               unsigned long long limit_ns, int site) {
   if (ld_acquire_gpu(f) < need) {
