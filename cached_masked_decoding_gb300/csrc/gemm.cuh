@@ -237,15 +237,20 @@ __device__ __forceinline__ void warp_transpose_argmax(float (&v)[32], int (&id)[
 constexpr int kStageLd = 132;
 
 // Eight floats as bf16 pairs: hi = bf16(x), lo = bf16(x - hi).
+// A pair of floats as bf16 (x0 in the low half) and their bf16 residuals,
+// with one paired conversion each (two scalar conversions cost a measurable
+// part of an epilogue).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(x0, x1);
+  hi = *reinterpret_cast<const uint32_t*>(&b);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 __device__ __forceinline__ void split8v(const float (&f)[8], uint4& hi, uint4& lo) {
   uint32_t h[4], l[4];
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const uint16_t b0 = f32_to_bf16_bits(f[2 * t]), b1 = f32_to_bf16_bits(f[2 * t + 1]);
-    h[t] = (uint32_t)b0 | ((uint32_t)b1 << 16);
-    l[t] = (uint32_t)f32_to_bf16_bits(f[2 * t] - bf16_bits_to_f32(b0)) |
-           ((uint32_t)f32_to_bf16_bits(f[2 * t + 1] - bf16_bits_to_f32(b1)) << 16);
-  }
+  for (int t = 0; t < 4; ++t) split2(f[2 * t], f[2 * t + 1], h[t], l[t]);
   hi = make_uint4(h[0], h[1], h[2], h[3]);
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
@@ -255,16 +260,7 @@ __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
   const float4 a = *reinterpret_cast<const float4*>(x);
   const float4 b = *reinterpret_cast<const float4*>(x + 4);
   const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const uint16_t b0 = f32_to_bf16_bits(f[2 * t]), b1 = f32_to_bf16_bits(f[2 * t + 1]);
-    h[t] = (uint32_t)b0 | ((uint32_t)b1 << 16);
-    l[t] = (uint32_t)f32_to_bf16_bits(f[2 * t] - bf16_bits_to_f32(b0)) |
-           ((uint32_t)f32_to_bf16_bits(f[2 * t + 1] - bf16_bits_to_f32(b1)) << 16);
-  }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
+  split8v(f, hi, lo);
 }
 
 // Epilogue of 32 consecutive activation rows (columns of the accumulator) for
@@ -398,6 +394,10 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
     }
     const float g4[4] = {__uint_as_float(graw.x << 16), __uint_as_float(graw.x & 0xffff0000u),
                          __uint_as_float(graw.y << 16), __uint_as_float(graw.y & 0xffff0000u)};
+    // the eight rows' sums of squares are reduced across the warp together:
+    // one dependent shuffle chain instead of eight (same order per row)
+    float sqv[8];
+    int rov[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int row = q + 4 * k;
@@ -413,28 +413,35 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
         const int bi = pos - blk0;
         ro = (bi >= 0 && bi < blen) ? seq * blen + bi : -1;
       }
+      rov[k] = r < N ? ro : -1;
       float sq = 0.0f;
       if (r < N) {
         *reinterpret_cast<float4*>(&h[(long long)r * d + fb]) = make_float4(hv[k][0], hv[k][1], hv[k][2], hv[k][3]);
         if (ro >= 0) {
           uint32_t hb[2], lb[2];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const float x0 = hv[k][2 * t] * g4[2 * t], x1 = hv[k][2 * t + 1] * g4[2 * t + 1];
-            const uint16_t b0 = f32_to_bf16_bits(x0), b1 = f32_to_bf16_bits(x1);
-            hb[t] = (uint32_t)b0 | ((uint32_t)b1 << 16);
-            lb[t] = (uint32_t)f32_to_bf16_bits(x0 - bf16_bits_to_f32(b0)) |
-                    ((uint32_t)f32_to_bf16_bits(x1 - bf16_bits_to_f32(b1)) << 16);
-          }
+          for (int t = 0; t < 2; ++t) split2(hv[k][2 * t] * g4[2 * t], hv[k][2 * t + 1] * g4[2 * t + 1], hb[t], lb[t]);
           *reinterpret_cast<uint2*>(&xo[(long long)ro * d + fb]) = make_uint2(hb[0], hb[1]);
           if (xl) *reinterpret_cast<uint2*>(&xl[(long long)ro * d + fb]) = make_uint2(lb[0], lb[1]);
           sq = (hv[k][0] * hv[k][0] + hv[k][1] * hv[k][1]) + (hv[k][2] * hv[k][2] + hv[k][3] * hv[k][3]);
         }
       }
-#pragma unroll
-      for (int s = 16; s >= 1; s >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, s);
-      if (lane == 0 && r < N && ro >= 0) sso[(long long)ro * (d >> 7) + m_idx] = sq;
+      sqv[k] = sq;
     }
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sqv[k] += __shfl_xor_sync(0xffffffffu, sqv[k], s);
+    // lane k stores row q + 4k's sum
+    float sq_out = sqv[0];
+    int ro_out = rov[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+      if (lane == k) {
+        sq_out = sqv[k];
+        ro_out = rov[k];
+      }
+    if (lane < 8 && ro_out >= 0) sso[(long long)ro_out * (d >> 7) + m_idx] = sq_out;
   } else if constexpr (KIND == GEMM_SWIGLU) {
     // The tile's 128 weight rows are 64 gate rows then the 64 matching up
     // rows.  Staged as [feature][row]; then every thread forms 16 outputs of
