@@ -341,8 +341,9 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, float (&v)[32], i
         *reinterpret_cast<uint4*>(&q_out[(long long)r * d + fm]) = hi;
         if (q_lo) *reinterpret_cast<uint4*>(&q_lo[(long long)r * d + fm]) = lo;
       } else {
-        const int seq = r / R, i = r - seq * R;
-        const int head = fm / hd, jj = fm - head * hd;
+        // one sequence needs no division; head_dim is 64 or 128
+        const int seq = b == 1 ? 0 : r / R, i = r - seq * R;
+        const int head = hd == 128 ? fm >> 7 : fm >> 6, jj = fm - head * hd;
         const long long plane = ((((long long)layer * 2 + (sec - 1)) * 2) * b + seq) * H + head;
         *reinterpret_cast<uint4*>(&kv[(plane * T + row0 + i) * hd + jj]) = hi;
         if (q_lo) *reinterpret_cast<uint4*>(&kv[((plane + (long long)b * H) * T + row0 + i) * hd + jj]) = lo;
