@@ -46,11 +46,13 @@ struct AttnParams {
   int* err;
 };
 
-template <int HD, int KT>
+// LO: room for the low halves of K and V (split precision); without them a
+// 32-key CTA needs 50 KB instead of 83 KB and four fit on an SM instead of two.
+template <int HD, int KT, bool LO = true>
 struct AttnCfg {
   static constexpr int TILE_BYTES = KT * HD * 2;     // one of K, V, K lo, V lo
   static constexpr int STAGES = 2;
-  static constexpr int PARTS = KT == 32 ? 2 : 1;     // 32-key tiles leave room for the low halves
+  static constexpr int PARTS = (KT == 32 && LO) ? 2 : 1;   // 32-key tiles leave room for the low halves
   static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * PARTS * TILE_BYTES + 32 * HD * 4 + 32 * 2 * 4 + 64;
 };
 
@@ -560,10 +562,10 @@ __device__ __forceinline__ bool attn_item(const CUtensorMap* tmK, const CUtensor
 
 // Standalone launch: one work item per CTA.  KT = 32 also takes the low
 // halves (kv_lo); KT = 64 is bf16 only.
-template <int HD, int WQ, int KT>
+template <int HD, int WQ, int KT, bool LO = true>
 __global__ void __launch_bounds__(128) attn_kernel(const __grid_constant__ CUtensorMap tmK,
                                                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using C = AttnCfg<HD, KT>;
+  using C = AttnCfg<HD, KT, LO>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;

@@ -170,13 +170,17 @@ def test_persistent_whole_run_matches_oracle_8_blocks(gmodel, omodel):
     st.free()
 
 
-def test_bf16_activation_mode(gmodel, omodel):
+@pytest.mark.parametrize("persistent", [True, False])
+def test_bf16_activation_mode(gmodel, omodel, persistent):
     """DLLM_PREC_BF16 rounds every GEMM input to bf16: the tiny model's steep
     LM head (logit sigma 10) turns those roundings into max-prob errors of up
-    to ~1e-2, which is the tolerance this mode is held to."""
+    to ~1e-2, which is the tolerance this mode is held to.  Both the
+    persistent step and the per-kernel launches (whose block attention then
+    runs the bf16-only 32-key CTA) are checked."""
     P, gen, B = 32, 64, 16
     pr = synth.prompts(CFG, 0, 1, P)
     st = binding.State(gmodel, pr, 1, P, gen, B)
+    st.set_persistent(persistent)
     st.set_precision("bf16")
     dec = OS.Decoder(omodel, pr, gen, B, "dual")
     st.refresh()
