@@ -371,6 +371,12 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       }
     }
   }
+  // Lanes 1-31 of the producer and MMA warps skipped their roles and arrive
+  // here first: reconverge each warp before the CTA-wide barrier (an aligned
+  // barrier reached by part of a warp would let the warp count as arrived
+  // while lane 0 still works, and tensor memory could be freed under the
+  // epilogue warps' last reads).
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

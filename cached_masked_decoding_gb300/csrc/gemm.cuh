@@ -856,6 +856,12 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (p.trace && l128 == 0) p.trace[cta * 8 + 4] = globaltimer();
   }
+  // Lanes 1-31 of the producer and MMA warps skipped their roles and arrive
+  // here first: reconverge each warp before the CTA-wide barrier (an aligned
+  // barrier reached by part of a warp would let the warp count as arrived
+  // while lane 0 still works, and tensor memory could be freed under the
+  // epilogue warps' last reads).
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (p.trace && threadIdx.x == 0) p.trace[cta * 8 + 5] = globaltimer();

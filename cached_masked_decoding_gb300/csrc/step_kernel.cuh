@@ -789,6 +789,12 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
       if (tl && l128 == 0) tl[ph * kTimelineSlots] = globaltimer();
     }
   }
+  // Lanes 1-31 of the producer and MMA warps skipped their roles and arrive
+  // here first: reconverge each warp before the CTA-wide barrier (an aligned
+  // barrier reached by part of a warp would let the warp count as arrived
+  // while lane 0 still works, and tensor memory could be freed under the
+  // epilogue warps' last reads).
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
