@@ -16,15 +16,17 @@
 // yields W.hi and W.lo side by side in TMEM, summed in the epilogue.  The
 // weights are read once either way; while the GEMM is bound by HBM the extra
 // MMA width is free.
-// Work split: W = tiles / gridDim.x whole waves of tiles first - CTA c takes
-// tiles w*G + c, so CTAs side by side work on tiles side by side, which share
-// their weight rows (tiles are numbered m-major): a weight tile comes from HBM
-// once per wave and from L2 for the other n-tiles.  The remaining tiles'
-// chunks of 64 reduction elements are cut into gridDim.x equal contiguous
-// ranges ("stream-K"), so every SM streams the same number of bytes.  A tile
-// cut between CTAs is finished by the last contributor to arrive, which sums
-// every contributor's partial in contributor order: results do not depend on
-// arrival order.
+// Work split: W = tiles / gridDim.x whole waves of tiles - CTA c takes tiles
+// w*G + c, so CTAs side by side work on tiles side by side, which share their
+// weight rows (tiles are numbered m-major): a weight tile comes from HBM once
+// per wave and from L2 for the other n-tiles.  The remaining tiles' chunks of
+// 64 reduction elements are cut into gridDim.x equal contiguous ranges
+// ("stream-K"), so every SM streams the same number of bytes.  A tile cut
+// between CTAs is finished by the last contributor to arrive, which sums every
+// contributor's partial in contributor order: results do not depend on arrival
+// order.  Each CTA runs its stream-K range before its whole tiles, so that the
+// partials' exchange and the fix-up epilogues overlap the whole tiles' main
+// loops instead of trailing the launch.
 #pragma once
 
 #include "ptx.cuh"
@@ -99,8 +101,8 @@ struct GemmSeg {
   uint32_t rg0;
 };
 
-// The segments of one CTA: its whole tiles, then its stream-K range of the
-// remainder (see the work split above).
+// The segments of one CTA: its stream-K range of the remainder, then its
+// whole tiles (see the work split above).
 struct GemmWork {
   uint32_t G, cta, kc, n_tiles, W, full, total_r, rs, re;
   __device__ __forceinline__ void init(uint32_t G_, uint32_t cta_, uint32_t tiles, uint32_t kc_, uint32_t n_tiles_) {
@@ -125,14 +127,7 @@ struct GemmSegCursor {
   }
   __device__ __forceinline__ bool next(const GemmWork& wk, GemmSeg& o) {
     uint32_t tile;
-    if (w < wk.W) {
-      tile = w * wk.G + wk.cta;
-      ++w;
-      o.k0 = 0;
-      o.len = (int)wk.kc;
-      o.whole = true;
-      o.rg0 = 0;
-    } else if (g < wk.re) {
+    if (g < wk.re) {
       const uint32_t rt = g / wk.kc, k = g - rt * wk.kc;
       const uint32_t len = (wk.kc - k < wk.re - g) ? wk.kc - k : wk.re - g;
       tile = wk.full + rt;
@@ -141,6 +136,13 @@ struct GemmSegCursor {
       o.whole = (k == 0) && (len == wk.kc);
       o.rg0 = g;
       g += len;
+    } else if (w < wk.W) {
+      tile = w * wk.G + wk.cta;
+      ++w;
+      o.k0 = 0;
+      o.len = (int)wk.kc;
+      o.whole = true;
+      o.rg0 = 0;
     } else {
       return false;
     }
