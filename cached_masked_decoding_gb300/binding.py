@@ -102,6 +102,7 @@ SIGNATURES = {
     "dllm_staleness": (_I32, [_P, _I32, _P, _P, _P, _P]),
     "dllm_op_attention_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
     "dllm_op_attention_tc": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]),
+    "dllm_op_attention_tc_ex": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "dllm_op_check": (_I32, [ctypes.POINTER(_I32), _P]),
     "dllm_op_wait_probe": (_I32, [_P, _I32, _I32, _P]),
     "dllm_op_select_commit": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(Select), _P, _P]),
@@ -380,9 +381,14 @@ def op_attention(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, b: int, H: int,
 
 
 def op_attention_tc(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, b: int, H: int, hd: int, R: int, T: int,
-                    stream: int = 0):
-    check(lib().dllm_op_attention_tc(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
-                                     ctypes.c_void_p(o_ptr), b, H, hd, R, T, ctypes.c_void_p(stream)))
+                    stream: int = 0, splits: int | None = None):
+    if splits is None:
+        check(lib().dllm_op_attention_tc(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                                         ctypes.c_void_p(o_ptr), b, H, hd, R, T, ctypes.c_void_p(stream)))
+    else:
+        check(lib().dllm_op_attention_tc_ex(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                                            ctypes.c_void_p(o_ptr), b, H, hd, R, T, splits,
+                                            ctypes.c_void_p(stream)))
 
 
 def op_attention_noalloc(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, b: int, H: int, hd: int, R: int,

@@ -201,6 +201,35 @@ AttnPlan plan_attention_persistent(int b, int H, int R, int T, int ctas) {
   return a;
 }
 
+// Query rows per sequence from which attention runs on the tensor cores
+// (128-query tiles); fewer rows use the key-split kernel.
+constexpr int kAttnTcMinRows = 65;
+
+// Plan of the tensor-core attention (128-query tiles, 64-key tiles): key
+// splits when the query tiles alone leave most SMs idle.  One CTA per SM; the
+// cost of s splits is taken as rounds x (key tiles per split + fixed work):
+// one tile's worth without splits, four with them (the partial's stores and
+// the last split's merge; measured on GB300: the 8B refresh's 192 query tiles
+// took 65.7 us unsplit and 73.9 us in two splits, a PrefixCache step's 64
+// tiles 33.8 and 29.0 us).  Splits are taken only when they promise at least
+// a fifth less time; at most 8 (the merge keeps 128 x splits weights in the
+// probabilities' tile).
+AttnPlan plan_attention_tc(int b, int H, int R, int T, int sms) {
+  AttnPlan a;
+  a.wq = 8;
+  a.q_tiles = ceil_div(R, 128);
+  const long long items = (long long)b * H * a.q_tiles;
+  const int kt = std::max(1, ceil_div(T, 64));
+  auto cost = [&](int sp) { return ((items * sp + sms - 1) / sms) * (ceil_div(kt, sp) + (sp > 1 ? 4 : 1)); };
+  int best = 1;
+  for (int sp = 2; sp <= 8 && sp <= kt; ++sp)
+    if (cost(sp) < cost(best)) best = sp;
+  if (best > 1 && 5 * cost(best) > 4 * cost(1)) best = 1;
+  a.kps = ceil_div(kt, best) * 64;
+  a.splits = ceil_div(T, a.kps);
+  return a;
+}
+
 }  // namespace
 
 // ====================================================================== model
@@ -498,6 +527,8 @@ struct dllm_state {
   float* gemm_ws = nullptr;
   int* gemm_cnt = nullptr;
   float* attn_o = nullptr;
+  size_t attn_o_floats = 0;   // attention merge workspace (partials and (m, l)), floats
+  size_t attn_cnt_n = 0;      // merge counters
   float* attn_ml = nullptr;
   int* attn_cnt = nullptr;
   float2* rope = nullptr;
@@ -647,6 +678,15 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
     const size_t pworks = (size_t)b * H * ap.q_tiles;
     attn_floats = std::max(attn_floats, pworks * ap.splits * 16 * ap.wq * (hd + 2));
     attn_cnt = std::max(attn_cnt, pworks);
+    // row counts that take the tensor-core kernel
+    for (int R : Rs) {
+      if (R < kAttnTcMinRows) continue;
+      AttnPlan at = plan_attention_tc(b, (int)H, R, (int)T, m->sms);
+      if (at.splits < 2) continue;
+      const size_t works = (size_t)b * H * at.q_tiles;
+      attn_floats = std::max(attn_floats, works * at.splits * 128 * (hd + 2));
+      attn_cnt = std::max(attn_cnt, works);
+    }
   }
   auto al = [](size_t bytes) { return (bytes + 1023) / 1024 * 1024; };
   size_t total = 0;
@@ -708,6 +748,8 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
   s->seq_done = reinterpret_cast<int*>(a + o_sd);
   s->gemm_cnt = reinterpret_cast<int*>(a + o_gc);
   s->attn_o = reinterpret_cast<float*>(a + o_ao2);
+  s->attn_o_floats = attn_floats;
+  s->attn_cnt_n = attn_cnt;
   s->attn_ml = s->attn_o;   // carved per launch from the same block (see run_attention)
   s->attn_cnt = reinterpret_cast<int*>(a + o_ac);
   s->rope = reinterpret_cast<float2*>(a + o_rope);
@@ -917,9 +959,6 @@ dllm_status run_gemm(dllm_state* s, int kind, const CUtensorMap& tmA, int M, int
   return DLLM_OK;
 }
 
-// Query rows per sequence from which attention runs on the tensor cores
-// (128-query tiles); fewer rows use the key-split kernel.
-constexpr int kAttnTcMinRows = 65;
 
 dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes) {
   const dllm_config& c = s->m->cfg;
@@ -939,6 +978,13 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
       CKS(map_kv(&m, s->kv, c.head_dim, s->T, (uint64_t)c.n_layers * 4 * bh, 64));
       it = s->kv64_maps.emplace(s->kv, m).first;
     }
+    AttnPlan at = plan_attention_tc(s->b, c.n_heads, R, s->T, s->m->sms);
+    const size_t tc_works = (size_t)s->b * c.n_heads * at.q_tiles;
+    if (at.splits > 1 &&
+        (tc_works * at.splits * 128 * (c.head_dim + 2) > s->attn_o_floats || tc_works > s->attn_cnt_n)) {
+      set_error("attention merge workspace too small for %d rows", R);
+      return DLLM_EINVAL;
+    }
     AttnParams p = {};
     p.q = s->q;
     p.q_lo = s->split ? s->q_lo : nullptr;
@@ -949,6 +995,12 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
     p.b = s->b;
     p.H = c.n_heads;
     p.T = s->T;
+    p.q_tiles = at.q_tiles;
+    p.splits = at.splits;
+    p.kps = at.kps;
+    p.ws_o = s->attn_o;
+    p.ws_ml = s->attn_o + (long long)s->b * c.n_heads * at.q_tiles * at.splits * 128 * c.head_dim;
+    p.counters = s->attn_cnt;
     p.z_k0 = ((layer * 2 + 0) * 2 + 0) * bh;
     p.z_kl0 = ((layer * 2 + 0) * 2 + 1) * bh;
     p.z_v0 = ((layer * 2 + 1) * 2 + 0) * bh;
@@ -961,7 +1013,7 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
     if (s->timing) s->kt_bytes[cls] += bytes;
     Timed t(s, cls, bytes);
     CK(launch_attention_tc(c.head_dim, *tq, *tqlo, it->second, it->second, p,
-                           dim3(ceil_div(R, 128), c.n_heads, s->b), s->st, true));
+                           dim3(at.q_tiles * at.splits, c.n_heads, s->b), s->st, true));
     ++s->launches;
     return DLLM_OK;
   }
@@ -2072,9 +2124,15 @@ extern "C" dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_ca
 extern "C" dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                                             uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R, int32_t T,
                                             void* stream) {
+  return dllm_op_attention_tc_ex(q, k_cache, v_cache, out, b, H, hd, R, T, 0, stream);
+}
+
+extern "C" dllm_status dllm_op_attention_tc_ex(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                               uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R, int32_t T,
+                                               int32_t splits, void* stream) {
   if (!q || !k_cache || !v_cache || !out || b < 1 || H < 1 || (hd != 64 && hd != 128) || R < 1 || T < 1 ||
-      !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) {
-    set_error("bad attention arguments: b=%d H=%d hd=%d R=%d T=%d", b, H, hd, R, T);
+      splits < 0 || splits > 8 || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) {
+    set_error("bad attention arguments: b=%d H=%d hd=%d R=%d T=%d splits=%d", b, H, hd, R, T, splits);
     return DLLM_EINVAL;
   }
   std::lock_guard<std::mutex> lk(g_op_mu);
@@ -2082,8 +2140,15 @@ extern "C" dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k
   CKS(map_2d(&tq, q, (uint64_t)H * hd, (uint64_t)b * R, 128));
   CKS(map_kv(&tk, k_cache, hd, T, (uint64_t)b * H, 64));
   CKS(map_kv(&tv, v_cache, hd, T, (uint64_t)b * H, 64));
+  AttnPlan at = plan_attention_tc(b, H, R, T, device_sms());
+  if (splits > 0) {
+    at.kps = ceil_div(ceil_div(T, 64), splits) * 64;
+    at.splits = ceil_div(T, at.kps);
+  }
+  const long long works = (long long)b * H * at.q_tiles;
   OpWorkspace* w = nullptr;
-  CKS(op_workspace(&w, 1, 0, 0));
+  CKS(op_workspace(&w, 1, at.splits > 1 ? (size_t)works * at.splits * 128 * (hd + 2) : 0,
+                   at.splits > 1 ? (size_t)works : 0));
   AttnParams p = {};
   p.q = q;
   p.o = out;
@@ -2091,10 +2156,16 @@ extern "C" dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k
   p.b = b;
   p.H = H;
   p.T = T;
+  p.q_tiles = at.q_tiles;
+  p.splits = at.splits;
+  p.kps = at.kps;
+  p.ws_o = w->attn;
+  p.ws_ml = w->attn + works * at.splits * 128 * hd;
+  p.counters = w->attn_cnt;
   p.scale_log2 = kLog2e / std::sqrt((float)hd);
   p.err = w->err;
-  CK(launch_attention_tc(hd, tq, tq, tk, tv, p, dim3(ceil_div(R, 128), H, b), static_cast<cudaStream_t>(stream),
-                         false));
+  CK(launch_attention_tc(hd, tq, tq, tk, tv, p, dim3(at.q_tiles * at.splits, H, b),
+                         static_cast<cudaStream_t>(stream), false));
   return DLLM_OK;
 }
 

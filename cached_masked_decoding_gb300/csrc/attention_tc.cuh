@@ -4,9 +4,12 @@
 // its sequence (or, under the block-causal mask, the keys below its block's
 // end).
 //
-// One CTA per (128-query tile, head, sequence) walks all keys in 64-key tiles:
+// One CTA per (128-query tile, key split, head, sequence) walks its keys in
+// 64-key tiles (with one split, all keys of the sequence):
 //   warp 0     TMA: the query tile once, then K and V tiles (with their low
-//              halves in split precision) through a two-stage ring;
+//              halves in split precision) through a two-stage ring whose K
+//              and V halves are refilled separately: a stage's keys as soon
+//              as its S product is done, its values once P V is done;
 //   warp 1     one thread issues tcgen05.mma: S = Q K^T into one of two
 //              64-column TMEM buffers, and O += P V into a HD-column TMEM
 //              accumulator; V is read as an MN-major operand straight from the
@@ -17,6 +20,10 @@
 //              rarely, in TMEM), write P as bf16 (hi and lo) into the
 //              K-major operand tile, and at the end O / l to global memory.
 // S of tile t+1 runs on the tensor cores while the softmax of tile t runs.
+// With several key splits each CTA stores its partial (O, m, l) and the last
+// split of a query tile to finish merges them (the key-split kernel's merge,
+// 128 rows); splits are planned when there are too few query tiles to fill
+// the GPU evenly.
 //
 // Split precision (kv_lo = 1): q, K, V and P are bf16 pairs x = hi + lo;
 // S = Qh Kh + Ql Kh + Qh Kl and O += Ph Vh + Pl Vh + Ph Vl (lo*lo dropped).
@@ -85,7 +92,9 @@ __device__ __forceinline__ int tc_key_limit(const AttnParams& p, int pos) {
   return lim < p.T ? lim : p.T;
 }
 
-// grid (query tiles of 128, H, b), 192 threads.  tmQ/tmQlo: 2-D maps over
+// grid (query tiles of 128 x p.splits, H, b), 192 threads; p.splits > 1
+// needs p.kps (a multiple of 64), p.q_tiles and the merge workspace
+// (p.ws_o, p.ws_ml, p.counters).  tmQ/tmQlo: 2-D maps over
 // q / q_lo [b*R][H*HD] with 128-row boxes; tmK/tmV: 3-D maps over the K and V
 // planes with 64-key boxes (the same map may serve both).
 template <int HD>
@@ -102,30 +111,40 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   uint8_t* sP = sKV + 2 * C::STAGE_BYTES;               // P hi, P lo
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * C::P_BYTES);
   uint64_t* qfull = bars;
-  uint64_t* kvfull = bars + 1;    // [2]
-  uint64_t* kvempty = bars + 3;   // [2]
+  uint64_t* kfull = bars + 1;     // [2] a stage's K (and K lo) landed
+  uint64_t* kempty = bars + 3;    // [2] its S product is done with it
   uint64_t* sfull = bars + 5;     // [2]
   uint64_t* sfree = bars + 7;     // [2]
   uint64_t* pready = bars + 9;
   uint64_t* pvdone = bars + 10;
   uint64_t* mdone = bars + 11;    // every MMA of the CTA finished (before TMEM is freed)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* vfull = bars + 12;    // [2] a stage's V (and V lo) landed
+  uint64_t* vempty = bars + 14;   // [2] its P V product is done with it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* bcast = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, head = blockIdx.y, seq = blockIdx.z;
+  const int splits = p.splits > 1 ? p.splits : 1;
+  const int qt = blockIdx.x / splits, split = blockIdx.x - qt * splits, head = blockIdx.y, seq = blockIdx.z;
   const bool lo = p.kv_lo != 0;
   const int parts = lo ? 2 : 1;
   // keys this tile's rows see at most: limits grow with the position
   const int last_row = min(p.R, qt * 128 + 128) - 1;
-  const int k_end = tc_key_limit(p, p.row0 + last_row);
-  const int nt = (k_end + KT - 1) / KT;
+  const int k_lim = tc_key_limit(p, p.row0 + last_row);
+  // this split's keys [k_beg, k_stop), tiles t0 .. t0 + nt - 1
+  const int k_beg = splits > 1 ? split * p.kps : 0;
+  const int k_stop = splits > 1 ? min(k_lim, k_beg + p.kps) : k_lim;
+  const int nt = k_stop > k_beg ? (k_stop - k_beg + KT - 1) / KT : 0;
+  const int t0 = k_beg / KT;
 
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&kvfull[s], 1);
-      mbar_init(&kvempty[s], 1);
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
       mbar_init(&sfull[s], 1);
       mbar_init(&sfree[s], 4);
     }
@@ -161,26 +180,36 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
                       row, pol_q);
       const int zk = p.z_k0 + seq * p.H + head, zv = p.z_v0 + seq * p.H + head;
       const int zkl = p.z_kl0 + seq * p.H + head, zvl = p.z_vl0 + seq * p.H + head;
-      int issued = 0;
+      // K of tile t waits for S of tile t-2, V of tile t for P V of tile
+      // t-2; since S runs about a tile ahead of P V, keys are requested a
+      // tile earlier than a whole-stage refill would allow
+      int k_issued = 0, v_issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int s = t & 1;
-        if (t >= 2 && !mbar_wait(&kvempty[s], (uint32_t)((t >> 1) - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL)) break;
         uint8_t* st = sKV + s * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&kvfull[s], (uint32_t)(2 * parts * C::KV_BYTES));
+        if (t >= 2 && !mbar_wait(&kempty[s], (uint32_t)((t >> 1) - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL)) break;
+        mbar_arrive_expect_tx(&kfull[s], (uint32_t)(parts * C::KV_BYTES));
         for (int bx = 0; bx < HD / 64; ++bx) {
-          tma_load_3d(st + 0 * C::KV_BYTES + bx * (KT * 128), &tmK, &kvfull[s], bx * 64, t * KT, zk, pol_kv);
-          tma_load_3d(st + 2 * C::KV_BYTES + bx * (KT * 128), &tmV, &kvfull[s], bx * 64, t * KT, zv, pol_kv);
-          if (lo) {
-            tma_load_3d(st + 1 * C::KV_BYTES + bx * (KT * 128), &tmK, &kvfull[s], bx * 64, t * KT, zkl, pol_kv);
-            tma_load_3d(st + 3 * C::KV_BYTES + bx * (KT * 128), &tmV, &kvfull[s], bx * 64, t * KT, zvl, pol_kv);
-          }
+          tma_load_3d(st + 0 * C::KV_BYTES + bx * (KT * 128), &tmK, &kfull[s], bx * 64, (t0 + t) * KT, zk, pol_kv);
+          if (lo)
+            tma_load_3d(st + 1 * C::KV_BYTES + bx * (KT * 128), &tmK, &kfull[s], bx * 64, (t0 + t) * KT, zkl, pol_kv);
         }
-        issued = t + 1;
+        k_issued = t + 1;
+        if (t >= 2 && !mbar_wait(&vempty[s], (uint32_t)((t >> 1) - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL)) break;
+        mbar_arrive_expect_tx(&vfull[s], (uint32_t)(parts * C::KV_BYTES));
+        for (int bx = 0; bx < HD / 64; ++bx) {
+          tma_load_3d(st + 2 * C::KV_BYTES + bx * (KT * 128), &tmV, &vfull[s], bx * 64, (t0 + t) * KT, zv, pol_kv);
+          if (lo)
+            tma_load_3d(st + 3 * C::KV_BYTES + bx * (KT * 128), &tmV, &vfull[s], bx * 64, (t0 + t) * KT, zvl, pol_kv);
+        }
+        v_issued = t + 1;
       }
       // nothing may land in shared memory after the CTA is gone
       mbar_wait(qfull, 0u, nullptr, p.err, ERR_ATTN_FULL);
-      for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
-        mbar_wait(&kvfull[t & 1], (uint32_t)(t >> 1) & 1u, nullptr, p.err, ERR_ATTN_FULL);
+      for (int t = k_issued - 2 < 0 ? 0 : k_issued - 2; t < k_issued; ++t)
+        mbar_wait(&kfull[t & 1], (uint32_t)(t >> 1) & 1u, nullptr, p.err, ERR_ATTN_FULL);
+      for (int t = v_issued - 2 < 0 ? 0 : v_issued - 2; t < v_issued; ++t)
+        mbar_wait(&vfull[t & 1], (uint32_t)(t >> 1) & 1u, nullptr, p.err, ERR_ATTN_FULL);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -205,6 +234,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
           }
         }
         mma_commit(&sfull[s]);
+        mma_commit(&kempty[s]);    // the stage's keys may be refilled
       };
       auto issue_pv = [&](int t) {
         const int s = t & 1;
@@ -219,7 +249,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
             mma_bf16_ss(d, sdesc_sw128(pa + kk * 32), sdesc_sw128_mn(vb + kk * 2048, KT * 128), idesc_o,
                         (t > 0 || pr > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kvempty[s]);   // the stage may be refilled
+        mma_commit(&vempty[s]);    // the stage's values may be refilled
         mma_commit(pvdone);
       };
       // Issue whichever is ready: P V of the oldest tile whose P is written
@@ -231,12 +261,13 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       uint32_t spins = 0;
       while (ok && np < nt) {
         bool did = false;
-        if (np < ns && mbar_test_wait(smem_u32(pready), (uint32_t)np & 1u)) {
+        if (np < ns && mbar_test_wait(smem_u32(pready), (uint32_t)np & 1u) &&
+            mbar_test_wait(smem_u32(&vfull[np & 1]), (uint32_t)(np >> 1) & 1u)) {
           tc_fence_after();
           issue_pv(np++);
           did = true;
         }
-        if (ns < nt && mbar_test_wait(smem_u32(&kvfull[ns & 1]), (uint32_t)(ns >> 1) & 1u) &&
+        if (ns < nt && mbar_test_wait(smem_u32(&kfull[ns & 1]), (uint32_t)(ns >> 1) & 1u) &&
             (ns < 2 || mbar_test_wait(smem_u32(&sfree[ns & 1]), (uint32_t)((ns >> 1) - 1) & 1u))) {
           tc_fence_after();
           issue_s(ns++);
@@ -283,7 +314,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[s]);
-      const int key0 = t * KT;
+      const int key0 = k_beg + t * KT;
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < KT; ++c) {
@@ -343,30 +374,64 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
     if (ok && nt > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(pvdone, (uint32_t)(nt - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL));
     tc_fence_after();
-    // O / l as bf16 (and its low half)
-    const float il = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
-    const long long obase = ((long long)seq * p.R + qi) * p.H * HD + head * HD;
+    if (splits > 1) {
+      // this split's partial: O relative to its reference max m, and (m, l)
+      const long long work = ((long long)seq * p.H + head) * p.q_tiles + qt;
+      const long long wrow = (work * splits + split) * 128 + row;
+      float* wo = p.ws_o + wrow * HD;
 #pragma unroll 1
-    for (int c0 = 0; c0 < HD; c0 += 32) {
-      float o[32];
-      if (nt > 0) {
-        tmem_ld32(trow + (uint32_t)(C::O_COL + c0), o);
-      } else {
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        float o[32];
+        if (nt > 0) {
+          tmem_ld32(trow + (uint32_t)(C::O_COL + c0), o);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+          for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          __stcg(reinterpret_cast<float4*>(wo + c0 + 4 * j), make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]));
       }
-      if (valid) {
+      __stcg(reinterpret_cast<float2*>(p.ws_ml + wrow * 2), ok ? make_float2(m, l) : make_float2(-INFINITY, 0.0f));
+      // the barrier orders every row's stores before the release; the
+      // acquire plus the next barrier order the merge's reads after
+      named_bar_sync(2, 128);
+      if (row == 0) {
+        const int old = atomic_add_acq_rel_gpu(&p.counters[work], 1);
+        const int last = (old == splits - 1);
+        if (last) p.counters[work] = 0;
+        *bcast = last;
+      }
+      named_bar_sync(2, 128);
+      // the probabilities' tile is free: every MMA that read it is done
+      if (*bcast) attn_merge<HD, 128>(p, work, qt, head, seq, reinterpret_cast<float*>(sP), row);
+    } else {
+      // O / l as bf16 (and its low half)
+      const float il = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
+      const long long obase = ((long long)seq * p.R + qi) * p.H * HD + head * HD;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        float o[32];
+        if (nt > 0) {
+          tmem_ld32(trow + (uint32_t)(C::O_COL + c0), o);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t h[4], lw[4];
+          for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+        }
+        if (valid) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = o[8 * j + 2 * e] * il, b = o[8 * j + 2 * e + 1] * il;
-            h[e] = pack_bf16(a, b);
-            lw[e] = pack_lo(a, b, h[e]);
+          for (int j = 0; j < 4; ++j) {
+            uint32_t h[4], lw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a = o[8 * j + 2 * e] * il, b = o[8 * j + 2 * e + 1] * il;
+              h[e] = pack_bf16(a, b);
+              lw[e] = pack_lo(a, b, h[e]);
+            }
+            *reinterpret_cast<uint4*>(&p.o[obase + c0 + 8 * j]) = make_uint4(h[0], h[1], h[2], h[3]);
+            if (p.o_lo)
+              *reinterpret_cast<uint4*>(&p.o_lo[obase + c0 + 8 * j]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
-          *reinterpret_cast<uint4*>(&p.o[obase + c0 + 8 * j]) = make_uint4(h[0], h[1], h[2], h[3]);
-          if (p.o_lo) *reinterpret_cast<uint4*>(&p.o_lo[obase + c0 + 8 * j]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
     }

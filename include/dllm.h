@@ -336,17 +336,28 @@ dllm_status dllm_op_attention(const uint16_t* q, const uint16_t* k_cache, const 
 
 /* The same attention (eq. 3 of the Fast-dLLM reading notes, section 2; same
  * arguments, layouts and output as dllm_op_attention) on the tensor cores:
- * one CTA per (128-query tile, head, sequence) runs S = q K^T and O = P V as
- * tcgen05.mma with S and O in tensor memory, over all T keys without a key
- * split, so it needs no workspace beyond the library's error word.  This is
- * the kernel the library uses for 65 or more query rows per sequence (the
- * refresh's full forward, PrefixCache and no-cache steps); block queries use
- * the key-split kernel.  q, k_cache, v_cache and out must be 16-byte aligned.
- * Results agree with dllm_op_attention to bf16 rounding of the probabilities
- * and the output, not bit for bit. */
+ * one CTA per (128-query tile, key split, head, sequence) runs S = q K^T and
+ * O = P V as tcgen05.mma with S and O in tensor memory.  The keys are split
+ * (at most 8 ways, 64-key granularity) when the query tiles alone would fill
+ * the GPU's SMs unevenly; the last split of a query tile to finish merges the
+ * partial softmax states in split order (deterministic), in a library-owned
+ * workspace grown on first use.  This is the kernel the library uses for 65
+ * or more query rows per sequence (the refresh's full forward, PrefixCache
+ * and no-cache steps); block queries use the key-split kernel.  q, k_cache,
+ * v_cache and out must be 16-byte aligned.  Results agree with
+ * dllm_op_attention to bf16 rounding of the probabilities and the output,
+ * not bit for bit. */
 dllm_status dllm_op_attention_tc(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                                  uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R,
                                  int32_t T, void* cuda_stream);
+
+/* dllm_op_attention_tc with the number of key splits chosen by the caller:
+ * splits = 0 takes the library's plan (as dllm_op_attention_tc), 1..8 cuts
+ * the keys into that many ranges of equal 64-key multiples (fewer when T is
+ * short: ranges past T are dropped).  Other values: DLLM_EINVAL. */
+dllm_status dllm_op_attention_tc_ex(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                    uint16_t* out, int32_t b, int32_t H, int32_t hd, int32_t R,
+                                    int32_t T, int32_t splits, void* cuda_stream);
 
 /* dllm_op_attention with no allocation of any kind.  The pages have no
  * counterpart to this entry point: it computes the same attention as

@@ -65,6 +65,8 @@ def test_host_side_errors_without_gpu_work():
         assert fn(16, 16, 16, 16, 1, 1, 96, 1, 1, None) == binding.EINVAL      # hd not 64 or 128
         assert fn(16, 16, 16, 16, 1, 1, 128, 0, 1, None) == binding.EINVAL     # no query rows
     assert L.dllm_op_attention_tc(18, 16, 16, 16, 1, 1, 128, 1, 1, None) == binding.EINVAL   # q not 16-byte aligned
+    assert L.dllm_op_attention_tc_ex(16, 16, 16, 16, 1, 1, 128, 1, 1, 9, None) == binding.EINVAL   # over 8 splits
+    assert L.dllm_op_attention_tc_ex(16, 16, 16, 16, 1, 1, 128, 1, 1, -1, None) == binding.EINVAL
     assert b"bad attention arguments" in L.dllm_last_error()
 
 

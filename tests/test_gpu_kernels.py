@@ -134,15 +134,18 @@ TC_ATTN_SHAPES = [
 ]
 
 
+# None: the library's own split plan; 1: every query tile walks all keys in
+# one CTA; 3: three key ranges merged by the last to finish (fewer when T is short)
+@pytest.mark.parametrize("splits", [None, 1, 3])
 @pytest.mark.parametrize("b,H,hd,R,T", TC_ATTN_SHAPES)
-def test_tensor_core_attention_matches_oracle(torch, b, H, hd, R, T):
+def test_tensor_core_attention_matches_oracle(torch, b, H, hd, R, T, splits):
     rng = np.random.default_rng(7 * b + H + hd + R + T)
     qb = bf16_bits(rng.standard_normal((b, R, H, hd)).astype(np.float32))
     kb = bf16_bits(rng.standard_normal((b, H, T, hd)).astype(np.float32))
     vb = bf16_bits(rng.standard_normal((b, H, T, hd)).astype(np.float32))
     q, k, v = to_dev(torch, qb), to_dev(torch, kb), to_dev(torch, vb)
     o = torch.zeros((b * R, H * hd), dtype=torch.int16, device="cuda")
-    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), b, H, hd, R, T)
+    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), b, H, hd, R, T, splits=splits)
     torch.cuda.synchronize()
     got = bits_to_f64(dev_bits(torch, o)).reshape(b, R, H, hd)
     for s in range(b):
@@ -153,14 +156,17 @@ def test_tensor_core_attention_matches_oracle(torch, b, H, hd, R, T):
         # P rounded to bf16 (2^-8 of sum p|v|) plus the bf16 output (2^-9 |o|)
         assert (err <= 6e-3 * vmax + 4e-3 * np.abs(ref)).all(), f"seq {s}: max err {err.max():.3e}"
     o2 = torch.zeros_like(o)
-    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), b, H, hd, R, T)
+    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), b, H, hd, R, T, splits=splits)
     torch.cuda.synchronize()
     assert torch.equal(o, o2)
+    assert binding.op_check() == 0
 
 
-def test_tensor_core_attention_peaked_rows(torch):
+@pytest.mark.parametrize("splits", [1, 2, 8])
+def test_tensor_core_attention_peaked_rows(torch, splits):
     # rows whose max moves by far more than 8 (base 2) between key tiles:
-    # the running output is rescaled in tensor memory
+    # the running output is rescaled in tensor memory (one or two key
+    # ranges), or the ranges' maxima differ widely in the merge (eight)
     b, H, hd, R, T = 1, 2, 128, 128, 512
     rng = np.random.default_rng(11)
     qf = rng.standard_normal((b, R, H, hd)).astype(np.float32)
@@ -170,7 +176,7 @@ def test_tensor_core_attention_peaked_rows(torch):
     vb = bf16_bits(rng.standard_normal((b, H, T, hd)).astype(np.float32))
     q, k, v = to_dev(torch, qb), to_dev(torch, kb), to_dev(torch, vb)
     o = torch.zeros((b * R, H * hd), dtype=torch.int16, device="cuda")
-    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), b, H, hd, R, T)
+    binding.op_attention_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), b, H, hd, R, T, splits=splits)
     torch.cuda.synchronize()
     got = bits_to_f64(dev_bits(torch, o)).reshape(R, H, hd)
     ref = OM.attention(bits_to_f64(qb[0]), bits_to_f64(kb[0]).transpose(1, 0, 2), bits_to_f64(vb[0]).transpose(1, 0, 2))
