@@ -12,14 +12,17 @@
 //              as its S product is done, its values once P V is done;
 //   warp 1     one thread issues tcgen05.mma: S = Q K^T into one of two
 //              64-column TMEM buffers, and O += P V into a HD-column TMEM
-//              accumulator; V is read as an MN-major operand straight from the
-//              TMA tile (keys along K, head dims along N);
+//              accumulator with P read from tensor memory; V is read as an
+//              MN-major operand straight from the TMA tile (keys along K,
+//              head dims along N);
 //   warps 2-5  one query row per thread: read S from TMEM, online softmax in
 //              base 2 (the row's reference max moves only when a tile's max
 //              exceeds it by more than 8, so P <= 256 and O is rescaled
-//              rarely, in TMEM), write P as bf16 (hi and lo) into the
-//              K-major operand tile, and at the end O / l to global memory.
-// S of tile t+1 runs on the tensor cores while the softmax of tile t runs.
+//              rarely, in TMEM), write P as bf16 (hi and lo) into one of two
+//              TMEM buffers (the row's lane, keys packed two per column), and
+//              at the end O / l to global memory.
+// S of tile t+1 runs on the tensor cores while the softmax of tile t runs,
+// and the softmax of tile t+1 writes its P while P V of tile t runs.
 // With several key splits each CTA stores its partial (O, m, l) and the last
 // split of a query tile to finish merges them (the key-split kernel's merge,
 // 128 rows); splits are planned when there are too few query tiles to fill
@@ -41,12 +44,14 @@ struct AttnTcCfg {
   static constexpr int KT = 64;                      // keys per tile
   static constexpr int Q_BYTES = 128 * HD * 2;       // one part (hi or lo) of the query tile
   static constexpr int KV_BYTES = KT * HD * 2;       // one part of a K or V tile
-  static constexpr int P_BYTES = 128 * KT * 2;       // one part of the probabilities
   static constexpr int STAGE_BYTES = 4 * KV_BYTES;   // K hi, K lo, V hi, V lo
-  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + 2 * STAGE_BYTES + 2 * P_BYTES + 256;
+  static constexpr int MERGE_BYTES = 128 * 8 * 4;    // split merge weights: 128 rows x up to 8 splits
+  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + 2 * STAGE_BYTES + MERGE_BYTES + 256;
   static constexpr int S_COL = 0;                    // two S buffers of KT columns
   static constexpr int O_COL = 2 * KT;               // O accumulator, HD columns
-  static constexpr int TMEM_COLS = 2 * KT + HD <= 256 ? 256 : 512;
+  static constexpr int P_COL = 2 * KT + HD;          // two P buffers of KT columns: KT/2 hi, KT/2 lo
+  static constexpr int TMEM_COLS = 512;
+  static_assert(P_COL + 2 * KT <= TMEM_COLS, "tensor memory");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -108,19 +113,19 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                   // Q hi, Q lo
   uint8_t* sKV = sQ + 2 * C::Q_BYTES;                   // per stage: K hi, K lo, V hi, V lo
-  uint8_t* sP = sKV + 2 * C::STAGE_BYTES;               // P hi, P lo
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * C::P_BYTES);
+  float* s_merge = reinterpret_cast<float*>(sKV + 2 * C::STAGE_BYTES);   // split merge weights
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + 2 * C::STAGE_BYTES + C::MERGE_BYTES);
   uint64_t* qfull = bars;
   uint64_t* kfull = bars + 1;     // [2] a stage's K (and K lo) landed
   uint64_t* kempty = bars + 3;    // [2] its S product is done with it
   uint64_t* sfull = bars + 5;     // [2]
   uint64_t* sfree = bars + 7;     // [2]
-  uint64_t* pready = bars + 9;
-  uint64_t* pvdone = bars + 10;
-  uint64_t* mdone = bars + 11;    // every MMA of the CTA finished (before TMEM is freed)
-  uint64_t* vfull = bars + 12;    // [2] a stage's V (and V lo) landed
-  uint64_t* vempty = bars + 14;   // [2] its P V product is done with it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* pready = bars + 9;    // [2] a P buffer written by the four softmax warps
+  uint64_t* pvdone = bars + 11;   // [2] P V of the tile in a P buffer done
+  uint64_t* vfull = bars + 13;    // [2] a stage's V (and V lo) landed
+  uint64_t* vempty = bars + 15;   // [2] its P V product is done with it
+  uint64_t* mdone = bars + 17;    // every MMA of the CTA finished (before TMEM is freed)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bcast = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -147,9 +152,9 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       mbar_init(&vempty[s], 1);
       mbar_init(&sfull[s], 1);
       mbar_init(&sfree[s], 4);
+      mbar_init(&pready[s], 4);
+      mbar_init(&pvdone[s], 1);
     }
-    mbar_init(pready, 4);
-    mbar_init(pvdone, 1);
     mbar_init(mdone, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -216,7 +221,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, KT);
       const uint32_t idesc_o = idesc_bf16_f32(128, HD) | (1u << 16);   // B (V) MN-major
-      const uint32_t q0 = smem_u32(sQ), p0 = smem_u32(sP);
+      const uint32_t q0 = smem_u32(sQ);
       bool ok = mbar_wait(qfull, 0u, abort_flag, p.err, ERR_ATTN_FULL);
       auto issue_s = [&](int t) {
         const int s = t & 1;
@@ -240,17 +245,18 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
         const int s = t & 1;
         const uint32_t v0 = smem_u32(sKV + s * C::STAGE_BYTES + 2 * C::KV_BYTES);
         const uint32_t d = tmem + (uint32_t)C::O_COL;
+        const uint32_t pt = tmem + (uint32_t)(C::P_COL + s * KT);   // P hi columns, then P lo
         // (P part, V part): hi*hi, then lo*hi and hi*lo
         for (int pr = 0; pr < (lo ? 3 : 1); ++pr) {
-          const uint32_t pa = p0 + (pr == 1 ? C::P_BYTES : 0);
+          const uint32_t pa = pt + (pr == 1 ? (uint32_t)(KT / 2) : 0u);
           const uint32_t vb = v0 + (pr == 2 ? C::KV_BYTES : 0);
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk)
-            mma_bf16_ss(d, sdesc_sw128(pa + kk * 32), sdesc_sw128_mn(vb + kk * 2048, KT * 128), idesc_o,
+            mma_bf16_ts(d, pa + (uint32_t)(kk * 8), sdesc_sw128_mn(vb + kk * 2048, KT * 128), idesc_o,
                         (t > 0 || pr > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&vempty[s]);    // the stage's values may be refilled
-        mma_commit(pvdone);
+        mma_commit(&pvdone[s]);    // the P buffer may be rewritten
       };
       // Issue whichever is ready: P V of the oldest tile whose P is written
       // (it frees a K/V stage for the next load), or S of the next tile once
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       uint32_t spins = 0;
       while (ok && np < nt) {
         bool did = false;
-        if (np < ns && mbar_test_wait(smem_u32(pready), (uint32_t)np & 1u) &&
+        if (np < ns && mbar_test_wait(smem_u32(&pready[np & 1]), (uint32_t)(np >> 1) & 1u) &&
             mbar_test_wait(smem_u32(&vfull[np & 1]), (uint32_t)(np >> 1) & 1u)) {
           tc_fence_after();
           issue_pv(np++);
@@ -333,46 +339,50 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       }
       l = l * corr + sum;
       m = mn;
-      // P's buffer and O are free once the previous tile's P V is done
-      if (t > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(pvdone, (uint32_t)(t - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL))) {
+      // P buffer s is free once P V of tile t-2 is done; O takes a rescale
+      // only after P V of tile t-1
+      if (t >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&pvdone[s], (uint32_t)((t >> 1) - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL))) {
+        ok = false;
+        break;
+      }
+      if (t > 0 && __any_sync(0xffffffffu, up)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pvdone[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, abort_flag, p.err,
+                                               ERR_ATTN_FULL))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, up)) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < HD; c0 += 32) {
-            float o[32];
-            tmem_ld32(trow + (uint32_t)(C::O_COL + c0), o);
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          float o[32];
+          tmem_ld32(trow + (uint32_t)(C::O_COL + c0), o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= corr;
-            tmem_st32(trow + (uint32_t)(C::O_COL + c0), o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] *= corr;
+          tmem_st32(trow + (uint32_t)(C::O_COL + c0), o);
         }
       }
-      // P row into the K-major operand tile (128-byte swizzle): 8 chunks of
-      // 8 keys, chunk j of row r at ((j ^ (r % 8)) * 16) within the row
-      uint8_t* ph = sP + (row >> 3) * 1024 + (row & 7) * 128;
+      tc_fence_after();
+      // P row into P buffer s: keys 2c and 2c+1 in column c (hi), KT/2 + c (lo)
+      {
+        float ph[KT / 2], pl[KT / 2];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t h[4], lw[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          h[e] = pack_bf16(sv[8 * j + 2 * e], sv[8 * j + 2 * e + 1]);
-          lw[e] = pack_lo(sv[8 * j + 2 * e], sv[8 * j + 2 * e + 1], h[e]);
+        for (int c = 0; c < KT / 2; ++c) {
+          const uint32_t h = pack_bf16(sv[2 * c], sv[2 * c + 1]);
+          ph[c] = __uint_as_float(h);
+          pl[c] = __uint_as_float(pack_lo(sv[2 * c], sv[2 * c + 1], h));
         }
-        const int off = ((j ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(ph + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        if (lo) *reinterpret_cast<uint4*>(ph + C::P_BYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        const uint32_t pcol = trow + (uint32_t)(C::P_COL + s * KT);
+        tmem_st32(pcol, ph);
+        if (lo) tmem_st32(pcol + (uint32_t)(KT / 2), pl);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pready);
+      if (lane == 0) mbar_arrive(&pready[s]);
     }
     if (ok && nt > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(pvdone, (uint32_t)(nt - 1) & 1u, abort_flag, p.err, ERR_ATTN_FULL));
+      ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[(nt - 1) & 1], (uint32_t)((nt - 1) >> 1) & 1u, abort_flag, p.err,
+                                             ERR_ATTN_FULL));
     tc_fence_after();
     if (splits > 1) {
       // this split's partial: O relative to its reference max m, and (m, l)
@@ -403,8 +413,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
         *bcast = last;
       }
       named_bar_sync(2, 128);
-      // the probabilities' tile is free: every MMA that read it is done
-      if (*bcast) attn_merge<HD, 128>(p, work, qt, head, seq, reinterpret_cast<float*>(sP), row);
+      if (*bcast) attn_merge<HD, 128>(p, work, qt, head, seq, s_merge, row);
     } else {
       // O / l as bf16 (and its low half)
       const float il = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
