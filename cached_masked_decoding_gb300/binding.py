@@ -54,7 +54,8 @@ class Stats(ctypes.Structure):
     _fields_ = [("wall_ms", ctypes.c_double), ("refresh_ms", ctypes.c_double), ("step_ms", ctypes.c_double),
                 ("steps", ctypes.c_int32), ("refreshes", ctypes.c_int32), ("blocks", ctypes.c_int32),
                 ("max_steps_per_block", ctypes.c_int32), ("committed", ctypes.c_int64),
-                ("tau_bar", ctypes.c_double), ("kernel_launches", ctypes.c_int64)]
+                ("tau_bar", ctypes.c_double), ("kernel_launches", ctypes.c_int64),
+                ("fused_steps", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}

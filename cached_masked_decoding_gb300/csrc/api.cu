@@ -545,6 +545,7 @@ struct dllm_state {
   float* trace_buf = nullptr;
   // per-kernel timing
   bool timing = false;
+  bool fused_fwd = false;   // a no-cache step standing in for a refresh and its step: timed as refresh kernels
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> pending;
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_next = 0;
@@ -1063,7 +1064,7 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
   const int d = c.d_model, L = c.n_layers, F = m->F_pad, V = c.vocab;
   const int n = s->b * R, n_lm = s->b * s->B;
   const double wb = 2.0;  // bf16
-  const int co = refresh ? KC_REFRESH : 0;
+  const int co = (refresh || s->fused_fwd) ? KC_REFRESH : 0;
   CKS(pin_carveouts());
   s->last_row0 = row0;
   s->last_R = R;
@@ -1674,9 +1675,20 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
   const auto t0 = std::chrono::steady_clock::now();
   const long long launches0 = s->launches;
   double refresh_ms = 0, step_ms = 0;
-  int steps = 0, refreshes = 0, max_spb = 0;
+  int steps = 0, refreshes = 0, max_spb = 0, fused = 0;
   long long committed = 0, active = 0;
   const bool cached = cache_mode != DLLM_CACHE_NONE;
+  // Under the bidirectional mask a refresh is deferred to the step after it
+  // and both run as one no-cache forward of that step: the forward rewrites
+  // every layer's K/V from the current canvas (the refresh), and a cached step
+  // right after a refresh reads exactly those K/V for every key, so its block
+  // rows are the step's.  The refresh's own forward stops after the last
+  // layer's K/V; the fused one finishes the last layer and the LM head, which
+  // costs far less than a separate step.  (Block-causal refreshes are commit
+  // forwards over one block, see below.)
+  const bool fuse = cached && !s->block_causal;
+  bool pending = false;
+  int pending_j = 0, pending_spb = 0;
   std::vector<int32_t> cnt(s->b);
   // the observer sees each event after it completed; a nonzero answer stops the run
   auto notify = [&](int event, int j, int spb) -> dllm_status {
@@ -1694,10 +1706,17 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
     ++refreshes;
     return DLLM_OK;
   };
-  if (cached && s->n_blocks > 0) {
+  auto refresh_before_step = [&](int j, int spb) -> dllm_status {
+    if (fuse) {
+      pending = true;
+      pending_j = j;
+      pending_spb = spb;
+      return DLLM_OK;
+    }
     CKS(timed_refresh());
-    CKS(notify(DLLM_EVENT_REFRESH, 0, 0));
-  }
+    return notify(DLLM_EVENT_REFRESH, j, spb);
+  };
+  if (cached && s->n_blocks > 0) CKS(refresh_before_step(0, 0));
   for (int j = 0; j < s->n_blocks; ++j) {
     int spb = 0;
     for (;;) {
@@ -1708,17 +1727,27 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
         act += rem > 0;
       }
       if (!any) break;
-      if (cached && refresh_interval > 0 && spb > 0 && spb % refresh_interval == 0) {
-        CKS(timed_refresh());
-        CKS(notify(DLLM_EVENT_REFRESH, j, spb));
-      }
+      if (cached && refresh_interval > 0 && spb > 0 && spb % refresh_interval == 0) CKS(refresh_before_step(j, spb));
       int total = 0;
       SelectRule rs = r;
       if (r.policy == 4) rs.k = std::max(1, r.k - spb);   // steps left in this block
-      CKS(do_step(s, j, rs, cache_mode, cnt.data(), &total, s->ev_a, s->ev_b));
+      const bool fused_step = pending;
+      s->fused_fwd = fused_step;
+      const dllm_status st = do_step(s, j, rs, fused_step ? (int)DLLM_CACHE_NONE : cache_mode, cnt.data(), &total,
+                                     s->ev_a, s->ev_b);
+      s->fused_fwd = false;
+      CKS(st);
       float ms = 0;
       CK(cudaEventElapsedTime(&ms, s->ev_a, s->ev_b));
-      step_ms += ms;
+      if (fused_step) {
+        pending = false;
+        refresh_ms += ms;
+        ++refreshes;
+        ++fused;
+        CKS(notify(DLLM_EVENT_REFRESH, pending_j, pending_spb));
+      } else {
+        step_ms += ms;
+      }
       ++steps;
       ++spb;
       committed += total;
@@ -1743,10 +1772,13 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
         ++refreshes;
         CKS(notify(DLLM_EVENT_COMMIT_FORWARD, j, spb));
       } else {
-        CKS(timed_refresh());
-        CKS(notify(DLLM_EVENT_REFRESH, j, spb));
+        CKS(refresh_before_step(j, spb));
       }
     }
+  }
+  if (pending) {   // no step followed the last refresh
+    CKS(timed_refresh());
+    CKS(notify(DLLM_EVENT_REFRESH, pending_j, pending_spb));
   }
   if (stats) {
     stats->wall_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
@@ -1759,6 +1791,8 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
     stats->committed = committed;
     stats->tau_bar = active > 0 ? (double)committed / (double)active : 0.0;
     stats->kernel_launches = s->launches - launches0;
+    stats->fused_steps = fused;
+    stats->reserved = 0;
   }
   return DLLM_OK;
 }

@@ -103,15 +103,20 @@ typedef enum dllm_tensor {
  * T_fast ~ S * C_active + R + T_selection; selection runs inside the step). */
 typedef struct dllm_stats {
     double wall_ms;       /* whole call, host clock                             */
-    double refresh_ms;    /* R: prefill + block-boundary refreshes (CUDA events) */
-    double step_ms;       /* S * C_active: all denoise steps (CUDA events)       */
-    int32_t steps;        /* S: denoise steps run                                */
+    double refresh_ms;    /* R: prefill + refreshes (CUDA events), the fused
+                             refresh-and-step forwards included                 */
+    double step_ms;       /* the other denoise steps (CUDA events)               */
+    int32_t steps;        /* S: denoise steps run, fused ones included           */
     int32_t refreshes;    /* full-sequence forwards (prefill included)           */
     int32_t blocks;
     int32_t max_steps_per_block;
     int64_t committed;    /* tokens committed over all sequences                 */
     double tau_bar;       /* committed / sum over sequences of active steps      */
     int64_t kernel_launches; /* kernels this call launched                       */
+    int32_t fused_steps;  /* steps run as the forward of the refresh before them
+                             (counted in steps and in refreshes; their time is in
+                             refresh_ms): C_active = step_ms / (steps - fused)   */
+    int32_t reserved;
 } dllm_stats;
 
 typedef struct dllm_model dllm_model;
@@ -189,6 +194,11 @@ dllm_status dllm_denoise_step_ex(dllm_state* s, int32_t block_idx, const dllm_se
  * next block (cached modes).  Tokens stay on the device (read them with
  * dllm_read_state).  refresh_interval > 0 also refreshes after every
  * refresh_interval steps inside a block (0 = only at block boundaries).
+ * Under the bidirectional mask a refresh and the step after it run as one
+ * full forward over all T rows: it rewrites every layer's K/V from the
+ * canvas, as the refresh does, and its block rows are the step's, which
+ * after a refresh reads exactly those K/V (stats->fused_steps counts them).
+ * The run hook still sees the refresh event, then the step event.
  * stats may be NULL. */
 dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t cache_mode,
                      int32_t refresh_interval, dllm_stats* stats);
