@@ -1684,9 +1684,11 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
   // right after a refresh reads exactly those K/V for every key, so its block
   // rows are the step's.  The refresh's own forward stops after the last
   // layer's K/V; the fused one finishes the last layer and the LM head, which
-  // costs far less than a separate step.  (Block-causal refreshes are commit
-  // forwards over one block, see below.)
-  const bool fuse = cached && !s->block_causal;
+  // costs far less than a separate step.  Under the block-causal mask the
+  // same holds for the prefill and a refresh interval's refreshes (full
+  // forwards under the mask); its block-boundary refreshes are commit
+  // forwards over one block (below) and stay separate.
+  const bool fuse = cached;
   bool pending = false;
   int pending_j = 0, pending_spb = 0;
   std::vector<int32_t> cnt(s->b);

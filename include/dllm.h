@@ -194,11 +194,13 @@ dllm_status dllm_denoise_step_ex(dllm_state* s, int32_t block_idx, const dllm_se
  * next block (cached modes).  Tokens stay on the device (read them with
  * dllm_read_state).  refresh_interval > 0 also refreshes after every
  * refresh_interval steps inside a block (0 = only at block boundaries).
- * Under the bidirectional mask a refresh and the step after it run as one
- * full forward over all T rows: it rewrites every layer's K/V from the
- * canvas, as the refresh does, and its block rows are the step's, which
- * after a refresh reads exactly those K/V (stats->fused_steps counts them).
- * The run hook still sees the refresh event, then the step event.
+ * A refresh and the step after it run as one full forward over all T rows:
+ * it rewrites every layer's K/V from the canvas, as the refresh does, and its
+ * block rows are the step's, which after a refresh reads exactly those K/V
+ * (stats->fused_steps counts them).  Under the block-causal mask this covers
+ * the prefill and a refresh interval's refreshes; its block-boundary commit
+ * forwards stay separate.  The run hook still sees the refresh event, then
+ * the step event.
  * stats may be NULL. */
 dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t cache_mode,
                      int32_t refresh_interval, dllm_stats* stats);
