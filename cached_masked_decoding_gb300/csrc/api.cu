@@ -18,6 +18,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <array>
 #include <map>
 #include <mutex>
 #include <set>
@@ -200,6 +201,15 @@ AttnPlan plan_attention_persistent(int b, int H, int R, int T, int ctas) {
   a.splits = ceil_div(T, a.kps);
   return a;
 }
+
+// Persistent step kinds (see step_rows) and the shape of one phase list.
+enum StepKind : int { SK_DUAL = 0, SK_COMMIT = 1, SK_KINDS = 2 };
+struct StepShape {
+  int bn = 0;     // activation tile rows (the kernel template); 0: no list
+  int rows = 0;   // rows per sequence
+  int row0 = 0;   // position of the first row
+  AttnPlan ap = {};
+};
 
 // Query rows per sequence from which attention runs on the tensor cores
 // (128-query tiles); fewer rows use the key-split kernel.
@@ -558,10 +568,10 @@ struct dllm_state {
   bool persistent = true;
   bool step_built = false;
   bool step_split = true;
-  int step_bn = 0;
   int n_phases = 0;
   int map_kv = 0;
-  StepPhase* d_phases = nullptr;  // [n_blocks][n_phases]
+  StepPhase* d_phases = nullptr;  // [SK_KINDS][n_blocks][n_phases]
+  std::vector<StepShape> step_shape;   // [SK_KINDS][n_blocks]
   CUtensorMap* d_maps = nullptr;
   // staleness diagnostics (allocated on first use)
   uint16_t* kv_fresh = nullptr;   // K/V of a full forward over the current canvas, the cache's layout
@@ -570,7 +580,6 @@ struct dllm_state {
   float* row_cos = nullptr;       // [L][K|V][b][H][T] cosine of cached and fresh rows
   int* d_flags = nullptr;         // dataflow flags of the persistent step, zeroed per launch
   int n_flags = 0;
-  AttnPlan step_attn = {};
   // weight tiles a CTA loads for a phase before its inputs are ready: 4 of
   // the 8 ring slots (8B workload, batch 1: 4.004 ms per step against 4.030
   // with the whole ring; fewer loads queued when the phase tail runs)
@@ -675,10 +684,15 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
       attn_floats = std::max(attn_floats, works * a.splits * 16 * a.wq * (hd + 2));
       attn_cnt = std::max(attn_cnt, works);
     }
-    AttnPlan ap = plan_attention_persistent(b, (int)H, block, (int)T, m->sms);
-    const size_t pworks = (size_t)b * H * ap.q_tiles;
-    attn_floats = std::max(attn_floats, pworks * ap.splits * 16 * ap.wq * (hd + 2));
-    attn_cnt = std::max(attn_cnt, pworks);
+    // persistent step row sets: the block, two blocks (block-causal commit
+    // forward + step)
+    for (int R : {block, 2 * block}) {
+      if (R < 1 || (long long)b * R > 128) continue;
+      AttnPlan ap = plan_attention_persistent(b, (int)H, R, (int)T, m->sms);
+      const size_t pworks = (size_t)b * H * ap.q_tiles;
+      attn_floats = std::max(attn_floats, pworks * ap.splits * 16 * ap.wq * (hd + 2));
+      attn_cnt = std::max(attn_cnt, pworks);
+    }
     // row counts that take the tensor-core kernel
     for (int R : Rs) {
       if (R < kAttnTcMinRows) continue;
@@ -1186,13 +1200,33 @@ dllm_status run_forward(dllm_state* s, int row0, int R, bool refresh, int blk, c
   return DLLM_OK;
 }
 
-// Tensor-map table and per-block phase lists of the persistent DualCache step.
+// Rows of the persistent step of kind k for block j: (first row position,
+// rows per sequence); rows = 0 when that step does not run persistent.
+//   SK_DUAL    the block's B rows (DualCache);
+//   SK_COMMIT  block j-1 and block j (2B rows) under the block-causal mask:
+//              block j-1's commit forward fused with block j's first step.
+// (PrefixCache steps over rows [block start, T) were measured on this kernel
+// too, for up to 128 and up to 64 rows: no faster than the per-kernel path.)
+std::pair<int, int> step_rows(const dllm_state* s, int k, int j) {
+  const int blk = s->P + j * s->B;
+  int row0 = blk, R = s->B;
+  if (k == SK_COMMIT) {
+    if (j == 0) return {0, 0};
+    row0 = blk - s->B;
+    R = 2 * s->B;
+  }
+  // at most 128 activation rows per tile; the fused merge and select handle
+  // blocks of up to 32 positions
+  if ((long long)s->b * R > 128 || s->B > 32) return {0, 0};
+  return {row0, R};
+}
+
+// Tensor-map table and per-kind, per-block phase lists of the persistent step.
 dllm_status build_step(dllm_state* s) {
   const dllm_model* m = s->m;
   const dllm_config& c = m->cfg;
   const int d = c.d_model, L = c.n_layers, F = m->F_pad, V = c.vocab;
-  const int n = s->b * s->B;
-  const int BN = pick_bn(n, true);
+  const int n_lm = s->b * s->B;
   std::vector<CUtensorMap> maps;
   auto add = [&](const CUtensorMap& t) {
     maps.push_back(t);
@@ -1208,26 +1242,48 @@ dllm_status build_step(dllm_state* s) {
   const int i_lm = add(m->tm_lm);
   s->map_kv = add(s->tm_kv);
   CUtensorMap t;
-  auto act = [&](const uint16_t* base, int K, int* idx) -> dllm_status {
-    CKS(map_2d(&t, base, K, n, BN));
-    *idx = add(t);
+  // activation maps per (rows, tile rows): xn, xn_lo, ao, ao_lo, act, act_lo over n rows; xf, xf_lo over the block rows
+  std::map<std::pair<int, int>, std::array<int, 8>> act_maps;
+  auto act_for = [&](int n, int BN, std::array<int, 8>* out) -> dllm_status {
+    auto it = act_maps.find({n, BN});
+    if (it != act_maps.end()) {
+      *out = it->second;
+      return DLLM_OK;
+    }
+    std::array<int, 8> ix;
+    const uint16_t* base[8] = {s->xn, s->xn_lo, s->ao, s->ao_lo, s->act, s->act_lo, s->xf, s->xf_lo};
+    const int K[8] = {d, d, d, d, F, F, d, d};
+    for (int i = 0; i < 8; ++i) {
+      CKS(map_2d(&t, base[i], K[i], i < 6 ? n : n_lm, BN));
+      ix[i] = add(t);
+    }
+    act_maps.emplace(std::make_pair(n, BN), ix);
+    *out = ix;
     return DLLM_OK;
   };
-  int i_xn, i_xnl, i_ao, i_aol, i_act, i_actl, i_xf, i_xfl;
-  CKS(act(s->xn, d, &i_xn));
-  CKS(act(s->xn_lo, d, &i_xnl));
-  CKS(act(s->ao, d, &i_ao));
-  CKS(act(s->ao_lo, d, &i_aol));
-  CKS(act(s->act, F, &i_act));
-  CKS(act(s->act_lo, F, &i_actl));
-  CKS(act(s->xf, d, &i_xf));
-  CKS(act(s->xf_lo, d, &i_xfl));
 
   const int n_phases = 5 * L + 3;
-  std::vector<StepPhase> ph((size_t)s->n_blocks * n_phases);
-  for (int j = 0; j < s->n_blocks; ++j) {
-    const int blk = s->P + j * s->B;
-    StepPhase* P = &ph[(size_t)j * n_phases];
+  const int NB = s->n_blocks;
+  std::vector<StepPhase> ph((size_t)SK_KINDS * NB * n_phases);
+  std::vector<StepShape> shapes((size_t)SK_KINDS * NB);
+  for (int kind = 0; kind < SK_KINDS; ++kind)
+  for (int j = 0; j < NB; ++j) {
+    const auto rr = step_rows(s, kind, j);
+    if (rr.second == 0) continue;
+    const int blk = s->P + j * s->B;      // the block whose step this is (LM head, select)
+    const int row0 = rr.first, R = rr.second;
+    const int n = s->b * R;
+    const int BN = pick_bn(n, true);
+    std::array<int, 8> ix;
+    CKS(act_for(n, BN, &ix));
+    const int i_xn = ix[0], i_xnl = ix[1], i_ao = ix[2], i_aol = ix[3], i_act = ix[4], i_actl = ix[5], i_xf = ix[6],
+              i_xfl = ix[7];
+    StepShape& sh = shapes[(size_t)kind * NB + j];
+    sh.bn = BN;
+    sh.rows = R;
+    sh.row0 = row0;
+    sh.ap = plan_attention_persistent(s->b, c.n_heads, R, s->T, s->m->sms);
+    StepPhase* P = &ph[((size_t)kind * NB + j) * n_phases];
     int k = 0;
     P[k] = StepPhase{};
     P[k++].kind = PH_EMBED;
@@ -1245,8 +1301,8 @@ dllm_status build_step(dllm_state* s) {
       q.g.ss_in_tiles = d / 128;
       q.g.inv_d = 1.0f / d;
       q.g.eps = c.norm_eps;
-      q.g.R = s->B;
-      q.g.row0 = blk;
+      q.g.R = R;
+      q.g.row0 = row0;
       q.g.q_out = s->q;
       q.g.q_out_lo = s->split ? s->q_lo : nullptr;
       q.g.kv = s->kv;
@@ -1269,8 +1325,8 @@ dllm_status build_step(dllm_state* s) {
       o.map_b = i_ao;
       o.map_blo = i_aol;
       gemm_shape(s, o.g, d, d, n, BN);
-      o.g.R = s->B;
-      o.g.row0 = blk;
+      o.g.R = R;
+      o.g.row0 = row0;
       o.g.d_model = d;
       o.g.h = s->h;
       o.g.g_next = w.ffn_norm;
@@ -1300,8 +1356,8 @@ dllm_status build_step(dllm_state* s) {
       dn.map_b = i_act;
       dn.map_blo = i_actl;
       gemm_shape(s, dn.g, d, F, n, BN);
-      dn.g.R = s->B;
-      dn.g.row0 = blk;
+      dn.g.R = R;
+      dn.g.row0 = row0;
       dn.g.d_model = d;
       dn.g.h = s->h;
       if (last) {
@@ -1326,7 +1382,7 @@ dllm_status build_step(dllm_state* s) {
     lm.map_a = i_lm;
     lm.map_b = i_xf;
     lm.map_blo = i_xfl;
-    gemm_shape(s, lm.g, V, d, n, BN);
+    gemm_shape(s, lm.g, V, d, n_lm, BN);
     lm.g.ss_in = s->ssf;
     lm.g.ss_in_tiles = d / 128;
     lm.g.inv_d = 1.0f / d;
@@ -1345,12 +1401,21 @@ dllm_status build_step(dllm_state* s) {
   // fix-up counters; an attention phase owns one flag per head (counting
   // finished works) and a completion counter; the embedding one counter (one
   // count per CTA).
-  const AttnPlan ap = plan_attention_persistent(s->b, c.n_heads, s->B, s->T, s->m->sms);
   const int G = s->m->sms;
   std::vector<int> cnt_of(n_phases, -1), unit_of(n_phases, -1), done_of(n_phases, -1);
   int n_flags = 0;
+  size_t first = 0;
+  while (first < shapes.size() && shapes[first].rows == 0) ++first;
+  if (first == shapes.size()) {
+    set_error("persistent step: no block fits");
+    return DLLM_EINVAL;
+  }
   for (int k = 0; k < n_phases; ++k) {
-    const StepPhase& q = ph[k];
+    const StepPhase& q = ph[first * n_phases + k];
+    if (q.kind == PH_GEMM && q.g.n_tiles != 1) {
+      set_error("persistent step: %d activation tiles in a phase", q.g.n_tiles);
+      return DLLM_EINVAL;
+    }
     if (q.kind == PH_EMBED) {
       done_of[k] = n_flags++;
     } else if (q.kind == PH_ATTN) {
@@ -1376,8 +1441,11 @@ dllm_status build_step(dllm_state* s) {
     CKS(dev_alloc((void**)&s->d_flags, (size_t)n_flags * 4));
     s->n_flags = n_flags;
   }
-  for (int j = 0; j < s->n_blocks; ++j) {
-    StepPhase* P = &ph[(size_t)j * n_phases];
+  for (size_t li = 0; li < shapes.size(); ++li) {
+    if (shapes[li].rows == 0) continue;
+    const int BN = shapes[li].bn;
+    const AttnPlan& ap = shapes[li].ap;
+    StepPhase* P = &ph[li * n_phases];
     int gemm_ord = 0;
     for (int k = 0; k < n_phases; ++k) {
       StepPhase& q = P[k];
@@ -1445,37 +1513,44 @@ dllm_status build_step(dllm_state* s) {
   CK(cudaMemcpy(s->d_phases, ph.data(), ph.size() * sizeof(StepPhase), cudaMemcpyHostToDevice));
   CK(cudaMemcpy(s->d_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
   s->n_phases = n_phases;
-  s->step_bn = BN;
+  s->step_shape = shapes;
   s->step_split = s->split;
-  s->step_attn = plan_attention_persistent(s->b, c.n_heads, s->B, s->T, s->m->sms);
   s->step_built = true;
   return DLLM_OK;
 }
 
-bool use_persistent(const dllm_state* s, int mode) {
-  return s->persistent && mode == DLLM_CACHE_DUAL && !s->trace && s->b * s->B <= 128 && s->B <= 32;
+// The persistent step of kind k runs block j's step when its rows fit.
+bool use_persistent(const dllm_state* s, int kind, int j) {
+  return s->persistent && !s->trace && step_rows(s, kind, j).second > 0;
 }
 
-// One DualCache denoise step of block j as a single cooperative launch.
-dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
+// One denoise step of block j as a single cooperative launch: DualCache, or
+// (block-causal) block j-1's commit forward with block j's first step.
+dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule, int kind) {
   if (!s->step_built || s->step_split != s->split) CKS(build_step(s));
   const dllm_model* m = s->m;
   const dllm_config& c = m->cfg;
   const int d = c.d_model, V = c.vocab;
   const int blk = s->P + j * s->B;
   const int n = s->b * s->B;
-  s->last_row0 = blk;
-  s->last_R = s->B;
+  const size_t li = (size_t)kind * s->n_blocks + j;
+  const StepShape& sh = s->step_shape[li];
+  if (sh.rows == 0) {
+    set_error("no persistent step of kind %d for block %d", kind, j);
+    return DLLM_EINVAL;
+  }
+  s->last_row0 = sh.row0;
+  s->last_R = sh.rows;
   s->last_blk = blk;
   StepArgs a = {};
-  a.phases = s->d_phases + (size_t)j * s->n_phases;
+  a.phases = s->d_phases + li * s->n_phases;
   a.n_phases = s->n_phases;
   a.maps = s->d_maps;
   a.flags = s->d_flags;
   a.err = s->count_err + s->b;
   a.emb = EmbedParams{s->x, m->embed, m->layers[0].attn_norm, s->h, s->xn, s->split ? s->xn_lo : nullptr, s->ss,
-                      d, s->B, blk, s->T};
-  const AttnPlan& ap = s->step_attn;
+                      d, sh.rows, sh.row0, s->T};
+  const AttnPlan& ap = sh.ap;
   const int QT = 32;
   const long long works = (long long)s->b * c.n_heads * ap.q_tiles;
   a.attn.q = s->q;
@@ -1483,11 +1558,11 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
   a.attn.kv_lo = s->split ? 1 : 0;
   a.attn.o = s->ao;
   a.attn.o_lo = s->split ? s->ao_lo : nullptr;
-  a.attn.R = s->B;
+  a.attn.R = sh.rows;
   a.attn.b = s->b;
   a.attn.H = c.n_heads;
   a.attn.T = s->T;
-  a.attn.row0 = blk;
+  a.attn.row0 = sh.row0;
   a.attn.mask_P = s->P;
   a.attn.mask_B = s->block_causal ? s->B : 0;
   a.attn.q_tiles = ap.q_tiles;
@@ -1529,8 +1604,8 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule) {
   if (s->timing) s->kt_bytes[KC_PSTEP] += bytes;
   Timed t(s, KC_PSTEP, bytes);
   const int grid = s->m->sms;
-  cudaError_t e = c.head_dim == 64 ? launch_step_hd64(s->step_bn, a, grid, s->st)
-                                   : launch_step_hd128(s->step_bn, a, grid, s->st);
+  cudaError_t e = c.head_dim == 64 ? launch_step_hd64(sh.bn, a, grid, s->st)
+                                   : launch_step_hd128(sh.bn, a, grid, s->st);
   CK(e);
   ++s->launches;
   return DLLM_OK;
@@ -1574,8 +1649,10 @@ dllm_status do_refresh(dllm_state* s, cudaEvent_t e0 = nullptr, cudaEvent_t e1 =
   return finish_sync(s);
 }
 
+// commit_prev (block-causal runs, dllm_run): block j-1's commit forward runs
+// in the same persistent launch as this step (the caller checked it fits).
 dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int32_t* committed, int* total,
-                    cudaEvent_t e0 = nullptr, cudaEvent_t e1 = nullptr) {
+                    cudaEvent_t e0 = nullptr, cudaEvent_t e1 = nullptr, bool commit_prev = false) {
   if (j < 0 || j >= s->n_blocks) {
     set_error("block_idx %d outside [0, %d)", j, s->n_blocks);
     return DLLM_EINVAL;
@@ -1598,8 +1675,13 @@ dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int3
   }
   if (e0) CK(cudaEventRecord(e0, s->st));
   CK(cudaMemsetAsync(s->count_err, 0, (s->b + 1) * 4, s->st));
-  if (use_persistent(s, mode)) {
-    CKS(run_step_persistent(s, j, rule));
+  const int kind = commit_prev ? SK_COMMIT : mode == DLLM_CACHE_DUAL ? SK_DUAL : -1;
+  if (commit_prev && !use_persistent(s, SK_COMMIT, j)) {
+    set_error("block %d: the fused commit forward does not fit one launch", j);
+    return DLLM_EINVAL;
+  }
+  if (kind >= 0 && use_persistent(s, kind, j)) {
+    CKS(run_step_persistent(s, j, rule, kind));
   } else {
     CKS(run_forward(s, row0, R, false, blk, rule));
   }
@@ -1691,6 +1773,12 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
   const bool fuse = cached;
   bool pending = false;
   int pending_j = 0, pending_spb = 0;
+  // Block-causal: block j's commit forward is deferred to block j+1's first
+  // step when both fit one persistent launch (2B rows): one forward over the
+  // two blocks writes block j's K/V from the final canvas and runs block
+  // j+1's step, whose rows see block j's fresh K/V in the same layer.
+  bool pending_commit = false;
+  int commit_j = 0, commit_spb = 0;
   std::vector<int32_t> cnt(s->b);
   // the observer sees each event after it completed; a nonzero answer stops the run
   auto notify = [&](int event, int j, int spb) -> dllm_status {
@@ -1734,19 +1822,22 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
       SelectRule rs = r;
       if (r.policy == 4) rs.k = std::max(1, r.k - spb);   // steps left in this block
       const bool fused_step = pending;
+      const bool commit_step = pending_commit;
       s->fused_fwd = fused_step;
       const dllm_status st = do_step(s, j, rs, fused_step ? (int)DLLM_CACHE_NONE : cache_mode, cnt.data(), &total,
-                                     s->ev_a, s->ev_b);
+                                     s->ev_a, s->ev_b, commit_step);
       s->fused_fwd = false;
       CKS(st);
       float ms = 0;
       CK(cudaEventElapsedTime(&ms, s->ev_a, s->ev_b));
-      if (fused_step) {
-        pending = false;
+      if (fused_step || commit_step) {
         refresh_ms += ms;
         ++refreshes;
         ++fused;
-        CKS(notify(DLLM_EVENT_REFRESH, pending_j, pending_spb));
+        if (fused_step) CKS(notify(DLLM_EVENT_REFRESH, pending_j, pending_spb));
+        if (commit_step) CKS(notify(DLLM_EVENT_COMMIT_FORWARD, commit_j, commit_spb));
+        pending = false;
+        pending_commit = false;
       } else {
         step_ms += ms;
       }
@@ -1758,7 +1849,11 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
     }
     max_spb = std::max(max_spb, spb);
     if (cached && j + 1 < s->n_blocks) {
-      if (s->block_causal) {
+      if (s->block_causal && cache_mode == DLLM_CACHE_DUAL && use_persistent(s, SK_COMMIT, j + 1)) {
+        pending_commit = true;
+        commit_j = j;
+        commit_spb = spb;
+      } else if (s->block_causal) {
         // nothing earlier attends to a later block: caching the finished
         // block's own K/V (one block forward) makes the cache exact again
         CK(cudaEventRecord(s->ev_a, s->st));

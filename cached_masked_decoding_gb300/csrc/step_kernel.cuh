@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
       if (P.rs_done >= 0 && l128 == 0) flag_wait(a.flags + P.rs_done, P.rs_need, abort_flag, a.err);
       if (named_bar_or(1, 128, *abort_flag != 0)) break;
       if (P.kind == PH_EMBED) {
-        embed_rows(a.emb, a.merge.n_rows, (int)cta, (int)G, l128);
+        embed_rows(a.emb, a.attn.b * a.emb.R, (int)cta, (int)G, l128);
         named_bar_sync(1, 128);
         if (l128 == 0) flag_publish(a.flags + P.done, nullptr);
       } else if (P.kind == PH_ATTN) {

@@ -198,9 +198,10 @@ dllm_status dllm_denoise_step_ex(dllm_state* s, int32_t block_idx, const dllm_se
  * it rewrites every layer's K/V from the canvas, as the refresh does, and its
  * block rows are the step's, which after a refresh reads exactly those K/V
  * (stats->fused_steps counts them).  Under the block-causal mask this covers
- * the prefill and a refresh interval's refreshes; its block-boundary commit
- * forwards stay separate.  The run hook still sees the refresh event, then
- * the step event.
+ * the prefill and a refresh interval's refreshes, and in DualCache runs each
+ * block-boundary commit forward (block j's K/V from the final canvas) runs in
+ * one launch with block j+1's first step, over both blocks' rows.  The run
+ * hook still sees the refresh (or commit-forward) event, then the step event.
  * stats may be NULL. */
 dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t cache_mode,
                      int32_t refresh_interval, dllm_stats* stats);
