@@ -89,21 +89,24 @@ def test_1b_long_context_two_blocks(torch):
     gm.free()
 
 
-def test_1b_prefix_cache_two_blocks(torch):
+@pytest.mark.parametrize("mask", ["full", "block_causal"])
+def test_1b_prefix_cache_two_blocks(torch, mask):
     """PrefixCache on the 1B model (every step recomputes rows [block start,
     T)): the 128 and 96 query rows of blocks 0 and 1 take the tensor-core
     attention, whose plan cuts each query tile's 384 keys into six ranges and
-    merges their partial softmax states; checked under the trajectory-sync
-    rule like the DualCache trajectory."""
+    merges their partial softmax states; under the block-causal mask the rows
+    of a query tile also stop at different keys.  Checked under the
+    trajectory-sync rule like the DualCache trajectory."""
     wl = configs.WORKLOADS["1b"]
     cfg = wl.model
     gm = binding.Model.from_synth(cfg, seed=wl.seed)
     pr = synth.prompts(cfg, wl.seed, wl.batch, wl.prompt_len)
     st = binding.State(gm, pr, wl.batch, wl.prompt_len, wl.gen_len, wl.block)
-    dec = OS.Decoder(OM.load_weights(cfg, wl.seed), pr, wl.gen_len, wl.block, "prefix")
+    st.set_mask(mask)
+    dec = OS.Decoder(OM.load_weights(cfg, wl.seed), pr, wl.gen_len, wl.block, "prefix", mask=mask)
     rep = run_synced(st, dec, OS.Rule(OS.THRESHOLD, wl.tau), "prefix", max_blocks=2)
-    print("1b prefix:", rep)
-    rep.log(workload="1b_prefix", T=wl.T)
+    print("1b prefix:", mask, rep)
+    rep.log(workload="1b_prefix", T=wl.T, mask=mask)
     assert (st.tokens()[:, wl.prompt_len:wl.prompt_len + 2 * wl.block] != cfg.mask_id).all()
     st.free()
     gm.free()
