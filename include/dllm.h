@@ -213,11 +213,14 @@ dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t cache_mode,
  * prefill and every refresh (block boundary, or the refresh interval inside a
  * block), DLLM_EVENT_STEP after every denoise step, DLLM_EVENT_COMMIT_FORWARD
  * after the forward over a finished block that replaces the block-boundary
- * refresh under the block-causal mask.  Inside the hook the state may be read
- * (dllm_read_state, dllm_read_hidden, dllm_read_kv) but not changed.  A
- * nonzero return stops the run: dllm_run returns DLLM_ECANCELLED, with the
- * canvas as the last completed event left it.  Use: stream committed tokens
- * to a caller, or follow the loop's decisions step by step. */
+ * refresh under the block-causal mask.  A refresh (or commit forward) that
+ * runs in one forward with the step after it is reported right before that
+ * step's event, once both are done: the canvas then already holds the step's
+ * commits.  Inside the hook the state may be read (dllm_read_state,
+ * dllm_read_hidden, dllm_read_kv) but not changed.  A nonzero return stops
+ * the run: dllm_run returns DLLM_ECANCELLED, with the canvas as the last
+ * completed forward left it.  Use: stream committed tokens to a caller, or
+ * follow the loop's decisions step by step. */
 typedef enum dllm_event { DLLM_EVENT_REFRESH = 0, DLLM_EVENT_STEP = 1, DLLM_EVENT_COMMIT_FORWARD = 2 } dllm_event;
 typedef int32_t (*dllm_run_hook)(void* user, int32_t event, int32_t block_idx, int32_t step_in_block);
 
