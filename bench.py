@@ -266,6 +266,7 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     state = binding.State(model, None, b, P, gen, B, stream=stream.cuda_stream)
     state.set_precision(args.precision)
     state.set_persistent(args.persistent)
+    state.set_fused_refresh(args.fused_refresh)
     state.set_mask(args.mask)
     if args.rule == "fixed":
         sel = binding.make_select(binding.SEL_FIXED_K, wl.tau, args.k)
@@ -423,6 +424,8 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
             "mask": "bidirectional" if args.mask == "full" else "block-causal (refresh = one block forward)",
             "step_launch": "persistent (one cooperative launch per denoise step)" if args.persistent
             else "one launch per kernel",
+            "refresh": "fused with the step after it (one forward)" if args.fused_refresh
+            else "separate forward, then the step",
             "l2": "inputs larger than L2 (every step streams all weights)",
             "parallelism": f"replicas x{world} (no data-path collective)",
         },
@@ -540,6 +543,8 @@ def main():
                     help="attention mask: bidirectional (the method's) or block-causal (exact cache)")
     ap.add_argument("--no-persistent", dest="persistent", action="store_false",
                     help="one launch per kernel instead of the persistent DualCache step")
+    ap.add_argument("--no-fused-refresh", dest="fused_refresh", action="store_false",
+                    help="run every refresh (and block-causal commit forward) apart from the step after it")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
     import dataclasses

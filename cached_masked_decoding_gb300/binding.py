@@ -95,6 +95,7 @@ SIGNATURES = {
     "dllm_op_gemm": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _P]),
     "dllm_state_set_precision": (_I32, [_P, _I32]),
     "dllm_state_set_persistent": (_I32, [_P, _I32]),
+    "dllm_state_set_fused_refresh": (_I32, [_P, _I32]),
     "dllm_state_set_mask": (_I32, [_P, _I32]),
     "dllm_state_set_step_timeline": (_I32, [_P, _I32]),
     "dllm_read_step_timeline": (_I32, [_P, _P, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
@@ -290,6 +291,9 @@ class State:
 
     def set_persistent(self, on: bool):
         check(lib().dllm_state_set_persistent(self.h, 1 if on else 0))
+
+    def set_fused_refresh(self, on: bool):
+        check(lib().dllm_state_set_fused_refresh(self.h, 1 if on else 0))
 
     def set_mask(self, mask: str):
         check(lib().dllm_state_set_mask(self.h, {"full": 0, "block_causal": 1}[mask]))

@@ -556,6 +556,7 @@ struct dllm_state {
   // per-kernel timing
   bool timing = false;
   bool fused_fwd = false;   // a no-cache step standing in for a refresh and its step: timed as refresh kernels
+  bool fuse_refresh = true; // dllm_run fuses refreshes and commit forwards with the step after them
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> pending;
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_next = 0;
@@ -1770,7 +1771,7 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
   // same holds for the prefill and a refresh interval's refreshes (full
   // forwards under the mask); its block-boundary refreshes are commit
   // forwards over one block (below) and stay separate.
-  const bool fuse = cached;
+  const bool fuse = cached && s->fuse_refresh;
   bool pending = false;
   int pending_j = 0, pending_spb = 0;
   // Block-causal: block j's commit forward is deferred to block j+1's first
@@ -1849,7 +1850,7 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
     }
     max_spb = std::max(max_spb, spb);
     if (cached && j + 1 < s->n_blocks) {
-      if (s->block_causal && cache_mode == DLLM_CACHE_DUAL && use_persistent(s, SK_COMMIT, j + 1)) {
+      if (s->block_causal && s->fuse_refresh && cache_mode == DLLM_CACHE_DUAL && use_persistent(s, SK_COMMIT, j + 1)) {
         pending_commit = true;
         commit_j = j;
         commit_spb = spb;
@@ -2002,6 +2003,15 @@ extern "C" dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable) 
     return DLLM_EINVAL;
   }
   s->persistent = enable != 0;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_fused_refresh(dllm_state* s, int32_t enable) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  s->fuse_refresh = enable != 0;
   return DLLM_OK;
 }
 

@@ -272,6 +272,14 @@ dllm_status dllm_state_set_precision(dllm_state* s, int32_t mode);
  * attention key split; tracing always uses it). */
 dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable);
 
+/* dllm_run's fused forwards (on by default): a refresh and the step after it
+ * run as one forward, and under the block-causal mask a DualCache run's
+ * commit forward shares a launch with the next block's first step (see
+ * dllm_run).  enable 0 runs every refresh and commit forward on its own, then
+ * the step, as Algorithm 1 lists them; the trajectory is the same up to the
+ * kernels' rounding. */
+dllm_status dllm_state_set_fused_refresh(dllm_state* s, int32_t enable);
+
 /* Attention mask.  DLLM_MASK_BIDIRECTIONAL (default): every position sees
  * every position, the Fast-dLLM setting, in which the cached prefix and
  * suffix go stale and a block-boundary refresh recomputes them.

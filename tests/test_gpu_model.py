@@ -260,7 +260,8 @@ def test_run_loop_matches_oracle(gmodel, omodel, mode, rule):
     """dllm_run - the block/step loop the bench times, with its refresh
     points, the skipped refresh after the last block, the lockstep batch and
     the scheduled rule's countdown - against the oracle's Algorithm 1, event
-    by event (notes, section 3, Algorithm 1)."""
+    by event (notes, section 3, Algorithm 1).  Each refresh runs fused with
+    the step after it (the default)."""
     P, gen, B, b = 24, 48, 16, 2
     pr = synth.prompts(CFG, 8, b, P)
     st = binding.State(gmodel, pr, b, P, gen, B)
@@ -268,9 +269,27 @@ def test_run_loop_matches_oracle(gmodel, omodel, mode, rule):
     rep, stats = run_loop_synced(st, dec, RULES[rule], mode)
     print(mode, rule, rep)
     assert stats["refreshes"] == (gen // B if mode != "none" else 0)
+    assert stats["fused_steps"] == stats["refreshes"]
     assert stats["committed"] == b * gen and (st.tokens()[:, P:] != CFG.mask_id).all()
     if rule == "schedule":
         assert stats["steps"] == RULES[rule].k * (gen // B)
+    st.free()
+
+
+@pytest.mark.parametrize("mask", ["full", "block_causal"])
+def test_run_loop_unfused_matches_oracle(gmodel, omodel, mask):
+    """dllm_run with every refresh (and block-causal commit forward) run on
+    its own before the step after it, as Algorithm 1 lists them: the same
+    events and the same trajectory-sync bar as the fused default."""
+    P, gen, B, b = 24, 48, 16, 2
+    pr = synth.prompts(CFG, 8, b, P)
+    st = binding.State(gmodel, pr, b, P, gen, B)
+    st.set_mask(mask)
+    st.set_fused_refresh(False)
+    dec = OS.Decoder(omodel, pr, gen, B, "dual", mask=mask)
+    rep, stats = run_loop_synced(st, dec, RULES["threshold"], "dual")
+    print(mask, rep)
+    assert stats["fused_steps"] == 0 and stats["refreshes"] == gen // B
     st.free()
 
 
