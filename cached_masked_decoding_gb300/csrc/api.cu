@@ -168,6 +168,7 @@ int device_sms() {
 
 struct AttnPlan {
   int wq, q_tiles, splits, kps;
+  long long n_whole = 0;   // tensor-core plan: leading query tiles run unsplit (whole waves)
 };
 
 AttnPlan plan_attention(int b, int H, int R, int T, int sms) {
@@ -216,29 +217,56 @@ struct StepShape {
 constexpr int kAttnTcMinRows = 65;
 
 // Plan of the tensor-core attention (128-query tiles, 64-key tiles): key
-// splits when the query tiles alone leave most SMs idle.  One CTA per SM; the
-// cost of s splits is taken as rounds x (key tiles per split + fixed work):
-// one tile's worth without splits, four with them (the partial's stores and
-// the last split's merge; measured on GB300: the 8B refresh's 192 query tiles
-// took 65.7 us unsplit and 73.9 us in two splits, a PrefixCache step's 64
-// tiles 33.8 and 29.0 us).  Splits are taken only when they promise at least
-// a fifth less time; at most 8 (the merge keeps 128 x splits weights in the
-// probabilities' tile).
+// splits when the query tiles fill the GPU's SMs unevenly.  One CTA per SM;
+// the cost of a round of CTAs is taken as the key tiles a CTA walks plus
+// fixed work: one tile's worth unsplit, four with a partial and its merge
+// (measured on GB300: the 8B refresh's 192 query tiles took 65.7 us unsplit
+// and 73.9 us with every tile in two splits; a PrefixCache step's 64 tiles
+// 33.8 and 29.0 us).  Two shapes are weighed: every query tile in s splits,
+// or whole waves of unsplit tiles followed by the remaining tiles in s
+// splits.  Splits are taken only when they promise at least a tenth less
+// time; at most 8 (the merge keeps 128 x splits weights in shared memory).
 AttnPlan plan_attention_tc(int b, int H, int R, int T, int sms) {
   AttnPlan a;
   a.wq = 8;
   a.q_tiles = ceil_div(R, 128);
   const long long items = (long long)b * H * a.q_tiles;
   const int kt = std::max(1, ceil_div(T, 64));
-  auto cost = [&](int sp) { return ((items * sp + sms - 1) / sms) * (ceil_div(kt, sp) + (sp > 1 ? 4 : 1)); };
-  int best = 1;
-  for (int sp = 2; sp <= 8 && sp <= kt; ++sp)
-    if (cost(sp) < cost(best)) best = sp;
-  if (best > 1 && 5 * cost(best) > 4 * cost(1)) best = 1;
-  a.kps = ceil_div(kt, best) * 64;
+  auto rounds = [&](long long n) { return (n + sms - 1) / sms; };
+  auto per = [&](int sp) { return (long long)ceil_div(kt, sp) + (sp > 1 ? 4 : 1); };
+  const long long unsplit = rounds(items) * per(1);
+  const long long whole = (items / sms) * sms, rem = items - whole;
+  long long best = unsplit, best_whole = 0;
+  int best_sp = 1;
+  for (int sp = 2; sp <= 8 && sp <= kt; ++sp) {
+    const long long uniform = rounds(items * sp) * per(sp);
+    if (uniform < best) {
+      best = uniform;
+      best_sp = sp;
+      best_whole = 0;
+    }
+    if (whole > 0 && rem > 0) {
+      const long long hybrid = (whole / sms) * per(1) + rounds(rem * sp) * per(sp);
+      if (hybrid < best) {
+        best = hybrid;
+        best_sp = sp;
+        best_whole = whole;
+      }
+    }
+  }
+  if (best_sp > 1 && 10 * best > 9 * unsplit) {
+    best_sp = 1;
+    best_whole = 0;
+  }
+  a.kps = ceil_div(kt, best_sp) * 64;
   a.splits = ceil_div(T, a.kps);
+  a.n_whole = a.splits > 1 ? best_whole : 0;
   return a;
 }
+
+// CTAs of a tensor-core plan and the query tiles that go through the merge.
+long long tc_ctas(const AttnPlan& a, long long items) { return a.n_whole + (items - a.n_whole) * a.splits; }
+long long tc_split_items(const AttnPlan& a, long long items) { return a.splits > 1 ? items - a.n_whole : 0; }
 
 }  // namespace
 
@@ -699,7 +727,7 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
       if (R < kAttnTcMinRows) continue;
       AttnPlan at = plan_attention_tc(b, (int)H, R, (int)T, m->sms);
       if (at.splits < 2) continue;
-      const size_t works = (size_t)b * H * at.q_tiles;
+      const size_t works = (size_t)tc_split_items(at, (long long)b * H * at.q_tiles);
       attn_floats = std::max(attn_floats, works * at.splits * 128 * (hd + 2));
       attn_cnt = std::max(attn_cnt, works);
     }
@@ -995,7 +1023,8 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
       it = s->kv64_maps.emplace(s->kv, m).first;
     }
     AttnPlan at = plan_attention_tc(s->b, c.n_heads, R, s->T, s->m->sms);
-    const size_t tc_works = (size_t)s->b * c.n_heads * at.q_tiles;
+    const long long tc_items = (long long)s->b * c.n_heads * at.q_tiles;
+    const size_t tc_works = (size_t)tc_split_items(at, tc_items);
     if (at.splits > 1 &&
         (tc_works * at.splits * 128 * (c.head_dim + 2) > s->attn_o_floats || tc_works > s->attn_cnt_n)) {
       set_error("attention merge workspace too small for %d rows", R);
@@ -1014,8 +1043,9 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
     p.q_tiles = at.q_tiles;
     p.splits = at.splits;
     p.kps = at.kps;
+    p.n_whole = (int)at.n_whole;
     p.ws_o = s->attn_o;
-    p.ws_ml = s->attn_o + (long long)s->b * c.n_heads * at.q_tiles * at.splits * 128 * c.head_dim;
+    p.ws_ml = s->attn_o + (long long)tc_works * at.splits * 128 * c.head_dim;
     p.counters = s->attn_cnt;
     p.z_k0 = ((layer * 2 + 0) * 2 + 0) * bh;
     p.z_kl0 = ((layer * 2 + 0) * 2 + 1) * bh;
@@ -1028,8 +1058,8 @@ dllm_status run_attention(dllm_state* s, int layer, int R, int cls, double bytes
     p.err = s->count_err + s->b;
     if (s->timing) s->kt_bytes[cls] += bytes;
     Timed t(s, cls, bytes);
-    CK(launch_attention_tc(c.head_dim, *tq, *tqlo, it->second, it->second, p,
-                           dim3(at.q_tiles * at.splits, c.n_heads, s->b), s->st, true));
+    CK(launch_attention_tc(c.head_dim, *tq, *tqlo, it->second, it->second, p, dim3((unsigned)tc_ctas(at, tc_items)),
+                           s->st, true));
     ++s->launches;
     return DLLM_OK;
   }
@@ -2285,8 +2315,10 @@ extern "C" dllm_status dllm_op_attention_tc_ex(const uint16_t* q, const uint16_t
   if (splits > 0) {
     at.kps = ceil_div(ceil_div(T, 64), splits) * 64;
     at.splits = ceil_div(T, at.kps);
+    at.n_whole = 0;
   }
-  const long long works = (long long)b * H * at.q_tiles;
+  const long long items = (long long)b * H * at.q_tiles;
+  const long long works = tc_split_items(at, items);
   OpWorkspace* w = nullptr;
   CKS(op_workspace(&w, 1, at.splits > 1 ? (size_t)works * at.splits * 128 * (hd + 2) : 0,
                    at.splits > 1 ? (size_t)works : 0));
@@ -2300,13 +2332,14 @@ extern "C" dllm_status dllm_op_attention_tc_ex(const uint16_t* q, const uint16_t
   p.q_tiles = at.q_tiles;
   p.splits = at.splits;
   p.kps = at.kps;
+  p.n_whole = (int)at.n_whole;
   p.ws_o = w->attn;
   p.ws_ml = w->attn + works * at.splits * 128 * hd;
   p.counters = w->attn_cnt;
   p.scale_log2 = kLog2e / std::sqrt((float)hd);
   p.err = w->err;
-  CK(launch_attention_tc(hd, tq, tq, tk, tv, p, dim3(at.q_tiles * at.splits, H, b),
-                         static_cast<cudaStream_t>(stream), false));
+  CK(launch_attention_tc(hd, tq, tq, tk, tv, p, dim3((unsigned)tc_ctas(at, items)), static_cast<cudaStream_t>(stream),
+                         false));
   return DLLM_OK;
 }
 

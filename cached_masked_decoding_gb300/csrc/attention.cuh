@@ -39,6 +39,7 @@ struct AttnParams {
   // mask_P + ((p - mask_P) / mask_B + 1) * mask_B.  mask_B = 0: every key.
   int row0, mask_P, mask_B;
   int q_tiles, splits, kps;  // query tiles per (seq, head), key splits, keys per split (multiple of 64)
+  int n_whole;         // tensor-core kernel: leading query tiles run unsplit, the rest in `splits` splits
   float scale_log2;    // log2(e) / sqrt(HD)
   float* ws_o;         // [works][splits][QT][HD]
   float* ws_ml;        // [works][splits][QT][2]

@@ -97,9 +97,12 @@ __device__ __forceinline__ int tc_key_limit(const AttnParams& p, int pos) {
   return lim < p.T ? lim : p.T;
 }
 
-// grid (query tiles of 128 x p.splits, H, b), 192 threads; p.splits > 1
-// needs p.kps (a multiple of 64), p.q_tiles and the merge workspace
-// (p.ws_o, p.ws_ml, p.counters).  tmQ/tmQlo: 2-D maps over
+// 1-D grid, 192 threads.  Query tiles (items, numbered (seq * H + head) *
+// q_tiles + qt, so that neighbouring CTAs share a head's keys in L2): the
+// first p.n_whole run unsplit, one CTA each; every later one in p.splits key
+// ranges of p.kps keys (a multiple of 64), merged in the workspace (p.ws_o,
+// p.ws_ml, p.counters, indexed from the first split item).  Grid:
+// n_whole + (items - n_whole) * splits CTAs.  tmQ/tmQlo: 2-D maps over
 // q / q_lo [b*R][H*HD] with 128-row boxes; tmK/tmV: 3-D maps over the K and V
 // planes with 64-key boxes (the same map may serve both).
 template <int HD>
@@ -130,8 +133,18 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   int* bcast = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int splits = p.splits > 1 ? p.splits : 1;
-  const int qt = blockIdx.x / splits, split = blockIdx.x - qt * splits, head = blockIdx.y, seq = blockIdx.z;
+  int item, split, splits;
+  if ((int)blockIdx.x < p.n_whole) {
+    item = (int)blockIdx.x;
+    split = 0;
+    splits = 1;
+  } else {
+    const int r = (int)blockIdx.x - p.n_whole;
+    splits = p.splits > 1 ? p.splits : 1;
+    item = p.n_whole + r / splits;
+    split = r - (r / splits) * splits;
+  }
+  const int qt = item % p.q_tiles, head = (item / p.q_tiles) % p.H, seq = item / (p.q_tiles * p.H);
   const bool lo = p.kv_lo != 0;
   const int parts = lo ? 2 : 1;
   // keys this tile's rows see at most: limits grow with the position
@@ -386,7 +399,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
     tc_fence_after();
     if (splits > 1) {
       // this split's partial: O relative to its reference max m, and (m, l)
-      const long long work = ((long long)seq * p.H + head) * p.q_tiles + qt;
+      const long long work = item - p.n_whole;   // merge slot of this split item
       const long long wrow = (work * splits + split) * 128 + row;
       float* wo = p.ws_o + wrow * HD;
 #pragma unroll 1

@@ -131,6 +131,7 @@ TC_ATTN_SHAPES = [
     (1, 1, 64, 70, 1),       # a single key
     (3, 1, 128, 65, 63),     # fewer keys than one tile; three sequences of 65 rows
     (2, 2, 64, 129, 129),    # one row and one key past a tile boundary
+    (1, 40, 128, 512, 512),  # 160 query tiles: planned as one whole wave of 152 and 8 tiles in key splits
 ]
 
 
