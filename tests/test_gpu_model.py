@@ -416,7 +416,9 @@ def test_block_causal_commit_forward_keeps_cache_exact(gmodel, omodel):
     by one forward over the finished block; the cache stays exact, so the
     DualCache run (persistent step) must decode what the oracle's no-cache
     decoder does under the same mask, step by step under the
-    trajectory-sync rule."""
+    trajectory-sync rule.  The prefill runs with block 0's first step, and
+    each commit forward in one persistent launch with the next block's first
+    step (2B rows per sequence, two sequences)."""
     P, gen, B = 32, 64, 16
     pr = synth.prompts(CFG, 7, 2, P)
     st = binding.State(gmodel, pr, 2, P, gen, B)
@@ -425,6 +427,7 @@ def test_block_causal_commit_forward_keeps_cache_exact(gmodel, omodel):
     rep, stats = run_loop_synced(st, ref, RULES["threshold"], "dual", ignore_refreshes=True)
     print(rep)
     assert stats["refreshes"] == gen // B       # the prefill plus one commit forward per finished block but the last
+    assert stats["fused_steps"] == gen // B
     assert (st.tokens()[:, P:] != CFG.mask_id).all()
     st.free()
 
