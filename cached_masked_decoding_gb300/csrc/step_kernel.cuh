@@ -131,22 +131,26 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 
 // Wait until *f >= need (acquire), then order later TMA reads after it.
 // Bounded by limit_ns; gives up early once this CTA raised *abort or any
-// CTA recorded an error; on giving up records `site` in err.
+// CTA recorded an error; on giving up records `site` in err.  The poll is
+// one acquire load per round trip (one thread per CTA polls); the error word
+// and the clock are looked at every 16th round, so a flag raised between
+// two polls is seen one L2 round trip later at most.
 __device__ __forceinline__ bool flag_wait_for(const int* f, int need, volatile int* abort, int* err,
                                               unsigned long long limit_ns, int site) {
   if (ld_acquire_gpu(f) < need) {
     const unsigned long long t0 = globaltimer();
-    for (;;) {
-      __nanosleep(32);
+    for (uint32_t i = 1;; ++i) {
       if (ld_acquire_gpu(f) >= need) break;
-      if (*abort || ld_relaxed_gpu(err) != 0) {
-        *abort = 1;
-        return false;
-      }
-      if (globaltimer() - t0 > limit_ns) {
-        *abort = 1;
-        record_error(err, site);
-        return false;
+      if ((i & 15u) == 0) {
+        if (*abort || ld_relaxed_gpu(err) != 0) {
+          *abort = 1;
+          return false;
+        }
+        if (globaltimer() - t0 > limit_ns) {
+          *abort = 1;
+          record_error(err, site);
+          return false;
+        }
       }
     }
   }
