@@ -267,6 +267,7 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
     state.set_precision(args.precision)
     state.set_persistent(args.persistent)
     state.set_fused_refresh(args.fused_refresh)
+    state.set_run_ahead(args.run_ahead)
     state.set_mask(args.mask)
     if args.rule == "fixed":
         sel = binding.make_select(binding.SEL_FIXED_K, wl.tau, args.k)
@@ -426,6 +427,8 @@ def run_ours(args, wl: configs.Workload, rank: int, world: int, local_rank: int)
             else "one launch per kernel",
             "refresh": "fused with the step after it (one forward)" if args.fused_refresh
             else "separate forward, then the step",
+            "host_loop": "a block's next step enqueued before the current step's commits are read" if args.run_ahead
+            else "every step's commits read before the next launch",
             "l2": "inputs larger than L2 (every step streams all weights)",
             "parallelism": f"replicas x{world} (no data-path collective)",
         },
@@ -545,6 +548,8 @@ def main():
                     help="one launch per kernel instead of the persistent DualCache step")
     ap.add_argument("--no-fused-refresh", dest="fused_refresh", action="store_false",
                     help="run every refresh (and block-causal commit forward) apart from the step after it")
+    ap.add_argument("--no-run-ahead", dest="run_ahead", action="store_false",
+                    help="read every step's commits back before launching the next step")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
     import dataclasses

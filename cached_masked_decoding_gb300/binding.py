@@ -96,6 +96,7 @@ SIGNATURES = {
     "dllm_state_set_precision": (_I32, [_P, _I32]),
     "dllm_state_set_persistent": (_I32, [_P, _I32]),
     "dllm_state_set_fused_refresh": (_I32, [_P, _I32]),
+    "dllm_state_set_run_ahead": (_I32, [_P, _I32]),
     "dllm_state_set_mask": (_I32, [_P, _I32]),
     "dllm_state_set_step_timeline": (_I32, [_P, _I32]),
     "dllm_read_step_timeline": (_I32, [_P, _P, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
@@ -294,6 +295,9 @@ class State:
 
     def set_fused_refresh(self, on: bool):
         check(lib().dllm_state_set_fused_refresh(self.h, 1 if on else 0))
+
+    def set_run_ahead(self, on: bool):
+        check(lib().dllm_state_set_run_ahead(self.h, 1 if on else 0))
 
     def set_mask(self, mask: str):
         check(lib().dllm_state_set_mask(self.h, {"full": 0, "block_causal": 1}[mask]))

@@ -570,7 +570,7 @@ struct dllm_state {
   float* attn_ml = nullptr;
   int* attn_cnt = nullptr;
   float2* rope = nullptr;
-  int32_t* host_ce = nullptr;     // pinned copy of count_err
+  int32_t* host_ce = nullptr;     // pinned copies of count_err: two slots of b + 1 (steps in flight at once)
   CUtensorMap tm_kv;
   std::map<std::tuple<const void*, int, int, int>, CUtensorMap> act_maps;
   std::map<const void*, CUtensorMap> kv64_maps;   // 64-key K/V maps of the tensor-core attention, per cache buffer
@@ -591,7 +591,10 @@ struct dllm_state {
   double kt_ms[KC_N] = {0};
   long long kt_n[KC_N] = {0};
   double kt_bytes[KC_N] = {0};
-  cudaEvent_t ev_a = nullptr, ev_b = nullptr;
+  cudaEvent_t ev_a = nullptr, ev_b = nullptr;   // step or refresh timing (host slot 0)
+  cudaEvent_t ev_c = nullptr, ev_d = nullptr;   // step timing (host slot 1)
+  cudaEvent_t ev_done[2] = {nullptr, nullptr};  // a host slot's counts have landed
+  bool run_ahead = true;          // dllm_run launches a block's next step before reading the current one's commits
   long long launches = 0;         // kernels launched by this state
   // persistent DualCache step (one cooperative launch per step)
   bool persistent = true;
@@ -635,8 +638,8 @@ dllm_status state_free_device(dllm_state* s) {
   if (s->x_save) cudaFree(s->x_save);
   if (s->row_cos) cudaFree(s->row_cos);
   for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
-  if (s->ev_a) cudaEventDestroy(s->ev_a);
-  if (s->ev_b) cudaEventDestroy(s->ev_b);
+  for (cudaEvent_t e : {s->ev_a, s->ev_b, s->ev_c, s->ev_d, s->ev_done[0], s->ev_done[1]})
+    if (e) cudaEventDestroy(e);
   if (s->own_stream && s->st) cudaStreamDestroy(s->st);
   s->arena = nullptr;
   s->gemm_ws = nullptr;
@@ -812,12 +815,15 @@ extern "C" dllm_status dllm_state_create(dllm_model* m, const int32_t* prompts, 
     }
     s->own_stream = true;
   }
-  if (cudaMallocHost((void**)&s->host_ce, (b + 1) * 4) != cudaSuccess) {
+  if (cudaMallocHost((void**)&s->host_ce, 2 * (b + 1) * 4) != cudaSuccess) {
     cudaGetLastError();
     set_error("cudaMallocHost failed");
     return fail(DLLM_ENOMEM);
   }
-  if (cudaEventCreate(&s->ev_a) != cudaSuccess || cudaEventCreate(&s->ev_b) != cudaSuccess) {
+  if (cudaEventCreate(&s->ev_a) != cudaSuccess || cudaEventCreate(&s->ev_b) != cudaSuccess ||
+      cudaEventCreate(&s->ev_c) != cudaSuccess || cudaEventCreate(&s->ev_d) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s->ev_done[0], cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s->ev_done[1], cudaEventDisableTiming) != cudaSuccess) {
     set_error("cudaEventCreate failed");
     return fail(DLLM_ECUDA);
   }
@@ -1557,7 +1563,7 @@ bool use_persistent(const dllm_state* s, int kind, int j) {
 
 // One denoise step of block j as a single cooperative launch: DualCache, or
 // (block-causal) block j-1's commit forward with block j's first step.
-dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule, int kind) {
+dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule, int kind, bool skip_done = false) {
   if (!s->step_built || s->step_split != s->split) CKS(build_step(s));
   const dllm_model* m = s->m;
   const dllm_config& c = m->cfg;
@@ -1622,6 +1628,7 @@ dllm_status run_step_persistent(dllm_state* s, int j, const SelectRule& rule, in
   a.merge.seq_done = s->seq_done;
   a.merge.rule = rule;
   a.prefetch = s->step_prefetch;
+  a.skip_done = skip_done ? 1 : 0;
   if (s->timeline) {
     const size_t tl_bytes = (size_t)s->m->sms * s->n_phases * kTimelineSlots * 8;
     if (!s->d_timeline) CKS(dev_alloc((void**)&s->d_timeline, tl_bytes));
@@ -1682,8 +1689,13 @@ dllm_status do_refresh(dllm_state* s, cudaEvent_t e0 = nullptr, cudaEvent_t e1 =
 
 // commit_prev (block-causal runs, dllm_run): block j-1's commit forward runs
 // in the same persistent launch as this step (the caller checked it fits).
-dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int32_t* committed, int* total,
-                    cudaEvent_t e0 = nullptr, cudaEvent_t e1 = nullptr, bool commit_prev = false) {
+// Enqueue one denoise step of block j on the state's stream without waiting
+// for it: its counts and error word are copied to host slot `slot`, and
+// ev_done[slot] is recorded after them.  skip_done: the step is launched
+// before the previous step's counts were read (a persistent DualCache step
+// only); it does nothing when block j no longer holds a MASK.
+dllm_status step_enqueue(dllm_state* s, int j, const SelectRule& rule, int mode, bool commit_prev, bool skip_done,
+                         int slot, cudaEvent_t e0, cudaEvent_t e1) {
   if (j < 0 || j >= s->n_blocks) {
     set_error("block_idx %d outside [0, %d)", j, s->n_blocks);
     return DLLM_EINVAL;
@@ -1704,23 +1716,43 @@ dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int3
     row0 = 0;
     R = s->T;
   }
-  if (e0) CK(cudaEventRecord(e0, s->st));
-  CK(cudaMemsetAsync(s->count_err, 0, (s->b + 1) * 4, s->st));
   const int kind = commit_prev ? SK_COMMIT : mode == DLLM_CACHE_DUAL ? SK_DUAL : -1;
   if (commit_prev && !use_persistent(s, SK_COMMIT, j)) {
     set_error("block %d: the fused commit forward does not fit one launch", j);
     return DLLM_EINVAL;
   }
-  if (kind >= 0 && use_persistent(s, kind, j)) {
-    CKS(run_step_persistent(s, j, rule, kind));
+  const bool persistent = kind >= 0 && use_persistent(s, kind, j);
+  if (skip_done && (kind != SK_DUAL || !persistent)) {
+    set_error("block %d: only a persistent DualCache step can be launched ahead", j);
+    return DLLM_EINVAL;
+  }
+  if (e0) CK(cudaEventRecord(e0, s->st));
+  CK(cudaMemsetAsync(s->count_err, 0, (s->b + 1) * 4, s->st));
+  if (persistent) {
+    CKS(run_step_persistent(s, j, rule, kind, skip_done));
   } else {
     CKS(run_forward(s, row0, R, false, blk, rule));
   }
   if (e1) CK(cudaEventRecord(e1, s->st));
-  CKS(finish_sync(s));
+  CK(cudaMemcpyAsync(s->host_ce + (size_t)slot * (s->b + 1), s->count_err, (s->b + 1) * 4, cudaMemcpyDeviceToHost,
+                     s->st));
+  CK(cudaEventRecord(s->ev_done[slot], s->st));
+  return DLLM_OK;
+}
+
+// Wait for the step whose counts go to host slot `slot` and apply them to
+// block j's MASK counts.
+dllm_status step_collect(dllm_state* s, int j, const SelectRule& rule, int slot, int32_t* committed, int* total) {
+  CK(cudaEventSynchronize(s->ev_done[slot]));
+  if (s->timing) collect_timing(s);
+  const int32_t* ce = s->host_ce + (size_t)slot * (s->b + 1);
+  if (ce[s->b] != 0) {
+    set_error("a kernel gave up a bounded wait (site %d); outputs are invalid", ce[s->b]);
+    return DLLM_ETIMEOUT;
+  }
   int sum = 0;
   for (int i = 0; i < s->b; ++i) {
-    const int cnt = s->host_ce[i];
+    const int cnt = ce[i];
     int& rem = s->remaining[(size_t)i * s->n_blocks + j];
     // every rule commits at least one MASK of the block per step, except the
     // scheduled one, which may commit none while more steps are left
@@ -1734,6 +1766,12 @@ dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int3
   }
   *total = sum;
   return DLLM_OK;
+}
+
+dllm_status do_step(dllm_state* s, int j, const SelectRule& rule, int mode, int32_t* committed, int* total,
+                    cudaEvent_t e0 = nullptr, cudaEvent_t e1 = nullptr, bool commit_prev = false) {
+  CKS(step_enqueue(s, j, rule, mode, commit_prev, false, 0, e0, e1));
+  return step_collect(s, j, rule, 0, committed, total);
 }
 
 }  // namespace
@@ -1837,9 +1875,30 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
     CKS(timed_refresh());
     return notify(DLLM_EVENT_REFRESH, j, spb);
   };
+  // Run-ahead: a block's next plain DualCache step is enqueued before the
+  // current step's commits are read back, so that the GPU does not idle for
+  // the host's round trip between steps.  When the current step finishes the
+  // block, the step launched ahead finds no MASK in it and ends at once.
+  // Off while a hook, per-kernel timing, the phase timeline or the trace
+  // observe the run step by step; the trajectory is the same either way.
+  const bool ahead_ok = s->run_ahead && !s->hook && !s->timing && !s->timeline && !s->trace &&
+                        cache_mode == DLLM_CACHE_DUAL;
+  auto rule_at = [&](int spb) {
+    SelectRule rs = r;
+    if (r.policy == 4) rs.k = std::max(1, r.k - spb);   // steps left in this block
+    return rs;
+  };
+  // an error with a step still in flight: let it finish before returning
+  auto drained = [&](dllm_status st) {
+    if (st != DLLM_OK) cudaStreamSynchronize(s->st);
+    return st;
+  };
+  cudaEvent_t ev0[2] = {s->ev_a, s->ev_c}, ev1[2] = {s->ev_b, s->ev_d};
   if (cached && s->n_blocks > 0) CKS(refresh_before_step(0, 0));
   for (int j = 0; j < s->n_blocks; ++j) {
     int spb = 0;
+    int cur = 0;          // host slot of the step collected next
+    bool ahead = false;   // step spb is already enqueued (launched ahead)
     for (;;) {
       int any = 0, act = 0;
       for (int i = 0; i < s->b; ++i) {
@@ -1847,20 +1906,38 @@ extern "C" dllm_status dllm_run(dllm_state* s, const dllm_select* sel, int32_t c
         any |= rem > 0;
         act += rem > 0;
       }
-      if (!any) break;
-      if (cached && refresh_interval > 0 && spb > 0 && spb % refresh_interval == 0) CKS(refresh_before_step(j, spb));
+      if (!any) {
+        if (ahead) {   // launched ahead of the block's last step: it found no MASK and did nothing
+          int none = 0;
+          CKS(drained(step_collect(s, j, rule_at(spb), cur, cnt.data(), &none)));
+        }
+        break;
+      }
+      const SelectRule rs = rule_at(spb);
+      bool fused_step = false, commit_step = false;
+      if (ahead) {
+        ahead = false;   // a plain step, enqueued by the previous round
+      } else {
+        if (cached && refresh_interval > 0 && spb > 0 && spb % refresh_interval == 0) CKS(refresh_before_step(j, spb));
+        fused_step = pending;
+        commit_step = pending_commit;
+        s->fused_fwd = fused_step;
+        const dllm_status st = step_enqueue(s, j, rs, fused_step ? (int)DLLM_CACHE_NONE : cache_mode, commit_step,
+                                            false, cur, ev0[cur], ev1[cur]);
+        s->fused_fwd = false;
+        CKS(drained(st));
+      }
+      const int nx = spb + 1;
+      if (ahead_ok && !(cached && refresh_interval > 0 && nx % refresh_interval == 0) &&
+          use_persistent(s, SK_DUAL, j)) {
+        CKS(drained(step_enqueue(s, j, rule_at(nx), cache_mode, false, true, cur ^ 1, ev0[cur ^ 1], ev1[cur ^ 1])));
+        ahead = true;
+      }
       int total = 0;
-      SelectRule rs = r;
-      if (r.policy == 4) rs.k = std::max(1, r.k - spb);   // steps left in this block
-      const bool fused_step = pending;
-      const bool commit_step = pending_commit;
-      s->fused_fwd = fused_step;
-      const dllm_status st = do_step(s, j, rs, fused_step ? (int)DLLM_CACHE_NONE : cache_mode, cnt.data(), &total,
-                                     s->ev_a, s->ev_b, commit_step);
-      s->fused_fwd = false;
-      CKS(st);
+      CKS(drained(step_collect(s, j, rs, cur, cnt.data(), &total)));
       float ms = 0;
-      CK(cudaEventElapsedTime(&ms, s->ev_a, s->ev_b));
+      CK(cudaEventElapsedTime(&ms, ev0[cur], ev1[cur]));
+      if (ahead) cur ^= 1;
       if (fused_step || commit_step) {
         refresh_ms += ms;
         ++refreshes;
@@ -2042,6 +2119,15 @@ extern "C" dllm_status dllm_state_set_fused_refresh(dllm_state* s, int32_t enabl
     return DLLM_EINVAL;
   }
   s->fuse_refresh = enable != 0;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_state_set_run_ahead(dllm_state* s, int32_t enable) {
+  if (!s) {
+    set_error("NULL state");
+    return DLLM_EINVAL;
+  }
+  s->run_ahead = enable != 0;
   return DLLM_OK;
 }
 

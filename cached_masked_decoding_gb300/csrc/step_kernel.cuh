@@ -84,6 +84,7 @@ struct StepArgs {
   MergeParams merge;
   unsigned long long* timeline;  // optional [grid][n_phases][kTimelineSlots] (diagnostics), or null
   int prefetch;                  // weight tiles loaded ahead of a phase's barrier (<= ring depth)
+  int skip_done;                 // 1: do nothing when the block [merge.blk_start, + merge.B) of every sequence holds no MASK
 };
 
 template <int BN, int HD>
@@ -280,6 +281,18 @@ template <int BN, int HD>
 __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
   using C = StepCfg<BN, HD>;
   constexpr int STAGES = C::STAGES;
+  if (a.skip_done) {
+    // launched before the host saw the previous step's commits: if that step
+    // finished the block there is nothing to denoise, and the launch ends
+    // here, before any write (every CTA reaches the same answer)
+    const int n = a.attn.b * a.merge.B;
+    int masked = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int sq = i / a.merge.B, c = i - sq * a.merge.B;
+      masked |= a.merge.x[(long long)sq * a.merge.T + a.merge.blk_start + c] == a.merge.mask_id;
+    }
+    if (!__syncthreads_or(masked)) return;
+  }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;                                        // STAGES weight tiles

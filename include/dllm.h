@@ -280,6 +280,20 @@ dllm_status dllm_state_set_persistent(dllm_state* s, int32_t enable);
  * kernels' rounding. */
 dllm_status dllm_state_set_fused_refresh(dllm_state* s, int32_t enable);
 
+/* Run-ahead in dllm_run (enable 1, the default): within a block, the next
+ * DualCache step that runs as one persistent launch is enqueued before the
+ * current step's commit counts are read back, so the GPU does not wait for
+ * the host between steps (Algorithm 1's inner loop, section 3 of the
+ * Fast-dLLM reading notes, decides whether the block still holds a MASK only
+ * after each step).  When the current step commits the block's last MASK,
+ * the step launched ahead finds none at its start and ends without writing
+ * anything; it is counted in kernel_launches, not in steps.  Tokens, steps
+ * and refreshes are the same as with enable 0.  Run-ahead is off while a
+ * run hook, per-kernel timing, the step timeline or the trace is set, and
+ * for PrefixCache and no-cache runs, refresh-interval steps and steps that
+ * do not fit one persistent launch. */
+dllm_status dllm_state_set_run_ahead(dllm_state* s, int32_t enable);
+
 /* Attention mask.  DLLM_MASK_BIDIRECTIONAL (default): every position sees
  * every position, the Fast-dLLM setting, in which the cached prefix and
  * suffix go stale and a block-boundary refresh recomputes them.

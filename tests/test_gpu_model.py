@@ -236,6 +236,41 @@ def test_run_is_deterministic_and_generate_agrees(gmodel):
     assert stats["steps"] == outs[0][3]["steps"] and stats["tau_bar"] > 0
 
 
+@pytest.mark.parametrize("mask", ["full", "block_causal"])
+@pytest.mark.parametrize("rule", ["threshold", "schedule"])
+def test_run_ahead_takes_the_same_trajectory(gmodel, mask, rule):
+    """dllm_run with run-ahead (a block's next step enqueued before the
+    current step's commits are read back) decodes exactly what the loop that
+    reads every step's commits first decodes: the same canvas, confidences,
+    steps and refreshes (same kernels, same inputs).  The only difference is
+    at most one extra launch per block: the step launched ahead of a block's
+    last step, which finds no MASK and does nothing."""
+    P, gen, B, b = 32, 64, 16, 2
+    pr = synth.prompts(CFG, 5, b, P)
+    sel = (binding.make_select(binding.SEL_THRESHOLD, 0.9) if rule == "threshold"
+           else binding.make_select(binding.SEL_SCHEDULE, k=8))
+    outs = []
+    for ahead in (False, True):
+        st = binding.State(gmodel, pr, b, P, gen, B)
+        if mask != "full":
+            st.set_mask(mask)
+        st.set_run_ahead(ahead)
+        stats = st.run(sel, "dual")
+        outs.append((st.read(), stats))
+        st.free()
+    (t0, c0, a0), s0 = outs[0]
+    (t1, c1, a1), s1 = outs[1]
+    np.testing.assert_array_equal(t0, t1)
+    np.testing.assert_array_equal(c0, c1)
+    np.testing.assert_array_equal(a0, a1)
+    assert (t1[:, P:] != CFG.mask_id).all()
+    for k in ("steps", "refreshes", "committed", "fused_steps", "max_steps_per_block"):
+        assert s0[k] == s1[k], k
+    assert s0["tau_bar"] == s1["tau_bar"]
+    n_blocks = gen // B
+    assert s0["kernel_launches"] <= s1["kernel_launches"] <= s0["kernel_launches"] + n_blocks
+
+
 def test_refresh_every_step_equals_no_cache_on_gpu(gmodel, omodel):
     """Invariant (iv) of the cached decoders: refreshing before every step makes
     DualCache read exactly the K/V a no-cache forward computes.  dllm_run with
