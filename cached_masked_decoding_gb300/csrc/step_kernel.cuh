@@ -402,24 +402,36 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
         // activation columns [64k, 64k+64) come from unit k >> dep_shift; the
         // last unit found complete is remembered within a run of chunks, and
         // once the whole producing phase is seen complete nothing is polled
-        int ready_unit = -1;
+        // units [ready_lo, ready_hi] are known complete.  A look reads the
+        // unit a chunk needs and the next three together (one round trip):
+        // the chunks of a segment visit the units in ascending order
+        int ready_lo = 0, ready_hi = -1;
         bool all_ready = false;
         const int* src_done = a.flags + P.src_done;
         const int src_need = P.src_need;
+        const int last_unit = dep_shift >= 31 ? 0 : (kc - 1) >> dep_shift;
         auto dep_ready = [&](int k) -> bool {
           if (all_ready) return true;
           const int unit = k >> dep_shift;
-          if (unit == ready_unit) return true;
+          if (unit >= ready_lo && unit <= ready_hi) return true;
           const int vd = ld_relaxed_gpu(src_done);
-          const int vu = ld_relaxed_gpu(dep + unit);
+          int vu[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) vu[j] = unit + j <= last_unit ? ld_relaxed_gpu(dep + unit + j) : 0;
+          int hi = unit;
           if (vd >= src_need) {
             all_ready = true;
-          } else if (vu < dep_need) {
+          } else if (vu[0] < dep_need) {
             if (!flag_wait(dep + unit, dep_need, abort_flag, a.err)) return false;
-            ready_unit = unit;
+            ready_lo = ready_hi = unit;
             return true;
+          } else {
+#pragma unroll
+            for (int j = 1; j < 4; ++j)
+              if (hi == unit + j - 1 && unit + j <= last_unit && vu[j] >= dep_need) hi = unit + j;
           }
-          ready_unit = unit;
+          ready_lo = unit;
+          ready_hi = hi;
           asm volatile("fence.acq_rel.gpu;" ::: "memory");
           asm volatile("fence.proxy.async.global;" ::: "memory");
           return true;
