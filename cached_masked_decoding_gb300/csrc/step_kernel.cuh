@@ -399,12 +399,12 @@ __global__ void __launch_bounds__(192, 1) step_kernel(const StepArgs a) {
           }
           if (!ok) break;
         }
-        // activation columns [64k, 64k+64) come from unit k >> dep_shift; the
-        // last unit found complete is remembered within a run of chunks, and
-        // once the whole producing phase is seen complete nothing is polled
-        // units [ready_lo, ready_hi] are known complete.  A look reads the
-        // unit a chunk needs and the next three together (one round trip):
-        // the chunks of a segment visit the units in ascending order
+        // activation columns [64k, 64k+64) come from unit k >> dep_shift.
+        // Units [ready_lo, ready_hi] are known complete; a look reads the
+        // flags of the unit a chunk needs and of the next three together (one
+        // round trip: the chunks of a segment visit the units in ascending
+        // order), and once the whole producing phase is seen complete nothing
+        // is polled
         int ready_lo = 0, ready_hi = -1;
         bool all_ready = false;
         const int* src_done = a.flags + P.src_done;
