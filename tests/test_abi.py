@@ -59,6 +59,9 @@ def test_host_side_errors_without_gpu_work():
     assert L.dllm_load(b"/nonexistent/weights.bin", ctypes.byref(h)) == binding.EIO
     assert L.dllm_prefill_refresh(None) == binding.EINVAL
     assert L.dllm_denoise_step(None, 0, 0.9, 2, None) == -binding.EINVAL
+    # state switches on a NULL state
+    for fn in (L.dllm_state_set_run_ahead, L.dllm_state_set_fused_refresh):
+        assert fn(None, 1) == binding.EINVAL
     # the single-kernel attention entries reject bad shapes and unaligned pointers before any launch
     for fn in (L.dllm_op_attention, L.dllm_op_attention_tc, L.dllm_op_attention_noalloc):
         assert fn(None, None, None, None, 1, 1, 128, 1, 1, None) == binding.EINVAL
